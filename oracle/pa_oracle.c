@@ -1,0 +1,257 @@
+/*
+ * pa_oracle.c -- plain, slow, fp64 CPU oracle for paged-KV decode attention
+ * and the KV-append (reshape-and-cache) step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, table or helper with the CUDA path; the two meet only in the
+ * seeded input generator, which holds none of the arithmetic below.
+ *
+ * What it computes (sources are the three web pages the method is described
+ * on; each page is cited by its title and section):
+ *
+ *  - Dense causal attention, "LLM 推理优化的系统视角", section 3.1 (KV Cache:
+ *    what it reuses): O_t = softmax(Q_t K_{1:t}^T / sqrt(d_h)) V_{1:t}.
+ *  - Blockwise (paged) attention equals that dense attention over the
+ *    physical blocks concatenated in logical order: "每生成一个字都要把全部权重
+ *    读一遍：从 vLLM 看 LLM 推理提速", section "KV Cache 又大又碎，为何不用操作
+ *    系统分页的思路管它？", the equation s_j = q^T K_j / sqrt(d_k),
+ *    o = sum_j softmax(s)_j V_j and the figure caption after it (physical
+ *    placement does not change the result).  The oracle therefore first
+ *    concatenates each sequence's blocks in logical order (walking its block
+ *    table) and then runs the dense definition; there is no blocking, no
+ *    online softmax and no split.
+ *  - Block table: same page, same section (the per-request table mapping
+ *    logical blocks to physical blocks, block size 16).
+ *  - Query heads share K/V heads in contiguous groups (GQA): "LLM 推理优化的
+ *    系统视角", section 3.2 (MHA / MQA / GQA list) and section 4.1.
+ *  - Decode step reads the cached K/V and appends the new position's K/V:
+ *    "LLM 推理优化的系统视角", section 3.1 (decode-step state change).  The
+ *    append is a byte copy of row t into slot slot_mapping[t], the slot
+ *    mapping being built in "prepare inputs" ("现代 LLM 推理引擎剖析", section
+ *    1.6, Forward Pass 内部).
+ *
+ * Readings where the pages are silent:
+ *  - context_lens[i] counts the tokens being decoded; the q_len query rows of
+ *    sequence i are its last q_len positions, and row j attends positions
+ *    0 .. L_i - q_len + j (causal inside the chunk).
+ *  - kv head of query head h is h / (num_heads / num_kv_heads).
+ *  - pool layout [num_blocks, block_size, num_kv_heads, head_dim], head_dim
+ *    fastest; slot = physical_block * block_size + offset; slot < 0 = skip.
+ *  - 16-bit storage: bf16 or IEEE fp16 bit patterns, widened exactly to fp64.
+ *
+ * PLANT: when compiled with -DPLANT=n (n > 0) one deliberate mistake is
+ * planted, so that the test suite can show that its pins catch it.  The
+ * product oracle is built with PLANT undefined.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef PLANT
+#define PLANT 0
+#endif
+
+enum { ORACLE_BF16 = 0, ORACLE_FP16 = 1 };
+
+/* Exact widening of one 16-bit storage value to fp64. */
+double oracle_bits_to_double(uint16_t bits, int dtype)
+{
+    if (dtype == ORACLE_BF16) {
+        /* bf16 is the top half of an IEEE binary32 value. */
+        uint32_t u = (uint32_t)bits << 16;
+        float f;
+        memcpy(&f, &u, sizeof f);
+        return (double)f;
+    }
+    /* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+    int sign = (bits >> 15) & 1;
+    int expo = (bits >> 10) & 0x1f;
+    int frac = bits & 0x3ff;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)frac, -24);                 /* zero / subnormal */
+    } else if (expo == 31) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + frac), expo - 25);  /* (1 + frac/1024) * 2^(expo-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* Vector form, used by the tests to pin the widening against library casts. */
+void oracle_bits_to_double_vec(const uint16_t* bits, int64_t n, int dtype, double* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_bits_to_double(bits[i], dtype);
+}
+
+/*
+ * Gather sequence i's K (or V) in logical order: token p lives in physical
+ * block block_table[p / block_size] at offset p % block_size.
+ * dst: [L, num_kv_heads, head_dim] fp64.  Returns 0, or -1 if a block id used
+ * by the sequence is outside [0, num_blocks).
+ */
+static int gather_sequence(const uint16_t* cache, const int32_t* table, int L,
+                           int num_kv_heads, int head_dim, int block_size,
+                           int64_t num_blocks, int dtype, double* dst)
+{
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int p = 0; p < L; ++p) {
+        int32_t blk = table[p / block_size];
+        int off = p % block_size;
+#if PLANT == 4
+        off = block_size - 1 - off;                   /* planted: offset reversed in block */
+#endif
+        if (blk < 0 || (int64_t)blk >= num_blocks) return -1;
+        const uint16_t* src = cache + ((int64_t)blk * block_size + off) * row;
+        for (int64_t e = 0; e < row; ++e) dst[(int64_t)p * row + e] = oracle_bits_to_double(src[e], dtype);
+    }
+    return 0;
+}
+
+/*
+ * Paged decode attention, fp64.
+ *   out          [num_seqs, q_len, num_heads, head_dim] fp64 (written)
+ *   query        [num_seqs, q_len, num_heads, head_dim] 16-bit
+ *   key_cache    [num_blocks, block_size, num_kv_heads, head_dim] 16-bit
+ *   value_cache  same as key_cache
+ *   block_tables [num_seqs, max_blocks_per_seq] int32
+ *   context_lens [num_seqs] int32 (includes the q_len positions being decoded)
+ * Sequences whose length is < q_len, or whose block table points outside the
+ * pool, get NaN outputs; the return value counts them.
+ * num_threads <= 0 uses the OpenMP default.
+ */
+int oracle_decode_attention(double* out, const uint16_t* query,
+                            const uint16_t* key_cache, const uint16_t* value_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int num_seqs, int q_len,
+                            int num_heads, int num_kv_heads, int head_dim,
+                            int block_size, int64_t num_blocks, double scale,
+                            int dtype, int num_threads)
+{
+    const int group = num_heads / num_kv_heads;
+    int bad = 0;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+    (void)num_threads;
+#endif
+
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+    for (int i = 0; i < num_seqs; ++i) {
+        const int L = context_lens[i];
+        double* o_seq = out + (int64_t)i * q_len * num_heads * head_dim;
+        int ok = (L >= q_len && L >= 1 && head_dim <= 1024 &&
+                  (L + block_size - 1) / block_size <= max_blocks_per_seq);
+        double *K = NULL, *V = NULL, *s = NULL;
+        if (ok) {
+            const int64_t n = (int64_t)L * num_kv_heads * head_dim;
+            K = (double*)malloc(sizeof(double) * n);
+            V = (double*)malloc(sizeof(double) * n);
+            s = (double*)malloc(sizeof(double) * L);
+            const int32_t* table = block_tables + (int64_t)i * max_blocks_per_seq;
+            /* Step 1: concatenate the physical blocks in logical order. */
+            ok = K && V && s &&
+                 gather_sequence(key_cache, table, L, num_kv_heads, head_dim, block_size, num_blocks, dtype, K) == 0 &&
+                 gather_sequence(value_cache, table, L, num_kv_heads, head_dim, block_size, num_blocks, dtype, V) == 0;
+#if PLANT == 7
+            if (ok) memcpy(V, K, sizeof(double) * n);      /* planted: V read from the K cache */
+#endif
+        }
+        if (!ok) {
+            for (int64_t e = 0; e < (int64_t)q_len * num_heads * head_dim; ++e) o_seq[e] = NAN;
+            bad += 1;
+            free(K); free(V); free(s);
+            continue;
+        }
+        /* Step 2: dense causal attention for every query row and head. */
+        for (int j = 0; j < q_len; ++j) {
+            int last = L - q_len + j;                         /* last position row j may attend */
+#if PLANT == 3
+            last = last - 1 < 0 ? 0 : last - 1;               /* planted: causal limit off by one */
+#elif PLANT == 6
+            last = L - 1 - j;                                 /* planted: chunk rows reversed */
+#endif
+            for (int h = 0; h < num_heads; ++h) {
+                int kvh = h / group;
+#if PLANT == 2
+                kvh = h % num_kv_heads;                       /* planted: interleaved head groups */
+#endif
+                const uint16_t* qrow = query + (((int64_t)i * q_len + j) * num_heads + h) * head_dim;
+                double* o = o_seq + ((int64_t)j * num_heads + h) * head_dim;
+                double qd[1024];
+                double sc = scale;
+#if PLANT == 1
+                sc = 1.0;                                     /* planted: scale dropped */
+#endif
+                for (int k = 0; k < head_dim; ++k) qd[k] = oracle_bits_to_double(qrow[k], dtype);
+                /* scores s_p = scale * q . K_p for p = 0 .. last */
+                double m = -INFINITY;
+                for (int p = 0; p <= last; ++p) {
+                    const double* kp = K + ((int64_t)p * num_kv_heads + kvh) * head_dim;
+                    double dot = 0.0;
+                    for (int k = 0; k < head_dim; ++k) dot += qd[k] * kp[k];
+                    s[p] = sc * dot;
+                    if (s[p] > m) m = s[p];
+                }
+                /* softmax weights and the weighted sum of V rows */
+                double den = 0.0;
+                for (int p = 0; p <= last; ++p) {
+                    s[p] = exp(s[p] - m);
+#if PLANT == 5
+                    if (p == last && last > 0) continue;      /* planted: last weight left out of the sum */
+#endif
+                    den += s[p];
+                }
+                for (int k = 0; k < head_dim; ++k) o[k] = 0.0;
+                for (int p = 0; p <= last; ++p) {
+                    const double* vp = V + ((int64_t)p * num_kv_heads + kvh) * head_dim;
+                    for (int k = 0; k < head_dim; ++k) o[k] += s[p] * vp[k];
+                }
+                for (int k = 0; k < head_dim; ++k) o[k] /= den;
+            }
+        }
+        free(K); free(V); free(s);
+    }
+    return bad;
+}
+
+/*
+ * KV append: for each new token t with slot_mapping[t] >= 0, copy its
+ * [num_kv_heads, head_dim] K row and V row byte for byte into
+ * cache[slot / block_size, slot % block_size].  Returns the number of tokens
+ * whose slot lies beyond the pool (those are not written).
+ */
+int oracle_reshape_and_cache(const uint16_t* key, const uint16_t* value,
+                             uint16_t* key_cache, uint16_t* value_cache,
+                             const int64_t* slot_mapping, int64_t num_tokens,
+                             int num_kv_heads, int head_dim, int block_size,
+                             int64_t num_blocks)
+{
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    int bad = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;                              /* padding token: nothing to write */
+        if (slot >= num_blocks * block_size) { ++bad; continue; }
+        int64_t blk = slot / block_size, off = slot % block_size;
+        uint16_t* kd = key_cache + (blk * block_size + off) * row;
+        uint16_t* vd = value_cache + (blk * block_size + off) * row;
+        memcpy(kd, key + t * row, sizeof(uint16_t) * row);
+        memcpy(vd, value + t * row, sizeof(uint16_t) * row);
+    }
+    return bad;
+}
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

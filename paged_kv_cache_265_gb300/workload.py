@@ -1,0 +1,287 @@
+"""Seeded synthetic inputs for paged-KV decode attention.
+
+This module only draws random numbers and lays them out as the inputs of one
+decode step; it holds none of the attention arithmetic.  Both the CUDA path
+(through the tests and the benchmark) and the CPU oracle are fed from it.
+
+What one decode step looks like (the model-runner view of "现代 LLM 推理引擎剖析",
+section 1.6, and the decode-step state change of "LLM 推理优化的系统视角",
+section 3.1): every sequence already holds the K/V of its earlier positions in
+fixed 16-token blocks scattered through one pool, addressed by its block table;
+the step appends the K/V rows of its newest ``append_len`` positions through the
+slot mapping, and then its ``q_len`` query rows attend over all ``L_i``
+positions (``L_i`` counts the new ones).
+
+Recipe (the same for every workload):
+  * lengths are uniform integers over inclusive bounds;
+  * physical blocks come from a seeded shuffled free list, popped in sequence
+    order (shared-prefix blocks are popped first and mapped by every sequence);
+  * Q/K/V values are fp32 N(0, 1) draws rounded to bf16 or fp16 (round to
+    nearest even); a shared prefix has one set of values that every sharing
+    sequence sees;
+  * every pool slot that holds no token, including the last block's tail and
+    the slots the append is about to fill, holds a NaN bit pattern, so a read
+    of an unused slot cannot go unnoticed.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+
+BLOCK_SIZE = 16
+NAN_BITS = {"bf16": 0x7FC0, "fp16": 0x7E00}
+ELEM_BYTES = {"bf16": 2, "fp16": 2}
+
+_CHUNK = 1 << 22  # values drawn per RNG stream chunk (keeps draws independent of threading)
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    dtype: str
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    q_len: int
+    block_size: int
+    num_blocks: int
+    scale: float
+    context_lens: np.ndarray          # int32 [N]
+    block_tables: np.ndarray          # int32 [N, max_blocks_per_seq], -1 where unused
+    query: np.ndarray                 # uint16 [N, q_len, Hq, d]
+    key_cache: np.ndarray             # uint16 [NB, B, Hkv, d]  state before the append
+    value_cache: np.ndarray           # uint16 [NB, B, Hkv, d]
+    new_key: np.ndarray               # uint16 [T, Hkv, d]  rows the append writes
+    new_value: np.ndarray             # uint16 [T, Hkv, d]
+    slot_mapping: np.ndarray          # int64 [T]
+    logical_key: Optional[list] = None    # per sequence uint16 [L_i, Hkv, d] (small cases)
+    logical_value: Optional[list] = None
+    shared_prefix_blocks: int = 0
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.context_lens.shape[0])
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.num_seqs else 0
+
+    @property
+    def num_new_tokens(self) -> int:
+        return int(self.slot_mapping.shape[0])
+
+
+def _to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    """fp32 -> 16-bit storage bits, round to nearest even (library casts)."""
+    if dtype == "fp16":
+        return x.astype(np.float16).view(np.uint16)
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _normal_bits(seed_seq: np.random.SeedSequence, n: int, dtype: str) -> np.ndarray:
+    """n seeded N(0,1) values as 16-bit bits, drawn chunk by chunk from child streams."""
+    out = np.empty(n, dtype=np.uint16)
+    nchunks = max(1, math.ceil(n / _CHUNK))
+    children = seed_seq.spawn(nchunks)
+    for c, child in enumerate(children):
+        lo, hi = c * _CHUNK, min(n, (c + 1) * _CHUNK)
+        if hi <= lo:
+            break
+        g = np.random.Generator(np.random.PCG64(child))
+        out[lo:hi] = _to_bits(g.standard_normal(hi - lo, dtype=np.float32), dtype)
+    return out
+
+
+def make_workload(name: str, context_lens: Sequence[int], *, num_heads: int, num_kv_heads: int,
+                  head_dim: int, dtype: str = "bf16", q_len: int = 1, append_len: Optional[int] = None,
+                  num_blocks: Optional[int] = None, seed: int = 0, shared_prefix_blocks: int = 0,
+                  max_blocks_per_seq: Optional[int] = None, keep_logical: bool = False,
+                  scale: Optional[float] = None, block_size: int = BLOCK_SIZE) -> Workload:
+    """Build one decode step's inputs.
+
+    ``append_len`` (default ``q_len``) newest positions of every sequence are
+    left out of the pool and returned as rows for the append step.
+    ``shared_prefix_blocks`` > 0 maps the first that many logical blocks of
+    every sequence onto the same physical blocks (read-only sharing).
+    """
+    assert dtype in ("bf16", "fp16")
+    lens = np.asarray(context_lens, dtype=np.int64)
+    n = int(lens.shape[0])
+    append_len = q_len if append_len is None else append_len
+    assert np.all(lens >= max(1, q_len, append_len)), "every sequence needs L >= q_len, append_len"
+    hkv, d, bs = num_kv_heads, head_dim, block_size
+    nblk = (lens + bs - 1) // bs
+    if shared_prefix_blocks:
+        assert np.all(lens >= shared_prefix_blocks * bs + append_len), "append must land after the prefix"
+    private = nblk - shared_prefix_blocks
+    need = int(shared_prefix_blocks + private.sum())
+    if num_blocks is None:
+        num_blocks = need
+    assert need <= num_blocks, f"pool of {num_blocks} blocks cannot hold {need}"
+    mbps = int(max_blocks_per_seq if max_blocks_per_seq is not None else max(1, int(nblk.max(initial=1))))
+    assert mbps >= int(nblk.max(initial=0))
+
+    ss = np.random.SeedSequence(seed)
+    s_place, s_q, s_k, s_v = ss.spawn(4)
+
+    # Physical placement: a shuffled free list, popped in sequence order.
+    free = np.random.Generator(np.random.PCG64(s_place)).permutation(num_blocks).astype(np.int32)
+    shared_ids = free[:shared_prefix_blocks]
+    pos = shared_prefix_blocks
+    block_tables = np.full((n, mbps), -1, dtype=np.int32)
+    for i in range(n):
+        block_tables[i, :shared_prefix_blocks] = shared_ids
+        k = int(private[i])
+        block_tables[i, shared_prefix_blocks:shared_prefix_blocks + k] = free[pos:pos + k]
+        pos += k
+
+    row = hkv * d
+    # Token contents.  Shared-prefix tokens are drawn once; every other token once per sequence.
+    shared_tok = shared_prefix_blocks * bs
+    priv_tok = lens - shared_tok
+    total_priv = int(priv_tok.sum())
+    k_shared = _normal_bits(s_k.spawn(1)[0], shared_tok * row, dtype).reshape(shared_tok, hkv, d)
+    v_shared = _normal_bits(s_v.spawn(1)[0], shared_tok * row, dtype).reshape(shared_tok, hkv, d)
+    k_priv = _normal_bits(s_k, total_priv * row, dtype).reshape(total_priv, hkv, d)
+    v_priv = _normal_bits(s_v, total_priv * row, dtype).reshape(total_priv, hkv, d)
+    query = _normal_bits(s_q, n * q_len * num_heads * d, dtype).reshape(n, q_len, num_heads, d)
+
+    # Destination row (block * B + offset) of every logical token, in sequence order.
+    seq_of_priv = np.repeat(np.arange(n), priv_tok)
+    starts = np.concatenate([[0], np.cumsum(priv_tok)[:-1]]) if n else np.zeros(0, np.int64)
+    p_priv = np.arange(total_priv, dtype=np.int64) - np.repeat(starts, priv_tok) + shared_tok
+    dest_priv = block_tables[seq_of_priv, p_priv // bs].astype(np.int64) * bs + p_priv % bs
+    is_new = p_priv >= np.repeat(lens, priv_tok) - append_len
+
+    sentinel = NAN_BITS[dtype]
+    key_cache = np.full((num_blocks * bs, hkv, d), sentinel, dtype=np.uint16)
+    value_cache = np.full((num_blocks * bs, hkv, d), sentinel, dtype=np.uint16)
+    if shared_tok:
+        p_sh = np.arange(shared_tok, dtype=np.int64)
+        dest_sh = shared_ids[p_sh // bs].astype(np.int64) * bs + p_sh % bs
+        key_cache[dest_sh] = k_shared
+        value_cache[dest_sh] = v_shared
+    old = ~is_new
+    key_cache[dest_priv[old]] = k_priv[old]
+    value_cache[dest_priv[old]] = v_priv[old]
+
+    new_key = np.ascontiguousarray(k_priv[is_new])
+    new_value = np.ascontiguousarray(v_priv[is_new])
+    slot_mapping = dest_priv[is_new].astype(np.int64)
+
+    logical_key = logical_value = None
+    if keep_logical:
+        logical_key, logical_value = [], []
+        for i in range(n):
+            a, b = int(starts[i]), int(starts[i] + priv_tok[i])
+            logical_key.append(np.concatenate([k_shared, k_priv[a:b]]))
+            logical_value.append(np.concatenate([v_shared, v_priv[a:b]]))
+
+    return Workload(
+        name=name, dtype=dtype, num_heads=num_heads, num_kv_heads=hkv, head_dim=d, q_len=q_len,
+        block_size=bs, num_blocks=num_blocks,
+        scale=float(scale if scale is not None else 1.0 / math.sqrt(d)),
+        context_lens=lens.astype(np.int32), block_tables=block_tables, query=query,
+        key_cache=key_cache.reshape(num_blocks, bs, hkv, d),
+        value_cache=value_cache.reshape(num_blocks, bs, hkv, d),
+        new_key=new_key, new_value=new_value, slot_mapping=slot_mapping,
+        logical_key=logical_key, logical_value=logical_value,
+        shared_prefix_blocks=shared_prefix_blocks)
+
+
+# ---------------------------------------------------------------------------
+# The five named decode workloads.  Seeds are 2650 + the workload number.
+# ---------------------------------------------------------------------------
+
+def _uniform_lens(seed: int, n: int, lo: int, hi: int) -> np.ndarray:
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 7])))
+    return g.integers(lo, hi + 1, size=n)
+
+
+def tiny_mha(**kw) -> Workload:
+    """4 sequences, L = {1, 17, 33, 100}, 4 heads MHA, d = 64, bf16, 64-block pool."""
+    return make_workload("tiny_mha_d64", [1, 17, 33, 100], num_heads=4, num_kv_heads=4, head_dim=64,
+                         dtype="bf16", q_len=1, num_blocks=64, seed=2651, max_blocks_per_seq=8, **kw)
+
+
+def opt13b_mha(**kw) -> Workload:
+    """32 sequences, L ~ U[512, 2048], 40 heads MHA, d = 128, fp16, 8192-block pool."""
+    lens = _uniform_lens(2652, 32, 512, 2048)
+    return make_workload("opt13b_mha_fp16", lens, num_heads=40, num_kv_heads=40, head_dim=128,
+                         dtype="fp16", q_len=1, num_blocks=8192, seed=2652, max_blocks_per_seq=128, **kw)
+
+
+def gqa_batch128(**kw) -> Workload:
+    """128 sequences, L ~ U[1, 4096], GQA 32q/8kv, d = 128, bf16, 40000-block pool."""
+    lens = _uniform_lens(2653, 128, 1, 4096)
+    return make_workload("gqa_batch128", lens, num_heads=32, num_kv_heads=8, head_dim=128,
+                         dtype="bf16", q_len=1, num_blocks=40000, seed=2653, max_blocks_per_seq=256, **kw)
+
+
+def shared_prefix_verify(**kw) -> Workload:
+    """64 sequences sharing a 1024-token prefix (64 blocks) + U[16, 512] private tokens;
+    5 query rows per sequence (4 drafts + 1), causal inside the chunk; GQA 32/8, d = 128."""
+    suffix = _uniform_lens(2654, 64, 16, 512)
+    return make_workload("shared_prefix_spec5", 1024 + suffix, num_heads=32, num_kv_heads=8,
+                         head_dim=128, dtype="bf16", q_len=5, num_blocks=4096, seed=2654,
+                         shared_prefix_blocks=64, max_blocks_per_seq=96, **kw)
+
+
+def long_context_skewed(**kw) -> Workload:
+    """16 sequences L ~ U[16384, 32768] + 240 sequences L ~ U[64, 1024], shuffled;
+    GQA 64q/8kv, d = 128, bf16, 65536-block pool."""
+    long_ = _uniform_lens(2655, 16, 16384, 32768)
+    short = _uniform_lens(2655 + 100, 240, 64, 1024)
+    lens = np.concatenate([long_, short])
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([2655, 11])))
+    lens = lens[g.permutation(lens.shape[0])]
+    return make_workload("long_context_skewed", lens, num_heads=64, num_kv_heads=8, head_dim=128,
+                         dtype="bf16", q_len=1, num_blocks=65536, seed=2655, max_blocks_per_seq=2048, **kw)
+
+
+WORKLOADS = {
+    1: tiny_mha,
+    2: opt13b_mha,
+    3: gqa_batch128,
+    4: shared_prefix_verify,
+    5: long_context_skewed,
+}
+
+
+def kv_bytes_per_token(num_layers: int, num_kv_heads: int, head_dim: int, elem_bytes: int) -> int:
+    """Logical KV bytes one token occupies: 2 (K and V) x layers x kv heads x head dim x bytes.
+
+    The formula of "LLM 推理优化的系统视角", section 3.2."""
+    return 2 * num_layers * num_kv_heads * head_dim * elem_bytes
+
+
+def block_bytes(block_size: int, num_kv_heads: int, head_size: int, elem_bytes: int) -> int:
+    """Bytes of one KV block of one layer: 2 x block_size x kv heads x head size x bytes.
+
+    The formula of "现代 LLM 推理引擎剖析", section 1.3."""
+    return 2 * block_size * num_kv_heads * head_size * elem_bytes
+
+
+def attention_bytes(w: Workload) -> int:
+    """Algorithmic HBM bytes of one decode-attention pass: each sequence's K and V rows
+    (all L_i positions, every kv head) once, plus Q read and O written once."""
+    e = ELEM_BYTES[w.dtype]
+    kv = int(w.context_lens.astype(np.int64).sum()) * kv_bytes_per_token(1, w.num_kv_heads, w.head_dim, e)
+    qo = 2 * w.num_seqs * w.q_len * w.num_heads * w.head_dim * e
+    return kv + qo
+
+
+def append_bytes(w: Workload) -> int:
+    """Algorithmic bytes of the KV append: each new K and V row read once and written once."""
+    e = ELEM_BYTES[w.dtype]
+    return 2 * w.num_new_tokens * kv_bytes_per_token(1, w.num_kv_heads, w.head_dim, e)

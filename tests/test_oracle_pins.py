@@ -1,0 +1,31 @@
+"""The oracle against its pins (CPU only), and each planted mistake against the pins."""
+import pytest
+
+import oracle
+import oracle_pins as P
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load()
+
+
+@pytest.mark.parametrize("pin", P.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(orc, pin):
+    pin(orc)
+
+
+# Each build plants one plausible mistake in the oracle (see the PLANT notes in
+# pa_oracle.c): 1 scale dropped, 2 interleaved head groups, 3 causal limit off
+# by one, 4 offsets reversed inside a block, 5 a softmax term left out of the
+# denominator, 6 chunk rows reversed, 7 V read from the K cache.
+@pytest.mark.parametrize("plant", [1, 2, 3, 4, 5, 6, 7])
+def test_planted_mistake_is_caught(plant):
+    bad = oracle.load(plant)
+    caught = []
+    for pin in P.ALL_PINS:
+        try:
+            pin(bad)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"planted mistake {plant} slipped past every pin"
