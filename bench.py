@@ -1,0 +1,439 @@
+"""Benchmark of one paged decode step on GB300: the KV append of every sequence's
+new token plus decode attention over the paged pool, through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload gqa_batch128|tiny_mha|opt13b_mha|shared_prefix|long_context]
+
+Prints ONE JSON line (rank 0).  A step is one pass of the whole hot path over
+the workload's batch: reshape_and_cache (append of the new K/V rows) + decode
+attention (plan, partition and merge kernels).  `value` is achieved HBM GB/s of
+the step's algorithmic bytes (each sequence's K and V rows once, Q and O once,
+the appended rows read and written once) with inputs resident in HBM;
+`seq_tokens_per_s` is sum(context_lens) per second.  Under torchrun every rank
+runs its own copy of the batch (weak scaling; sequences are independent, no
+collective on the data path) and rank 0 reports the max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle on the host cores on bounded samples
+of the same workload (the only baseline the pages allow: they ship no code).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_265_gb300 import workload as W  # noqa: E402
+
+METRIC = "paged decode attention: achieved HBM GB/s vs peak; seq-tokens/s per layer"
+WORKLOADS = {
+    "tiny_mha": 1,
+    "opt13b_mha": 2,
+    "gqa_batch128": 3,
+    "shared_prefix": 4,
+    "long_context": 5,
+}
+DESCR = {
+    1: "tiny_mha_d64: 4 seqs L={1,17,33,100}, MHA 4 heads, d=64, bf16, block 16, 64-block pool, 4-row append",
+    2: "opt13b_mha_fp16: 32 seqs L~U[512,2048], MHA 40 heads, d=128, fp16, block 16, 8192-block pool, 32-row append",
+    3: "gqa_batch128: 128 seqs L~U[1,4096], GQA 32q/8kv, d=128, bf16, block 16, 40000-block pool, 128-row append",
+    4: "shared_prefix_spec5: 64 seqs = 1024-token shared prefix + U[16,512], 5 query rows causal, GQA 32q/8kv, "
+       "d=128, bf16, 4096-block pool, 320-row append",
+    5: "long_context_skewed: 16 seqs L~U[16384,32768] + 240 seqs L~U[64,1024], GQA 64q/8kv, d=128, bf16, "
+       "65536-block pool, 256-row append",
+}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_265_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch of the partition kernel from the committed ncu summary, if the
+    summary was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_kernel_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch_full")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 8]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        busy = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_time(w: W.Workload, seq_idx: np.ndarray, threads: int, pools=None):
+    """One oracle step (append + attention) over the chosen sequences; returns (seconds, bytes, seq_tokens)."""
+    import oracle
+
+    orc = oracle.load()
+    kc, vc = pools if pools is not None else (w.key_cache.copy(), w.value_cache.copy())
+    per_seq = w.num_new_tokens // max(1, w.num_seqs)      # new rows are grouped by sequence, in order
+    rows = (np.asarray(seq_idx)[:, None] * per_seq + np.arange(per_seq)[None, :]).ravel()
+    sub = W.Workload(**{**w.__dict__, "context_lens": w.context_lens[seq_idx], "block_tables": w.block_tables[seq_idx],
+                        "query": np.ascontiguousarray(w.query[seq_idx]),
+                        "new_key": np.ascontiguousarray(w.new_key[rows]),
+                        "new_value": np.ascontiguousarray(w.new_value[rows]),
+                        "slot_mapping": np.ascontiguousarray(w.slot_mapping[rows])})
+    t0 = time.perf_counter()
+    orc.reshape_and_cache(sub.new_key, sub.new_value, kc, vc, sub.slot_mapping)
+    _, bad = orc.decode_attention(sub.query, kc, vc, sub.block_tables, sub.context_lens, sub.scale, sub.dtype,
+                                  num_threads=threads)
+    dt = time.perf_counter() - t0
+    assert bad == 0
+    nbytes = W.attention_bytes(sub) + W.append_bytes(sub)
+    return dt, nbytes, int(sub.context_lens.astype(np.int64).sum())
+
+
+def cpu_baseline(w: W.Workload, budget_s: float = 12.0):
+    """The oracle as it stands on all host cores, on a bounded sample of the workload."""
+    import oracle
+
+    threads = oracle.load().max_threads()
+    pools = (w.key_cache.copy(), w.value_cache.copy())
+    n = w.num_seqs
+    # grow the sample (whole sequences, in batch order) until it takes >= 1 s, then repeat to fill the budget
+    k = max(1, min(n, 8))
+    while True:
+        dt, nbytes, toks = oracle_time(w, np.arange(k), threads, pools)
+        if dt >= 1.0 or k == n:
+            break
+        k = min(n, k * 2)
+    reps, tot_t, tot_b, tot_tok = 1, dt, nbytes, toks
+    while tot_t < budget_s:
+        dt, nbytes, toks = oracle_time(w, np.arange(k), threads, pools)
+        reps += 1
+        tot_t += dt
+        tot_b += nbytes
+        tot_tok += toks
+    return {"value": tot_b / tot_t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "seq_tokens_per_s": tot_tok / tot_t,
+            "sample": f"first {k} of {n} sequences (append + attention), {reps} repetitions, {tot_t:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    cfg = WORKLOADS[args.workload]
+    w = W.WORKLOADS[cfg]()
+    import oracle
+
+    threads = oracle.load().max_threads()
+    pools = (w.key_cache.copy(), w.value_cache.copy())
+    # size each step's sample so warmup + steps fit in about two minutes
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    order = np.arange(w.num_seqs)
+    dt1, _, _ = oracle_time(w, order[:1], threads, pools)
+    k = int(max(1, min(w.num_seqs, per_step / max(dt1, 1e-4))))
+    for _ in range(args.warmup):
+        oracle_time(w, order[:k], threads, pools)
+    tt, tb, ttok = 0.0, 0, 0
+    for s in range(args.steps):
+        sel = np.roll(order, -s * k)[:k]
+        dt, nb, tok = oracle_time(w, np.sort(sel), threads, pools)
+        tt += dt
+        tb += nb
+        ttok += tok
+    value = tb / tt / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": tt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": DESCR[cfg], "sample_seqs_per_step": k},
+            "seq_tokens_per_s": ttok / tt,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{k} of {w.num_seqs} sequences per step (append + attention)"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    from paged_kv_cache_265_gb300 import build as B
+    from paged_kv_cache_265_gb300 import pa
+
+    if rank == 0 or world == 1:
+        B.build()
+    barrier(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = WORKLOADS[args.workload]
+    w = W.WORKLOADS[cfg]()
+    tdt = {"bf16": torch.bfloat16, "fp16": torch.float16}[w.dtype]
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(tdt)
+
+    kc, vc = up(w.key_cache), up(w.value_cache)
+    nk, nv = up(w.new_key), up(w.new_value)
+    q = up(w.query)
+    out = torch.empty_like(q)
+    sm = torch.from_numpy(w.slot_mapping).to(dev)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    ws = pa.alloc_workspace(w.num_seqs, w.q_len, w.num_heads, w.head_dim, w.max_context_len, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    pa.get_device_error(clear=True)
+
+    def step():
+        pa.reshape_and_cache(nk, nv, kc, vc, sm, stream=stream)
+        n1 = pa.last_launch_count()
+        pa.decode_attention(out, q, kc, vc, bt, cl, w.scale, w.max_context_len, ws, stream=stream)
+        return n1 + pa.last_launch_count()
+
+    for _ in range(max(3, args.warmup)):
+        launches_per_step = step()
+    torch.cuda.synchronize(dev)
+
+    attn_bytes = W.attention_bytes(w)
+    step_bytes = attn_bytes + W.append_bytes(w)
+    seq_tokens = int(w.context_lens.astype(np.int64).sum())
+    flush = None
+    if step_bytes < 2 * L2_BYTES:   # small working set: flush L2 between steps
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+    # --- device-resident timed region
+    pa.profile_enable(True)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush_ms = 0.0
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for _ in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    pa.profile_enable(False)
+    kern_ms_total, kern_n = pa.profile_read()
+    total_ms = start.elapsed_time(stop)
+    if flush is not None:
+        fs, fe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fs.record(stream)
+        for _ in range(args.steps):
+            flush.zero_()
+        fe.record(stream)
+        torch.cuda.synchronize(dev)
+        flush_ms = fs.elapsed_time(fe)
+    step_ms_local = max(1e-9, (total_ms - flush_ms) / args.steps)
+    step_ms = max_over_ranks(step_ms_local, world, dev)
+    err = pa.get_device_error(clear=True)
+
+    # --- end to end through the public API: host inputs in, host output back, every step
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    h_q, h_nk, h_nv = pin(q), pin(nk), pin(nv)
+    h_sm, h_bt, h_cl = pin(sm), pin(bt), pin(cl)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_nk, h_nv, h_sm, h_bt, h_cl))
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_steps = max(1, min(args.steps, 200))
+
+    def e2e_step():
+        q.copy_(h_q, non_blocking=True)
+        nk.copy_(h_nk, non_blocking=True)
+        nv.copy_(h_nv, non_blocking=True)
+        sm.copy_(h_sm, non_blocking=True)
+        bt.copy_(h_bt, non_blocking=True)
+        cl.copy_(h_cl, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    es.record(stream)
+    for _ in range(e2e_steps):
+        if flush is not None:
+            flush.zero_()
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks((es.elapsed_time(ee) - flush_ms * e2e_steps / max(1, args.steps)) / e2e_steps,
+                            world, dev)
+
+    total_bytes = sum_over_ranks(step_bytes, world, dev)
+    total_tokens = sum_over_ranks(seq_tokens, world, dev)
+    if rank != 0:
+        return
+    peak, peak_kind = peaks()
+    kern_ms = kern_ms_total / max(1, kern_n)
+    achieved = attn_bytes / (kern_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": total_bytes / (step_ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": DESCR[cfg], "seq_tokens_per_step": seq_tokens, "bytes_per_step": step_bytes,
+                   "attention_bytes": attn_bytes, "partition_tokens": 512,
+                   "l2": "flushed between steps" if flush is not None else
+                   f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step vs 129 MB L2)",
+                   "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
+        "seq_tokens_per_s": total_tokens / (step_ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",
+                     "kernel": "decode_kernel (partition pass)", "kernel_ms": kern_ms,
+                     "traffic": traffic},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "device_error_flags": err,
+        "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa_batch128")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged-KV decode-attention library (libpa.so).
+ *
+ * The library implements one decode step's hot path of a PagedAttention-style
+ * serving engine:
+ *   1. the KV append ("reshape and cache"): the newest positions' K/V rows are
+ *      written into their slots of the paged pool;
+ *   2. decode attention: every sequence's query rows attend over the K/V of all
+ *      its positions, which live in fixed 16-token blocks scattered through the
+ *      pool and are found through the sequence's block table.
+ *
+ * Sources (three web pages; cited by title and section):
+ *   [P1] "每生成一个字都要把全部权重读一遍：从 vLLM 看 LLM 推理提速", section
+ *        "KV Cache 又大又碎，为何不用操作系统分页的思路管它？": fixed-size blocks in
+ *        one pool, the block table (logical -> physical block), block size 16,
+ *        blockwise attention s_j = q^T K_j / sqrt(d_k), o = sum_j softmax(s)_j V_j,
+ *        equal to attention over the blocks concatenated in logical order;
+ *        read-only sharing of one physical block by several sequences.
+ *   [P2] "现代 LLM 推理引擎剖析", section 1.3 (KV cache manager, block layout
+ *        2 x block_size x num_kv_heads x head_size x dtype bytes per layer) and
+ *        section 1.6 (prepare inputs builds the slot mapping; forward runs the
+ *        paged attention kernel).
+ *   [P3] "LLM 推理优化的系统视角", section 3.1 (dense causal attention
+ *        O_t = softmax(Q_t K_{1:t}^T / sqrt(d_h)) V_{1:t}; a decode step reads the
+ *        cache and appends the new position's K/V) and section 3.2 (MHA / MQA /
+ *        GQA: groups of query heads share one K/V head).
+ *   Speculative verification of gamma draft tokens plus one (P1, section
+ *   "对症下药": the large model checks gamma + 1 positions in one forward) is the
+ *   multi-query entry point below.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers, owned by the caller, C-contiguous,
+ *     16-byte aligned.  The library never allocates device memory, never frees
+ *     caller memory and never synchronises the stream (pa_get_device_error and
+ *     pa_profile_read are the documented exceptions: they wait for the stream).
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = the
+ *     legacy default stream) of the current device.
+ *   - 16-bit element types: PA_BF16 (bfloat16) or PA_FP16 (IEEE binary16).
+ *     Arithmetic is fp32 inside the kernels; outputs are rounded once (round to
+ *     nearest even) to the input type.
+ *   - Pool layout: key_cache and value_cache are separate tensors, each
+ *     [num_blocks, block_size, num_kv_heads, head_dim] with head_dim fastest.
+ *     Token p of sequence i is at block block_tables[i][p / 16], offset p % 16.
+ *   - Query head h uses kv head h / (num_heads / num_kv_heads).
+ *   - context_lens[i] counts every position of sequence i INCLUDING the q_len
+ *     positions being decoded (their K/V must already be appended).
+ *   - Supported: head_dim 64 or 128; block_size 16;
+ *     (num_heads / num_kv_heads) * q_len <= 64.
+ *   - Host-side argument errors return a status and enqueue nothing.  Device
+ *     contents (block ids, lengths, slots) are checked inside the kernels: a
+ *     bad value sets a bit in the library's device error word (see
+ *     pa_get_device_error) and the offending read or write is skipped; the
+ *     kernels never trap.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_BF16 = 0, PA_FP16 = 1 } pa_dtype;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, inconsistent sizes */
+    PA_ERR_UNSUPPORTED = 2,   /* head_dim, block_size or group x q_len outside what is compiled */
+    PA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than pa_decode_workspace_size() */
+    PA_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
+} pa_status;
+
+/* Bits of the device error word. */
+#define PA_DEVERR_BLOCK_ID 0x1  /* a block-table entry in use lies outside [0, num_blocks) */
+#define PA_DEVERR_CONTEXT  0x2  /* context_lens[i] < q_len, < 1, > max_context_len or beyond the table */
+#define PA_DEVERR_SLOT     0x4  /* slot_mapping[t] >= num_blocks * block_size */
+#define PA_DEVERR_TIMEOUT  0x8  /* a bounded wait inside a kernel gave up (internal error) */
+
+#define PA_BLOCK_SIZE 16
+#define PA_DEFAULT_PARTITION 512  /* tokens per split-K partition */
+
+/*
+ * KV append ([P3] section 3.1, decode-step state change; slot mapping from [P2]
+ * section 1.6).  For every new token t with slot = slot_mapping[t] >= 0:
+ *   key_cache  [slot / block_size, slot % block_size, :, :] = key  [t, :, :]
+ *   value_cache[slot / block_size, slot % block_size, :, :] = value[t, :, :]
+ * a byte-exact copy.  Negative slots are padding and write nothing; slots
+ * >= num_blocks * block_size set PA_DEVERR_SLOT and write nothing.
+ *   key, value   [num_tokens, num_kv_heads, head_dim], read
+ *   key_cache,   [num_blocks, block_size, num_kv_heads, head_dim], written
+ *   value_cache
+ *   slot_mapping [num_tokens] int64, read
+ * num_tokens == 0 is a no-op.
+ */
+int pa_reshape_and_cache(const void* key, const void* value, void* key_cache, void* value_cache,
+                         const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int64_t num_blocks, int dtype, void* stream);
+
+/*
+ * Bytes of device workspace pa_decode_attention* needs for these sizes and the
+ * default partition (PA_DEFAULT_PARTITION tokens).  The workspace holds the
+ * per-call work list and the split-K partials (fp32 m, l and unnormalised o
+ * per partition); it needs no initialisation and may be reused by every call
+ * on the same stream.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int q_len, int num_heads, int head_dim,
+                                int max_context_len);
+
+/* Same, for an explicit partition size in tokens (a positive multiple of 16). */
+size_t pa_decode_workspace_size_ex(int num_seqs, int q_len, int num_heads, int head_dim,
+                                   int max_context_len, int partition_size);
+
+/*
+ * Paged decode attention, one query token per sequence ([P1] blockwise
+ * attention; [P3] section 3.1 dense definition it equals; [P3] section 3.2
+ * GQA).  For sequence i, query head h, kv head g = h / (num_heads/num_kv_heads),
+ * L = context_lens[i]:
+ *   out[i, h, :] = sum_p softmax_p(scale * q[i, h, :] . K_i[p, g, :]) V_i[p, g, :],
+ *   p = 0 .. L-1,
+ * where K_i / V_i are the sequence's blocks in logical order.
+ *   out          [num_seqs, num_heads, head_dim], written
+ *   query        [num_seqs, num_heads, head_dim], read
+ *   key_cache,   [num_blocks, 16, num_kv_heads, head_dim], read
+ *   value_cache
+ *   block_tables [num_seqs, max_blocks_per_seq] int32, read; entries past
+ *                ceil(L/16) are never read
+ *   context_lens [num_seqs] int32, read; each in [1, max_context_len]
+ *   max_context_len  an upper bound of every context_lens[i] (sizes the workspace)
+ *   workspace    device scratch of at least pa_decode_workspace_size() bytes
+ * Sequences longer than one partition are split into PA_DEFAULT_PARTITION-token
+ * partitions whose fp32 partial results are merged by their log-sum-exp.
+ * Sequences with invalid lengths leave their output rows unwritten and set
+ * PA_DEVERR_CONTEXT.
+ */
+int pa_decode_attention(void* out, const void* query, const void* key_cache, const void* value_cache,
+                        const int32_t* block_tables, int max_blocks_per_seq,
+                        const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                        int head_dim, int block_size, int64_t num_blocks, int max_context_len,
+                        float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Multi-query decode attention: q_len query rows per sequence (gamma draft
+ * tokens + 1 for speculative verification, or a prefill chunk), causal inside
+ * the chunk.  Row j of sequence i is position L - q_len + j and attends
+ * positions 0 .. L - q_len + j.
+ *   out, query [num_seqs, q_len, num_heads, head_dim]
+ * Everything else as pa_decode_attention; each context_lens[i] must be >= q_len.
+ */
+int pa_decode_attention_multiquery(void* out, const void* query, const void* key_cache,
+                                   const void* value_cache, const int32_t* block_tables,
+                                   int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                                   int q_len, int num_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int64_t num_blocks, int max_context_len,
+                                   float scale, int dtype, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/*
+ * General form of the two calls above with an explicit split-K partition size
+ * (tokens, a positive multiple of 16; 0 = PA_DEFAULT_PARTITION).  A partition
+ * size >= max_context_len computes every sequence in one piece (no merge).
+ * The workspace must be sized with pa_decode_workspace_size_ex() for the same
+ * partition size.  Results agree with the default within fp32 rounding.
+ */
+int pa_decode_attention_ex(void* out, const void* query, const void* key_cache, const void* value_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int num_seqs, int q_len, int num_heads,
+                           int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                           int max_context_len, float scale, int dtype, int partition_size,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* pa_status_string(int status);
+
+/*
+ * Reads (and, if clear != 0, resets) the current device's error word after
+ * waiting for `stream`.  *host_flags receives an OR of PA_DEVERR_* bits.
+ */
+int pa_get_device_error(int32_t* host_flags, int clear, void* stream);
+
+/*
+ * Timing hook for benchmarks.  pa_profile_enable(1) makes every following
+ * decode call record a CUDA event pair around its main (partition) kernel on
+ * the call's stream (up to 4096 pairs); pa_profile_read() waits for the
+ * recorded events, returns the summed milliseconds and the launch count, and
+ * clears the record.  pa_profile_enable(0) stops recording.
+ */
+int pa_profile_enable(int on);
+int pa_profile_read(float* total_ms, int* launches);
+
+/* Number of kernel launches the last decode call on this thread enqueued. */
+int pa_last_launch_count(void);
+
+/* Library ABI version (major * 100 + minor). */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

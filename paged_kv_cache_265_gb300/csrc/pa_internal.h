@@ -1,0 +1,83 @@
+// pa_internal.h -- host-side contract between the C ABI (pa_api.cpp) and the
+// kernel launchers (pa_kernels.cu).  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Workspace of one decode call (byte offsets from the workspace base).
+//   header      int32[64]: [0] = number of (sequence, partition) work entries
+//   part_start  int32[N+1]: first partial slot of each sequence (exclusive scan)
+//   units       int2[N * Pmax]: work entries (sequence, partition), full
+//               partitions first, then each sequence's shorter last partition
+//   pml         float2[slots, q_len, Hq]: per-partition (max, sum) in log2 units
+//   pacc        float[slots, q_len, Hq, D]: per-partition unnormalised outputs
+struct WsLayout {
+    size_t header, part_start, units, pml, pacc, total;
+    int pmax;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(int num_seqs, int q_len, int num_heads, int head_dim, int max_context_len,
+                          int partition) {
+    WsLayout w{};
+    int pmax = (max_context_len + partition - 1) / partition;
+    if (pmax < 1) pmax = 1;
+    const size_t n = num_seqs > 0 ? (size_t)num_seqs : 0;
+    const size_t slots = n * (size_t)pmax;
+    size_t off = 0;
+    w.header = off;
+    off += 256;
+    w.part_start = off;
+    off += align256(4 * (n + 1));
+    w.units = off;
+    off += align256(8 * slots);
+    w.pml = w.pacc = off;
+    if (pmax > 1) {
+        w.pml = off;
+        off += align256(8 * slots * (size_t)q_len * (size_t)num_heads);
+        w.pacc = off;
+        off += align256(4 * slots * (size_t)q_len * (size_t)num_heads * (size_t)head_dim);
+    }
+    w.total = off;
+    w.pmax = pmax;
+    return w;
+}
+
+struct DecodeArgs {
+    void* out;
+    const void* query;
+    const void* key_cache;
+    const void* value_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    int max_blocks_per_seq;
+    int num_seqs;
+    int q_len;
+    int num_heads;
+    int num_kv_heads;
+    int head_dim;
+    int64_t num_blocks;
+    int max_context_len;
+    float scale;
+    int dtype;
+    int partition;
+    void* workspace;
+};
+
+// Launchers: return a pa_status; `launches` receives the number of kernels enqueued.
+int launch_reshape_and_cache(const void* key, const void* value, void* key_cache, void* value_cache,
+                             const int64_t* slot_mapping, int64_t num_tokens, int row_bytes,
+                             int64_t num_slots, cudaStream_t stream, int* launches);
+int launch_decode(const DecodeArgs& a, cudaStream_t stream, int* launches);
+int read_device_error(int32_t* flags, int clear, cudaStream_t stream);
+
+// Benchmark timing hook around the main decode kernel.
+int profile_enable(int on);
+int profile_read(float* total_ms, int* launches);
+
+}  // namespace pa

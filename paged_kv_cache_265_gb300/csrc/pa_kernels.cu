@@ -1,0 +1,870 @@
+// pa_kernels.cu -- sm_103a kernels of the paged-KV decode step and their launchers.
+//
+//   reshape_kernel  the KV append: copies each new token's [Hkv, D] K and V rows
+//                   into its slot (16-byte vector copies).
+//   plan_kernel     builds the work list of one decode call: (sequence,
+//                   partition) entries, full partitions first, and each
+//                   sequence's first partial slot.  One CTA; no host sync.
+//   decode_kernel   persistent; one CTA per (sequence, partition, kv head)
+//                   work unit at a time.  A producer warp streams the unit's
+//                   16-token K/V blocks (found through the block table) into a
+//                   ring of shared-memory stages with bulk copies completing on
+//                   mbarriers; four consumer warps compute the grouped-head
+//                   tile S = Q K^T and O += P V on the tensor cores
+//                   (mma.sync m16n8k16, fp32 accumulate) with an online softmax,
+//                   merge their partial states in shared memory and write either
+//                   the final output or the partition's fp32 partial.
+//   merge_kernel    merges the partitions of split sequences by log-sum-exp.
+//
+// The blockwise computation follows "每生成一个字都要把全部权重读一遍：从 vLLM 看 LLM
+// 推理提速", section on paged KV cache (s_j = q^T K_j / sqrt(d_k),
+// o = sum_j softmax(s)_j V_j over blocks in logical order), which equals the
+// dense causal attention of "LLM 推理优化的系统视角", section 3.1; the query-head
+// grouping is section 3.2 of the latter.  The online softmax is the tiling idea
+// named in its section 4.2 (execution order changes, semantics do not).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------------------
+// Device state owned by the library (module globals, not allocations).
+// ---------------------------------------------------------------------------
+__device__ int g_pa_error;                            // PA_DEVERR_* bits
+__device__ __align__(128) uint4 g_zero_rows[16 * 16];  // 16 rows x 256 B of zeros (never written)
+
+constexpr int kBlock = 16;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxStages = 8;
+
+// ---------------------------------------------------------------------------
+// KV append
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) reshape_kernel(const uint4* __restrict__ key,
+                                                      const uint4* __restrict__ value,
+                                                      uint4* __restrict__ key_cache,
+                                                      uint4* __restrict__ value_cache,
+                                                      const long long* __restrict__ slots,
+                                                      long long num_tokens, int row_vecs,
+                                                      long long num_slots) {
+    const long long per_token = 2LL * row_vecs;
+    const long long total = num_tokens * per_token;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long t = idx / per_token;
+        const int rem = (int)(idx - t * per_token);
+        const int which = rem >= row_vecs;  // 0 = K, 1 = V
+        const int v = rem - which * row_vecs;
+        const long long slot = __ldg(slots + t);
+        if (slot < 0) continue;  // padding token
+        if (slot >= num_slots) {
+            if (rem == 0) atomicOr(&g_pa_error, PA_DEVERR_SLOT);
+            continue;
+        }
+        const uint4* src = which ? value : key;
+        uint4* dst = which ? value_cache : key_cache;
+        dst[slot * row_vecs + v] = __ldg(src + t * row_vecs + v);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Work list
+// ---------------------------------------------------------------------------
+struct PlanParams {
+    const int* context_lens;
+    int* header;
+    int* part_start;
+    int2* units;
+    int num_seqs;
+    int q_len;
+    int partition;
+    int max_blocks_per_seq;
+    int max_context_len;
+};
+
+// Exclusive scan of v over the 1024-thread block; `total` receives the sum.
+__device__ int block_exclusive_scan(int v, int* scratch32, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch32[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = scratch32[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        scratch32[lane] = w;
+    }
+    __syncthreads();
+    const int before = warp ? scratch32[warp - 1] : 0;
+    total = scratch32[31];
+    __syncthreads();
+    return before + x - v;
+}
+
+__device__ __forceinline__ void seq_parts(const PlanParams& p, int i, int& full, int& partial) {
+    full = partial = 0;
+    if (i >= p.num_seqs) return;
+    const int L = p.context_lens[i];
+    const bool ok = L >= 1 && L >= p.q_len && L <= p.max_context_len &&
+                    (L + kBlock - 1) / kBlock <= p.max_blocks_per_seq;
+    if (!ok) {
+        atomicOr(&g_pa_error, PA_DEVERR_CONTEXT);
+        return;
+    }
+    full = L / p.partition;
+    partial = (L % p.partition) != 0;
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
+    __shared__ int scratch[32];
+    // Pass 1: number of full partitions (they go first in the list).
+    int total_full = 0;
+    for (int base = 0; base < p.num_seqs; base += 1024) {
+        int full, partial, tot;
+        seq_parts(p, base + threadIdx.x, full, partial);
+        block_exclusive_scan(full, scratch, tot);
+        total_full += tot;
+    }
+    // Pass 2: slots, full entries, partial entries.
+    int carry_slot = 0, carry_full = 0, carry_part = 0;
+    for (int base = 0; base < p.num_seqs; base += 1024) {
+        const int i = base + threadIdx.x;
+        int full, partial, t_slot, t_full, t_part;
+        seq_parts(p, i, full, partial);
+        const int slot = carry_slot + block_exclusive_scan(full + partial, scratch, t_slot);
+        const int fpos = carry_full + block_exclusive_scan(full, scratch, t_full);
+        const int ppos = carry_part + block_exclusive_scan(partial, scratch, t_part);
+        if (i < p.num_seqs) {
+            p.part_start[i] = slot;
+            for (int c = 0; c < full; ++c) p.units[fpos + c] = make_int2(i, c);
+            if (partial) p.units[total_full + ppos] = make_int2(i, full);
+        }
+        carry_slot += t_slot;
+        carry_full += t_full;
+        carry_part += t_part;
+    }
+    if (threadIdx.x == 0) {
+        p.part_start[p.num_seqs] = carry_slot;
+        p.header[0] = carry_full + carry_part;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Decode attention
+// ---------------------------------------------------------------------------
+struct DecodeParams {
+    void* out;
+    const void* query;
+    const void* key_cache;
+    const void* value_cache;
+    const int* block_tables;
+    const int* context_lens;
+    const int* header;
+    const int* part_start;
+    const int2* units;
+    float2* pml;
+    float* pacc;
+    long long num_blocks;
+    int max_blocks_per_seq;
+    int q_len;
+    int num_heads;
+    int num_kv_heads;
+    int group;         // query heads per kv head
+    int rows;          // group * q_len query rows per work unit
+    int partition;     // tokens per partition (multiple of 16)
+    int stages;        // ring length, a multiple of block_splits, <= kMaxStages
+    int mtiles;        // ceil(rows / 16) tensor-core row tiles
+    int block_splits;  // kConsumerWarps / mtiles warps share a tile's blocks
+    int slot_rows;     // min(16, rows): rows each warp leaves in the combine buffer
+    float scale_log2;  // scale * log2(e)
+};
+
+struct UnitInfo {
+    int seq, part, len, nparts, slot0, kvh, ntok, pad;
+};
+
+struct SmemLayout {
+    int pitch, stage_bytes, q_half_bytes;
+    int off_q, off_comb, off_m, off_l, off_bars, off_info, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int head_dim, int stages, int mtiles, int slot_rows) {
+    SmemLayout s;
+    s.pitch = head_dim * 2 + 16;  // 16 B of padding per row: conflict-free ldmatrix
+    s.stage_bytes = 2 * kBlock * s.pitch;
+    s.q_half_bytes = mtiles * 16 * s.pitch;
+    s.off_q = stages * s.stage_bytes;
+    s.off_comb = s.off_q + 2 * s.q_half_bytes;
+    s.off_m = s.off_comb + kConsumerWarps * slot_rows * head_dim * 4;
+    s.off_l = s.off_m + kConsumerWarps * 16 * 4;
+    s.off_bars = s.off_l + kConsumerWarps * 16 * 4;
+    s.off_info = s.off_bars + (2 * kMaxStages + 4) * 8;
+    s.total = s.off_info + 2 * (int)sizeof(UnitInfo) + 16;
+    return s;
+}
+
+// bar.red.or over the 128 consumer threads (named barrier 1): every thread
+// gets the OR of `v` across them.
+__device__ __forceinline__ bool consumers_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred q, r;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred r, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, r;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const SmemLayout lay = smem_layout(D, p.stages, p.mtiles, p.slot_rows);
+    const int pitch = lay.pitch;
+    constexpr int kRowBytes = D * 2;
+    uint8_t* stage_base = smem;
+    uint8_t* qbuf = smem + lay.off_q;
+    float* comb_o = reinterpret_cast<float*>(smem + lay.off_comb);
+    float* comb_m = reinterpret_cast<float*>(smem + lay.off_m);
+    float* comb_l = reinterpret_cast<float*>(smem + lay.off_l);
+    UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + lay.off_info);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(info + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t full0 = smem_addr(smem + lay.off_bars);
+    const uint32_t empty0 = full0 + 8 * kMaxStages;
+    const uint32_t qfull0 = empty0 + 8 * kMaxStages;
+    const uint32_t qempty0 = qfull0 + 16;
+    const int stages = p.stages;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, p.mtiles);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(qfull0 + 8 * b, 1);
+            mbar_init(qempty0 + 8 * b, kConsumerWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    // Query rows past `rows` in the last row tile must read as zeros.
+    for (int i = threadIdx.x; i < 2 * lay.q_half_bytes / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    const long long total_units = (long long)p.header[0] * p.num_kv_heads;
+
+    if (warp == kConsumerWarps) {
+        // ===================== producer warp =====================
+        const uint64_t pol_stream = l2_policy_evict_first();
+        const uint64_t pol_keep = l2_policy_evict_last();
+        const int blocks_per_part = p.partition / kBlock;
+        const long long kv_row = (long long)p.num_kv_heads * D;  // elements per token row of the pool
+        uint32_t k = 0;
+        int ul = 0;
+        bool ok = true;
+        for (long long u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++ul) {
+            const int e = (int)(u / p.num_kv_heads);
+            const int kvh = (int)(u - (long long)e * p.num_kv_heads);
+            const int2 sp = p.units[e];
+            const int L = p.context_lens[sp.x];
+            const int tok0 = sp.y * p.partition;
+            const int ntok = min(p.partition, L - tok0);
+            const int nblk = (ntok + kBlock - 1) / kBlock;
+            const int qb = ul & 1;
+            if (ul >= 2 &&
+                !__all_sync(0xffffffffu, mbar_wait(qempty0 + 8 * qb, ((ul - 2) >> 1) & 1, &g_pa_error, abort_flag))) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                UnitInfo ui;
+                ui.seq = sp.x;
+                ui.part = sp.y;
+                ui.len = L;
+                ui.nparts = (L + p.partition - 1) / p.partition;
+                ui.slot0 = p.part_start[sp.x];
+                ui.kvh = kvh;
+                ui.ntok = ntok;
+                ui.pad = 0;
+                info[qb] = ui;
+                mbar_arrive_expect_tx(qfull0 + 8 * qb, p.rows * kRowBytes);
+            }
+            __syncwarp();
+            for (int r = lane; r < p.rows; r += 32) {
+                const int qi = r / p.group, hg = r - qi * p.group;
+                const T* src = static_cast<const T*>(p.query) +
+                               ((long long)(sp.x * p.q_len + qi) * p.num_heads + kvh * p.group + hg) * D;
+                bulk_g2s(smem_addr(qbuf + qb * lay.q_half_bytes + r * pitch), src, kRowBytes,
+                         qfull0 + 8 * qb, pol_keep);
+            }
+            const int* bt = p.block_tables + (long long)sp.x * p.max_blocks_per_seq +
+                            (long long)sp.y * blocks_per_part;
+            for (int c = 0; c < nblk && ok; c += 32) {
+                const bool have = c + lane < nblk;
+                const int bid = have ? __ldg(bt + c + lane) : 0;
+                const bool bad = have && (bid < 0 || (long long)bid >= p.num_blocks);
+                if (bad) atomicOr(&g_pa_error, PA_DEVERR_BLOCK_ID);
+                const int cn = min(32, nblk - c);
+                for (int jj = 0; jj < cn; ++jj, ++k) {
+                    const int j = c + jj;
+                    const int s = (int)(k % stages);
+                    if (k >= (uint32_t)stages &&
+                        !__all_sync(0xffffffffu,
+                                    mbar_wait(empty0 + 8 * s, ((k / stages) - 1) & 1, &g_pa_error, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    const int b = __shfl_sync(0xffffffffu, bid, jj);
+                    const bool b_bad = __shfl_sync(0xffffffffu, (int)bad, jj) != 0;
+                    const int valid = b_bad ? 0 : min(kBlock, ntok - kBlock * j);
+                    if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * s, 2 * kBlock * kRowBytes);
+                    __syncwarp();
+                    // Lane r < 16 fetches K row r, lane 16 + r fetches V row r; rows past the
+                    // sequence's end (or of a rejected block) come from the zero buffer so the
+                    // P.V product never meets stale data.
+                    const int r = lane & 15;
+                    const bool is_v = lane >= 16;
+                    const void* src;
+                    if (r < valid) {
+                        const T* base = static_cast<const T*>(is_v ? p.value_cache : p.key_cache);
+                        src = base + ((long long)b * kBlock + r) * kv_row + (long long)kvh * D;
+                    } else {
+                        src = reinterpret_cast<const uint8_t*>(g_zero_rows) + r * kRowBytes;
+                    }
+                    uint8_t* dst = stage_base + s * lay.stage_bytes + (is_v ? kBlock * pitch : 0) + r * pitch;
+                    bulk_g2s(smem_addr(dst), src, kRowBytes, full0 + 8 * s, pol_stream);
+                }
+            }
+        }
+        // Never leave the CTA with bulk copies in flight: wait for the last fill of
+        // every stage and of both query buffers (immediate on the normal path).
+        for (int s = 0; s < stages; ++s) {
+            if (k > (uint32_t)s) {
+                const uint32_t last = s + ((k - 1 - s) / stages) * stages;
+                mbar_wait(full0 + 8 * s, (last / stages) & 1, &g_pa_error, nullptr);
+            }
+        }
+        for (int back = 1; back <= 2; ++back) {
+            const int u2 = ul - back;
+            if (u2 >= 0) mbar_wait(qfull0 + 8 * (u2 & 1), (u2 >> 1) & 1, &g_pa_error, nullptr);
+        }
+        return;
+    }
+
+    // ===================== consumer warps =====================
+    const int mt = warp / p.block_splits;  // row tile of this warp
+    const int bsg = warp % p.block_splits; // which of the tile's block-split warps
+    const int gid = lane >> 2, tig = lane & 3;
+    const int row_lo = mt * 16 + gid, row_hi = row_lo + 8;
+    const int rows_here = min(16, p.rows - mt * 16);
+    uint32_t k = 0;
+    int ul = 0;
+    for (long long u = blockIdx.x; u < total_units; u += gridDim.x, ++ul) {
+        const int qb = ul & 1;
+        // (all waits below are made warp-uniform: a timeout seen by one lane stops the warp)
+        bool ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8 * qb, (ul >> 1) & 1, &g_pa_error, abort_flag));
+        UnitInfo ui = info[qb];
+        uint32_t qa[D / 16][4];
+        float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+        float o[D / 8][4];
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        int nblk = 0;
+        if (ok) {
+            const uint8_t* qrow = qbuf + qb * lay.q_half_bytes + mt * 16 * pitch;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int rr = (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int cc = kk * 16 + (lane >> 4) * 8;
+                ldsm_x4(smem_addr(qrow + rr * pitch + cc * 2), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qempty0 + 8 * qb);
+
+            nblk = (ui.ntok + kBlock - 1) / kBlock;
+            const int tok0 = ui.part * p.partition;
+            // Last position (relative to the partition) each of this lane's two rows may see:
+            // row j of the q_len-row chunk is position L - q_len + j.
+            const int qi_lo = min(row_lo / p.group, p.q_len - 1);
+            const int qi_hi = min(row_hi / p.group, p.q_len - 1);
+            const int lim_lo = ui.len - p.q_len + qi_lo - tok0;
+            const int lim_hi = ui.len - p.q_len + qi_hi - tok0;
+            const int first = (bsg - (int)(k % p.block_splits) + p.block_splits) % p.block_splits;
+            for (int j = first; j < nblk; j += p.block_splits) {
+                const uint32_t kj = k + j;
+                const int s = (int)(kj % stages);
+                if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (kj / stages) & 1, &g_pa_error, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* kst = stage_base + s * lay.stage_bytes;
+                const uint8_t* vst = kst + kBlock * pitch;
+                // S = Q K^T for 16 rows x 16 tokens.
+                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    uint32_t b0, b1, b2, b3;
+                    const int tr = (lane >> 4) * 8 + (lane & 7);
+                    const int cc = kk * 16 + ((lane >> 3) & 1) * 8;
+                    ldsm_x4(smem_addr(kst + tr * pitch + cc * 2), b0, b1, b2, b3);
+                    Elem<T>::mma(sc[0], qa[kk], b0, b1);
+                    Elem<T>::mma(sc[1], qa[kk], b2, b3);
+                }
+                // Scale into log2 units and mask positions past each row's limit.
+                const int tb = kBlock * j + 2 * tig;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int tok = tb + nt * 8 + (c & 1);
+                        const int lim = c < 2 ? lim_lo : lim_hi;
+                        sc[nt][c] = tok <= lim ? sc[nt][c] * p.scale_log2 : -INFINITY;
+                    }
+                }
+                float mx_lo = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+                float mx_hi = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+                mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+                mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+                mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+                mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+                const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+                const float base_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
+                const float base_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+                const float a_lo = ex2(m_lo - base_lo), a_hi = ex2(m_hi - base_hi);
+                m_lo = mn_lo;
+                m_hi = mn_hi;
+                float pr[2][4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    pr[nt][0] = ex2(sc[nt][0] - base_lo);
+                    pr[nt][1] = ex2(sc[nt][1] - base_lo);
+                    pr[nt][2] = ex2(sc[nt][2] - base_hi);
+                    pr[nt][3] = ex2(sc[nt][3] - base_hi);
+                }
+                l_lo = l_lo * a_lo + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
+                l_hi = l_hi * a_hi + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
+                if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {
+#pragma unroll
+                    for (int n = 0; n < D / 8; ++n) {
+                        o[n][0] *= a_lo;
+                        o[n][1] *= a_lo;
+                        o[n][2] *= a_hi;
+                        o[n][3] *= a_hi;
+                    }
+                }
+                // P as the A operand in two 16-bit pieces (hi + residual): together they
+                // carry about 16 significant bits, so P.V loses nothing a single rounding
+                // of P would.
+                uint32_t ph[4], pl[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int nt = q >> 1, c0 = (q & 1) * 2;
+                    const float x0 = pr[nt][c0], x1 = pr[nt][c0 + 1];
+                    const float h0 = Elem<T>::round_trip(x0), h1 = Elem<T>::round_trip(x1);
+                    ph[q] = Elem<T>::pack(h0, h1);
+                    pl[q] = Elem<T>::pack(x0 - h0, x1 - h1);
+                }
+                // A-fragment order: (row lo, tokens 0-7), (row hi, 0-7), (row lo, 8-15), (row hi, 8-15)
+                const uint32_t pa_hi[4] = {ph[0], ph[1], ph[2], ph[3]};
+                const uint32_t pa_lo[4] = {pl[0], pl[1], pl[2], pl[3]};
+#pragma unroll
+                for (int np = 0; np < D / 16; ++np) {
+                    uint32_t v0, v1, v2, v3;
+                    const int tr = (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const int cc = np * 16 + (lane >> 4) * 8;
+                    ldsm_x4_trans(smem_addr(vst + tr * pitch + cc * 2), v0, v1, v2, v3);
+                    Elem<T>::mma(o[2 * np], pa_hi, v0, v1);
+                    Elem<T>::mma(o[2 * np], pa_lo, v0, v1);
+                    Elem<T>::mma(o[2 * np + 1], pa_hi, v2, v3);
+                    Elem<T>::mma(o[2 * np + 1], pa_lo, v2, v3);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * s);
+            }
+        }
+        k += nblk;
+        // Row sums over the quad of lanes sharing a row.
+        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+        if (ok) {
+            float* co = comb_o + warp * p.slot_rows * D;
+            if (gid < rows_here) {
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n)
+                    *reinterpret_cast<float2*>(co + gid * D + n * 8 + 2 * tig) = make_float2(o[n][0], o[n][1]);
+                if (tig == 0) {
+                    comb_m[warp * 16 + gid] = m_lo;
+                    comb_l[warp * 16 + gid] = l_lo;
+                }
+            }
+            if (gid + 8 < rows_here) {
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n)
+                    *reinterpret_cast<float2*>(co + (gid + 8) * D + n * 8 + 2 * tig) = make_float2(o[n][2], o[n][3]);
+                if (tig == 0) {
+                    comb_m[warp * 16 + gid + 8] = m_hi;
+                    comb_l[warp * 16 + gid + 8] = l_hi;
+                }
+            }
+        }
+        // All consumer warps agree on whether to go on (and the buffer writes above are
+        // ordered before the reads below).
+        if (consumers_any(!ok)) break;
+        // Merge the block-split warps of each row tile; write the output or the partial.
+        const int nthreads = kConsumerWarps * 32;
+        for (int idx = threadIdx.x; idx < p.rows * D; idx += nthreads) {
+            const int r = idx / D, e = idx - r * D;
+            const int tile = r >> 4, rr = r & 15;
+            float M = -INFINITY;
+            for (int b = 0; b < p.block_splits; ++b) M = fmaxf(M, comb_m[(tile * p.block_splits + b) * 16 + rr]);
+            float lsum = 0.f, acc = 0.f;
+            if (M != -INFINITY) {
+                for (int b = 0; b < p.block_splits; ++b) {
+                    const int w = tile * p.block_splits + b;
+                    const float f = ex2(comb_m[w * 16 + rr] - M);
+                    lsum += comb_l[w * 16 + rr] * f;
+                    acc += comb_o[(w * p.slot_rows + rr) * D + e] * f;
+                }
+            }
+            const int qi = r / p.group;
+            const int h = ui.kvh * p.group + (r - qi * p.group);
+            const long long orow = (long long)(ui.seq * p.q_len + qi) * p.num_heads + h;
+            if (ui.nparts == 1) {
+                static_cast<uint16_t*>(p.out)[orow * D + e] = Elem<T>::to_bits(acc / lsum);
+            } else {
+                const long long prow = ((long long)(ui.slot0 + ui.part) * p.q_len + qi) * p.num_heads + h;
+                p.pacc[prow * D + e] = acc;
+                if (e == 0) p.pml[prow] = make_float2(M, lsum);
+            }
+        }
+        named_barrier_sync(1, nthreads);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Split-K merge
+// ---------------------------------------------------------------------------
+struct MergeParams {
+    void* out;
+    const int* context_lens;
+    const int* part_start;
+    const float2* pml;
+    const float* pacc;
+    int num_seqs;
+    int q_len;
+    int num_heads;
+    int partition;
+    int max_context_len;
+};
+
+// One warp per output row (sequence, query row, head).
+template <typename T, int D>
+__global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
+    constexpr int kPer = D / 32;
+    const long long row = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long rows_total = (long long)p.num_seqs * p.q_len * p.num_heads;
+    if (row >= rows_total) return;
+    const int per_seq = p.q_len * p.num_heads;
+    const int seq = (int)(row / per_seq);
+    const int rem = (int)(row - (long long)seq * per_seq);
+    const int L = p.context_lens[seq];
+    if (L < 1 || L < p.q_len || L > p.max_context_len) return;
+    const int nparts = (L + p.partition - 1) / p.partition;
+    if (nparts <= 1) return;
+    const long long slot0 = p.part_start[seq];
+    float M = -INFINITY;
+    for (int i = lane; i < nparts; i += 32) M = fmaxf(M, p.pml[(slot0 + i) * per_seq + rem].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float acc[kPer];
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
+    float lsum = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll 4
+        for (int i = 0; i < nparts; ++i) {
+            const long long prow = (slot0 + i) * per_seq + rem;
+            const float2 ml = p.pml[prow];
+            const float f = ex2(ml.x - M);
+            lsum += ml.y * f;
+            const float* src = p.pacc + prow * D + lane * kPer;
+            if constexpr (kPer == 4) {
+                const float4 v = *reinterpret_cast<const float4*>(src);
+                acc[0] += v.x * f;
+                acc[1] += v.y * f;
+                acc[2] += v.z * f;
+                acc[3] += v.w * f;
+            } else {
+                const float2 v = *reinterpret_cast<const float2*>(src);
+                acc[0] += v.x * f;
+                acc[1] += v.y * f;
+            }
+        }
+    }
+    uint16_t* dst = static_cast<uint16_t*>(p.out) + row * D + lane * kPer;
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) dst[c] = Elem<T>::to_bits(acc[c] / lsum);
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers
+// ---------------------------------------------------------------------------
+namespace {
+
+std::mutex g_mu;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int max_smem_optin = 0;
+};
+DeviceInfo g_dev[64];
+
+int device_info(DeviceInfo& out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PA_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return PA_ERR_CUDA;
+        d.ready = true;
+    }
+    out = d;
+    return PA_OK;
+}
+
+// Occupancy of one decode instantiation for a given dynamic shared memory size,
+// cached per device.
+struct OccEntry {
+    const void* fn;
+    int dev, smem, blocks;
+};
+OccEntry g_occ[256];
+int g_occ_n = 0;
+
+int decode_blocks_per_sm(const void* fn, int smem, int& blocks) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < g_occ_n; ++i)
+        if (g_occ[i].fn == fn && g_occ[i].dev == dev && g_occ[i].smem == smem) {
+            blocks = g_occ[i].blocks;
+            return PA_OK;
+        }
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return PA_ERR_CUDA;
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, kThreads, smem) != cudaSuccess) return PA_ERR_CUDA;
+    if (b < 1) return PA_ERR_UNSUPPORTED;
+    if (g_occ_n < 256) g_occ[g_occ_n++] = OccEntry{fn, dev, smem, b};
+    blocks = b;
+    return PA_OK;
+}
+
+struct Profile {
+    bool on = false;
+    int dev = -1;
+    int n = 0;
+    cudaEvent_t ev[2 * 4096] = {};
+    bool created = false;
+} g_prof;
+
+template <typename T, int D>
+int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches) {
+    const WsLayout w = ws_layout(a.num_seqs, a.q_len, a.num_heads, D, a.max_context_len, a.partition);
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    int* header = reinterpret_cast<int*>(ws + w.header);
+    int* part_start = reinterpret_cast<int*>(ws + w.part_start);
+    int2* units = reinterpret_cast<int2*>(ws + w.units);
+    float2* pml = reinterpret_cast<float2*>(ws + w.pml);
+    float* pacc = reinterpret_cast<float*>(ws + w.pacc);
+
+    DeviceInfo dev;
+    if (int st = device_info(dev)) return st;
+
+    PlanParams pp;
+    pp.context_lens = a.context_lens;
+    pp.header = header;
+    pp.part_start = part_start;
+    pp.units = units;
+    pp.num_seqs = a.num_seqs;
+    pp.q_len = a.q_len;
+    pp.partition = a.partition;
+    pp.max_blocks_per_seq = a.max_blocks_per_seq;
+    pp.max_context_len = a.max_context_len;
+    plan_kernel<<<1, 1024, 0, stream>>>(pp);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    *launches += 1;
+
+    DecodeParams p;
+    p.out = a.out;
+    p.query = a.query;
+    p.key_cache = a.key_cache;
+    p.value_cache = a.value_cache;
+    p.block_tables = a.block_tables;
+    p.context_lens = a.context_lens;
+    p.header = header;
+    p.part_start = part_start;
+    p.units = units;
+    p.pml = pml;
+    p.pacc = pacc;
+    p.num_blocks = a.num_blocks;
+    p.max_blocks_per_seq = a.max_blocks_per_seq;
+    p.q_len = a.q_len;
+    p.num_heads = a.num_heads;
+    p.num_kv_heads = a.num_kv_heads;
+    p.group = a.num_heads / a.num_kv_heads;
+    p.rows = p.group * a.q_len;
+    p.partition = a.partition;
+    p.mtiles = (p.rows + 15) / 16;
+    p.block_splits = kConsumerWarps / p.mtiles;
+    p.slot_rows = std::min(16, p.rows);
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+
+    // Deepest ring (a multiple of block_splits) that still lets two CTAs share an SM.
+    const void* fn = reinterpret_cast<const void*>(decode_kernel<T, D>);
+    int stages = kMaxStages;
+    SmemLayout lay = smem_layout(D, stages, p.mtiles, p.slot_rows);
+    const int per_sm_budget = 227 * 1024 / 2 - 1024;
+    while (stages > p.block_splits && lay.total > per_sm_budget) {
+        stages -= p.block_splits;
+        lay = smem_layout(D, stages, p.mtiles, p.slot_rows);
+    }
+    if (lay.total > dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
+    p.stages = stages;
+    int per_sm = 1;
+    if (int st = decode_blocks_per_sm(fn, lay.total, per_sm)) return st;
+    const long long max_units = (long long)a.num_seqs * w.pmax * a.num_kv_heads;
+    const int grid = (int)std::max(1LL, std::min<long long>((long long)dev.sms * per_sm, max_units));
+
+    const bool prof = g_prof.on && g_prof.n < 4096;
+    if (prof) cudaEventRecord(g_prof.ev[2 * g_prof.n], stream);
+    decode_kernel<T, D><<<grid, kThreads, lay.total, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (prof) {
+        cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], stream);
+        g_prof.n++;
+    }
+    *launches += 1;
+
+    if (w.pmax > 1) {
+        MergeParams mp;
+        mp.out = a.out;
+        mp.context_lens = a.context_lens;
+        mp.part_start = part_start;
+        mp.pml = pml;
+        mp.pacc = pacc;
+        mp.num_seqs = a.num_seqs;
+        mp.q_len = a.q_len;
+        mp.num_heads = a.num_heads;
+        mp.partition = a.partition;
+        mp.max_context_len = a.max_context_len;
+        const long long rows = (long long)a.num_seqs * a.q_len * a.num_heads;
+        const long long blocks = (rows * 32 + 127) / 128;
+        merge_kernel<T, D><<<(unsigned)blocks, 128, 0, stream>>>(mp);
+        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+        *launches += 1;
+    }
+    return PA_OK;
+}
+
+}  // namespace
+
+int launch_reshape_and_cache(const void* key, const void* value, void* key_cache, void* value_cache,
+                             const int64_t* slot_mapping, int64_t num_tokens, int row_bytes,
+                             int64_t num_slots, cudaStream_t stream, int* launches) {
+    DeviceInfo dev;
+    if (int st = device_info(dev)) return st;
+    const int row_vecs = row_bytes / 16;
+    const long long total = (long long)num_tokens * 2 * row_vecs;
+    const long long want = (total + 255) / 256;
+    const int grid = (int)std::max(1LL, std::min<long long>(want, (long long)dev.sms * 8));
+    reshape_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                                             static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache),
+                                             reinterpret_cast<const long long*>(slot_mapping), num_tokens,
+                                             row_vecs, num_slots);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    *launches += 1;
+    return PA_OK;
+}
+
+int launch_decode(const DecodeArgs& a, cudaStream_t stream, int* launches) {
+    if (a.dtype == PA_BF16) {
+        if (a.head_dim == 128) return launch_decode_typed<__nv_bfloat16, 128>(a, stream, launches);
+        if (a.head_dim == 64) return launch_decode_typed<__nv_bfloat16, 64>(a, stream, launches);
+    } else {
+        if (a.head_dim == 128) return launch_decode_typed<__half, 128>(a, stream, launches);
+        if (a.head_dim == 64) return launch_decode_typed<__half, 64>(a, stream, launches);
+    }
+    return PA_ERR_UNSUPPORTED;
+}
+
+int read_device_error(int32_t* flags, int clear, cudaStream_t stream) {
+    int v = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_pa_error, sizeof(int), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (clear) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbolAsync(g_pa_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return PA_ERR_CUDA;
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    *flags = v;
+    return PA_OK;
+}
+
+int profile_enable(int on) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (on && !g_prof.created) {
+        for (int i = 0; i < 2 * 4096; ++i)
+            if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) return PA_ERR_CUDA;
+        g_prof.created = true;
+        cudaGetDevice(&g_prof.dev);
+    }
+    g_prof.on = on != 0;
+    return PA_OK;
+}
+
+int profile_read(float* total_ms, int* launches) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    float sum = 0.f;
+    for (int i = 0; i < g_prof.n; ++i) {
+        if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess) return PA_ERR_CUDA;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess) return PA_ERR_CUDA;
+        sum += ms;
+    }
+    *total_ms = sum;
+    *launches = g_prof.n;
+    g_prof.n = 0;
+    return PA_OK;
+}
+
+}  // namespace pa

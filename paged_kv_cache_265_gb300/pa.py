@@ -1,0 +1,179 @@
+"""Python binding of libpa.so (ctypes).  Argument marshalling only: every step of
+the decode path runs in the library's CUDA kernels.
+
+Tensors are torch CUDA tensors (PyTorch supplies device memory and streams);
+their data pointers and the current CUDA stream are handed to the C ABI
+declared in ``include/pa.h``.  A missing library raises instead of falling
+back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa.so")
+
+PA_BF16, PA_FP16 = 0, 1
+PA_DEVERR_BLOCK_ID, PA_DEVERR_CONTEXT, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT = 1, 2, 4, 8
+BLOCK_SIZE = 16
+DEFAULT_PARTITION = 512
+
+_DT = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16}
+
+_c_int, _c_i64, _c_sz, _c_f, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p
+
+_SIGS = {
+    "pa_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_int, _vp]),
+    "pa_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "pa_decode_workspace_size_ex": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "pa_decode_attention": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                     _c_i64, _c_int, _c_f, _c_int, _vp, _c_sz, _vp]),
+    "pa_decode_attention_multiquery": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int,
+                                                _c_int, _c_int, _c_int, _c_i64, _c_int, _c_f, _c_int, _vp, _c_sz,
+                                                _vp]),
+    "pa_decode_attention_ex": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int,
+                                        _c_int, _c_int, _c_i64, _c_int, _c_f, _c_int, _c_int, _vp, _c_sz, _vp]),
+    "pa_status_string": (ctypes.c_char_p, [_c_int]),
+    "pa_get_device_error": (_c_int, [ctypes.POINTER(ctypes.c_int32), _c_int, _vp]),
+    "pa_profile_enable": (_c_int, [_c_int]),
+    "pa_profile_read": (_c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
+    "pa_last_launch_count": (_c_int, []),
+    "pa_version": (_c_int, []),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class PaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpa.so (built in-tree by ``paged_kv_cache_265_gb300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libpa.so is not built ({LIB_PATH}); run paged_kv_cache_265_gb300.build.build()")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pa_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise PaError(fn, status)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise ValueError(f"unsupported dtype {t.dtype}; use bfloat16 or float16")
+    return _DT[t.dtype]
+
+
+def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                      slot_mapping: torch.Tensor, stream=None) -> None:
+    """Append new K/V rows ([T, Hkv, d]) into the paged caches ([NB, 16, Hkv, d]) at slot_mapping (int64 [T])."""
+    nb, bs, hkv, d = key_cache.shape
+    if key.shape != (slot_mapping.shape[0], hkv, d) or value.shape != key.shape:
+        raise ValueError("key/value must be [num_tokens, num_kv_heads, head_dim]")
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    if key.dtype != key_cache.dtype or value.dtype != key_cache.dtype or value_cache.dtype != key_cache.dtype:
+        raise ValueError("key, value and the caches must share one dtype")
+    st = lib().pa_reshape_and_cache(
+        _dev(key, "key"), _dev(value, "value"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(slot_mapping, "slot_mapping"), slot_mapping.shape[0], hkv, d, bs, nb, dtype_code(key_cache),
+        _stream(stream))
+    _check("pa_reshape_and_cache", st)
+
+
+def workspace_size(num_seqs: int, q_len: int, num_heads: int, head_dim: int, max_context_len: int,
+                   partition_size: int = 0) -> int:
+    return int(lib().pa_decode_workspace_size_ex(num_seqs, q_len, num_heads, head_dim, max_context_len,
+                                                 partition_size))
+
+
+def alloc_workspace(num_seqs: int, q_len: int, num_heads: int, head_dim: int, max_context_len: int,
+                    partition_size: int = 0, device=None) -> torch.Tensor:
+    n = workspace_size(num_seqs, q_len, num_heads, head_dim, max_context_len, partition_size)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def decode_attention(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                     block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, max_context_len: int,
+                     workspace: torch.Tensor, partition_size: int = 0, stream=None) -> torch.Tensor:
+    """Paged decode attention.  query/out are [N, Hq, d] (one query row) or [N, q_len, Hq, d]
+    (q_len rows, causal inside the chunk)."""
+    if query.dim() == 3:
+        n, hq, d = query.shape
+        q_len = 1
+    elif query.dim() == 4:
+        n, q_len, hq, d = query.shape
+    else:
+        raise ValueError("query must be [N, Hq, d] or [N, q_len, Hq, d]")
+    if out.shape != query.shape or out.dtype != query.dtype:
+        raise ValueError("out must match query in shape and dtype")
+    nb, bs, hkv, d2 = key_cache.shape
+    if d2 != d or value_cache.shape != key_cache.shape:
+        raise ValueError("cache shape mismatch")
+    if query.dtype != key_cache.dtype or value_cache.dtype != key_cache.dtype:
+        raise ValueError("query and caches must share one dtype")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != n or context_lens.shape != (n,):
+        raise ValueError("block_tables must be [N, max_blocks] and context_lens [N]")
+    st = lib().pa_decode_attention_ex(
+        _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(block_tables, "block_tables"), block_tables.shape[1], _dev(context_lens, "context_lens"), n, q_len,
+        hq, hkv, d, bs, nb, int(max_context_len), float(scale), dtype_code(query), int(partition_size),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("pa_decode_attention_ex", st)
+    return out
+
+
+def get_device_error(clear: bool = True, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    _check("pa_get_device_error", lib().pa_get_device_error(ctypes.byref(v), int(clear), _stream(stream)))
+    return int(v.value)
+
+
+def profile_enable(on: bool = True) -> None:
+    _check("pa_profile_enable", lib().pa_profile_enable(int(on)))
+
+
+def profile_read() -> tuple[float, int]:
+    ms, n = ctypes.c_float(0.0), ctypes.c_int(0)
+    _check("pa_profile_read", lib().pa_profile_read(ctypes.byref(ms), ctypes.byref(n)))
+    return float(ms.value), int(n.value)
+
+
+def last_launch_count() -> int:
+    return int(lib().pa_last_launch_count())

@@ -1,0 +1,94 @@
+"""Shared plumbing of the GPU parity tests: upload a workload, run one decode step
+through the C ABI (append, then attention), run the oracle on the same inputs,
+and compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from paged_kv_cache_265_gb300 import pa
+from paged_kv_cache_265_gb300 import workload as W
+
+TORCH_DT = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+# Attention tolerance: an element passes when |gpu - oracle| <= ABS_TOL or
+# |gpu - oracle| <= REL_TOL * |oracle|.
+ABS_TOL = 2e-3
+REL_TOL = 1e-2
+
+
+def to_dev(bits: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(device).view(TORCH_DT[dtype])
+
+
+def to_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def bits_to_f64(bits: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "fp16":
+        return bits.view(np.float16).astype(np.float64)
+    return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+class GpuStep:
+    """Device copies of one workload's inputs; runs the append and the attention."""
+
+    def __init__(self, w: W.Workload, partition_size: int = 0):
+        self.w = w
+        self.partition_size = partition_size
+        dt = w.dtype
+        self.key_cache = to_dev(w.key_cache, dt)
+        self.value_cache = to_dev(w.value_cache, dt)
+        self.new_key = to_dev(w.new_key, dt)
+        self.new_value = to_dev(w.new_value, dt)
+        self.slot_mapping = torch.from_numpy(w.slot_mapping).cuda()
+        self.block_tables = torch.from_numpy(w.block_tables).cuda()
+        self.context_lens = torch.from_numpy(w.context_lens).cuda()
+        self.query = to_dev(w.query, dt)
+        self.out = torch.empty_like(self.query)
+        self.workspace = pa.alloc_workspace(w.num_seqs, w.q_len, w.num_heads, w.head_dim, w.max_context_len,
+                                            partition_size)
+
+    def append(self):
+        pa.reshape_and_cache(self.new_key, self.new_value, self.key_cache, self.value_cache, self.slot_mapping)
+
+    def attend(self) -> torch.Tensor:
+        pa.decode_attention(self.out, self.query, self.key_cache, self.value_cache, self.block_tables,
+                            self.context_lens, self.w.scale, self.w.max_context_len, self.workspace,
+                            partition_size=self.partition_size)
+        return self.out
+
+    def run(self) -> np.ndarray:
+        self.append()
+        self.attend()
+        torch.cuda.synchronize()
+        return to_bits(self.out)
+
+
+def oracle_step(w: W.Workload, threads: int = 0):
+    """Oracle append on host copies of the pools, then oracle attention on the result."""
+    orc = oracle.load()
+    kc, vc = w.key_cache.copy(), w.value_cache.copy()
+    bad = orc.reshape_and_cache(w.new_key, w.new_value, kc, vc, w.slot_mapping)
+    assert bad == 0
+    out, bad = orc.decode_attention(w.query, kc, vc, w.block_tables, w.context_lens, w.scale, w.dtype,
+                                    num_threads=threads)
+    assert bad == 0
+    return kc, vc, out
+
+
+def compare(gpu_bits: np.ndarray, ref: np.ndarray, dtype: str, what: str = ""):
+    """Asserts the attention tolerance element by element; returns (max_abs, max_rel)."""
+    g = bits_to_f64(gpu_bits, dtype).reshape(ref.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
+    err = np.abs(g - ref)
+    rel = err / np.maximum(np.abs(ref), 1e-30)
+    ok = (err <= ABS_TOL) | (rel <= REL_TOL)
+    if not np.all(ok):
+        i = np.unravel_index(np.argmax(np.where(ok, 0, err)), err.shape)
+        raise AssertionError(f"{what}: {np.count_nonzero(~ok)} elements out of tolerance; worst at {i}: "
+                             f"gpu {g[i]!r} oracle {ref[i]!r}")
+    return float(err.max(initial=0.0)), float(np.where(err > ABS_TOL, rel, 0.0).max(initial=0.0))

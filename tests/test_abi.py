@@ -1,0 +1,92 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol its
+header declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_265_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = B.build()
+    from paged_kv_cache_265_gb300 import pa
+
+    return pa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, text in [(0, "ok"), (1, "invalid argument"), (2, "unsupported"), (3, "workspace"), (4, "CUDA")]:
+        assert text in lib.pa_status_string(code).decode()
+    assert lib.pa_status_string(99).decode() == "unknown status"
+    assert lib.pa_version() >= 100
+
+
+FAKE = 1 << 20  # an aligned, never-dereferenced "device" address
+
+
+def _decode(lib, **kw):
+    a = dict(out=FAKE, query=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, mbps=8, cl=FAKE, n=2, q_len=1, hq=4, hkv=4, d=64,
+             bs=16, nb=64, max_ctx=100, scale=0.125, dtype=0, part=0, ws=FAKE, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.pa_decode_attention_ex(a["out"], a["query"], a["kc"], a["vc"], a["bt"], a["mbps"], a["cl"], a["n"],
+                                      a["q_len"], a["hq"], a["hkv"], a["d"], a["bs"], a["nb"], a["max_ctx"],
+                                      a["scale"], a["dtype"], a["part"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+def test_decode_host_validation(lib):
+    assert _decode(lib, n=0) == 0                       # nothing to do
+    assert _decode(lib, hkv=3) == 1                     # heads not a multiple of kv heads
+    assert _decode(lib, q_len=0) == 1
+    assert _decode(lib, dtype=7) == 1
+    assert _decode(lib, scale=float("nan")) == 1
+    assert _decode(lib, part=24) == 1                   # partition not a multiple of 16
+    assert _decode(lib, max_ctx=8 * 16 + 1) == 1        # longer than the block table can map
+    assert _decode(lib, out=None) == 1
+    assert _decode(lib, query=FAKE + 8) == 1            # misaligned
+    assert _decode(lib, d=96) == 2                      # head_dim not compiled
+    assert _decode(lib, bs=32) == 2                     # block size other than 16
+    assert _decode(lib, hq=64, hkv=1, q_len=2) == 2     # 128 rows per kv head
+    assert _decode(lib, ws=None) == 3
+    assert _decode(lib, ws_bytes=16) == 3
+
+
+def test_workspace_size(lib):
+    lib.pa_decode_workspace_size_ex.restype = ctypes.c_size_t
+    lib.pa_decode_workspace_size.restype = ctypes.c_size_t
+    small = lib.pa_decode_workspace_size(4, 1, 4, 64, 100)
+    assert small > 0
+    # one partition per sequence: no partial buffers
+    assert lib.pa_decode_workspace_size_ex(4, 1, 4, 64, 100, 1 << 20) == small
+    split = lib.pa_decode_workspace_size_ex(4, 1, 4, 64, 100, 16)
+    # 7 partitions x 4 seqs x 4 heads x (64 fp32 + 2 fp32) at least
+    assert split >= small + 7 * 4 * 4 * (64 + 2) * 4
+    assert lib.pa_decode_workspace_size_ex(4, 1, 4, 64, 100, 24) == 0
+
+
+def test_reshape_host_validation(lib):
+    f = lib.pa_reshape_and_cache
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 64, 16, 64, 0, None) == 0      # no tokens
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 96, 16, 64, 0, None) == 2      # head_dim
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 64, 8, 64, 0, None) == 2       # block size
+    assert f(None, FAKE, FAKE, FAKE, FAKE, 4, 4, 64, 16, 64, 0, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE + 4, 4, 4, 64, 16, 64, 0, None) == 1  # slot_mapping alignment
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 4, 64, 16, 64, 0, None) == 1
