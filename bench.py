@@ -42,6 +42,7 @@ WORKLOADS = {
     "gqa_batch128": 3,
     "shared_prefix": 4,
     "long_context": 5,
+    "gqa_batch32": 6,
 }
 DESCR = {
     1: "tiny_mha_d64: 4 seqs L={1,17,33,100}, MHA 4 heads, d=64, bf16, block 16, 64-block pool, 4-row append",
@@ -51,6 +52,8 @@ DESCR = {
        "d=128, bf16, 4096-block pool, 320-row append",
     5: "long_context_skewed: 16 seqs L~U[16384,32768] + 240 seqs L~U[64,1024], GQA 64q/8kv, d=128, bf16, "
        "65536-block pool, 256-row append",
+    6: "gqa_batch32 (profiling size): 32 seqs L~U[1,4096], GQA 32q/8kv, d=128, bf16, block 16, 10000-block pool, "
+       "32-row append",
 }
 L2_BYTES = 129 * 1024 * 1024
 

@@ -677,7 +677,15 @@ int decode_blocks_per_sm(const void* fn, int smem, int& blocks) {
             blocks = g_occ[i].blocks;
             return PA_OK;
         }
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    // The opt-in limit is raised to what this call needs and never lowered, so every
+    // cached (fn, smem) entry stays launchable.
+    int cur = 0;
+    {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return PA_ERR_CUDA;
+        cur = fa.maxDynamicSharedSizeBytes;
+    }
+    if (cur < smem && cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return PA_ERR_CUDA;
     int b = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, kThreads, smem) != cudaSuccess) return PA_ERR_CUDA;

@@ -249,12 +249,21 @@ def long_context_skewed(**kw) -> Workload:
                          dtype="bf16", q_len=1, num_blocks=65536, seed=2655, max_blocks_per_seq=2048, **kw)
 
 
+def gqa_batch32(**kw) -> Workload:
+    """Profiling-size member of the GQA family: 32 sequences, L ~ U[1, 4096], GQA 32q/8kv, d = 128,
+    bf16, 10000-block pool (about 0.25 GB of K/V per step: still larger than L2)."""
+    lens = _uniform_lens(2663, 32, 1, 4096)
+    return make_workload("gqa_batch32", lens, num_heads=32, num_kv_heads=8, head_dim=128,
+                         dtype="bf16", q_len=1, num_blocks=10000, seed=2663, max_blocks_per_seq=256, **kw)
+
+
 WORKLOADS = {
     1: tiny_mha,
     2: opt13b_mha,
     3: gqa_batch128,
     4: shared_prefix_verify,
     5: long_context_skewed,
+    6: gqa_batch32,
 }
 
 

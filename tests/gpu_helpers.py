@@ -92,3 +92,21 @@ def compare(gpu_bits: np.ndarray, ref: np.ndarray, dtype: str, what: str = ""):
         raise AssertionError(f"{what}: {np.count_nonzero(~ok)} elements out of tolerance; worst at {i}: "
                              f"gpu {g[i]!r} oracle {ref[i]!r}")
     return float(err.max(initial=0.0)), float(np.where(err > ABS_TOL, rel, 0.0).max(initial=0.0))
+
+
+def ulps_from_rounded_oracle(gpu_bits: np.ndarray, ref: np.ndarray, dtype: str, floor: float = 2.0 ** -6) -> int:
+    """Largest distance, in units in the last place of the 16-bit type, between the GPU output
+    and the oracle rounded once to that type (round to nearest even, library cast), over the
+    elements with |oracle| >= floor (below it, cancellation makes the last place meaningless;
+    the absolute tolerance covers those)."""
+    if dtype == "fp16":
+        rb = ref.astype(np.float16).view(np.uint16)
+    else:
+        rb = torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    g = gpu_bits.reshape(ref.shape).astype(np.int64)
+    r = rb.astype(np.int64)
+    # map sign-magnitude bit patterns onto a monotone integer line
+    g = np.where(g & 0x8000, 0x8000 - g, g)
+    r = np.where(r & 0x8000, 0x8000 - r, r)
+    big = np.abs(ref) >= floor
+    return int(np.abs(g - r)[big].max(initial=0))
