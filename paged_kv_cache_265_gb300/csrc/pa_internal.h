@@ -11,8 +11,9 @@ namespace pa {
 // Workspace of one decode call (byte offsets from the workspace base).
 //   header      int32[64]: [0] = number of (sequence, partition) work entries
 //   part_start  int32[N+1]: first partial slot of each sequence (exclusive scan)
-//   units       int2[N * Pmax]: work entries (sequence, partition), full
-//               partitions first, then each sequence's shorter last partition
+//   units       int4[N * Pmax]: work entries (sequence, partition, context length,
+//               first partial slot), full partitions first, then each
+//               sequence's shorter last partition
 //   pml         float2[slots, q_len, Hq]: per-partition (max, sum) in log2 units
 //   pacc        float[slots, q_len, Hq, D]: per-partition unnormalised outputs
 struct WsLayout {
@@ -35,7 +36,7 @@ inline WsLayout ws_layout(int num_seqs, int q_len, int num_heads, int head_dim, 
     w.part_start = off;
     off += align256(4 * (n + 1));
     w.units = off;
-    off += align256(8 * slots);
+    off += align256(16 * slots);
     w.pml = w.pacc = off;
     if (pmax > 1) {
         w.pml = off;

@@ -22,6 +22,7 @@
 // dense causal attention of "LLM 推理优化的系统视角", section 3.1; the query-head
 // grouping is section 3.2 of the latter.  The online softmax is the tiling idea
 // named in its section 4.2 (execution order changes, semantics do not).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -37,7 +38,6 @@ namespace pa {
 // Device state owned by the library (module globals, not allocations).
 // ---------------------------------------------------------------------------
 __device__ int g_pa_error;                            // PA_DEVERR_* bits
-__device__ __align__(128) uint4 g_zero_rows[16 * 16];  // 16 rows x 256 B of zeros (never written)
 
 constexpr int kBlock = 16;
 constexpr int kConsumerWarps = 4;
@@ -81,7 +81,7 @@ struct PlanParams {
     const int* context_lens;
     int* header;
     int* part_start;
-    int2* units;
+    int4* units;
     int num_seqs;
     int q_len;
     int partition;
@@ -151,8 +151,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
         const int ppos = carry_part + block_exclusive_scan(partial, scratch, t_part);
         if (i < p.num_seqs) {
             p.part_start[i] = slot;
-            for (int c = 0; c < full; ++c) p.units[fpos + c] = make_int2(i, c);
-            if (partial) p.units[total_full + ppos] = make_int2(i, full);
+            const int L = p.context_lens[i];
+            for (int c = 0; c < full; ++c) p.units[fpos + c] = make_int4(i, c, L, slot);
+            if (partial) p.units[total_full + ppos] = make_int4(i, full, L, slot);
         }
         carry_slot += t_slot;
         carry_full += t_full;
@@ -167,16 +168,24 @@ __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
 // ---------------------------------------------------------------------------
 // Decode attention
 // ---------------------------------------------------------------------------
-struct DecodeParams {
+// K/V staging.  Each 16-token block of one kv head is fetched by tensor-map TMA
+// as boxes of 16 rows x 64 elements (128 B), 128-byte swizzled in shared memory
+// (16-byte chunk c of row r sits at chunk c ^ (r & 7)), so ldmatrix reads are
+// bank-conflict free without padding.  A block with only `valid` < 16 tokens is
+// fetched with its box starting at token coordinate valid - 16: the rows before
+// coordinate 0 are outside the tensor and arrive as zeros, the tokens land in
+// the last `valid` rows, and P.V never multiplies stale data.
+constexpr int kBoxCols = 64;                       // elements per box row (128 B)
+constexpr int kBoxBytes = kBlock * kBoxCols * 2;   // 2 KB
+
+struct alignas(64) DecodeParams {
+    CUtensorMap tmap_k;  // [num_blocks, 16, Hkv, D] viewed as 4-D, box {64, 1, 16, 1}
+    CUtensorMap tmap_v;
     void* out;
     const void* query;
-    const void* key_cache;
-    const void* value_cache;
     const int* block_tables;
-    const int* context_lens;
     const int* header;
-    const int* part_start;
-    const int2* units;
+    const int4* units;   // (seq, partition, context_len, first partial slot)
     float2* pml;
     float* pacc;
     long long num_blocks;
@@ -195,27 +204,43 @@ struct DecodeParams {
 };
 
 struct UnitInfo {
-    int seq, part, len, nparts, slot0, kvh, ntok, pad;
+    int seq, part, len, slot0, kvh, ntok, pad0, pad1;
 };
 
 struct SmemLayout {
-    int pitch, stage_bytes, q_half_bytes;
+    int stage_bytes, qpitch, q_half_bytes;
     int off_q, off_comb, off_m, off_l, off_bars, off_info, total;
 };
 
+// Offsets from a 1024-byte aligned base (the swizzled TMA boxes need that alignment).
 __host__ __device__ inline SmemLayout smem_layout(int head_dim, int stages, int mtiles, int slot_rows) {
     SmemLayout s;
-    s.pitch = head_dim * 2 + 16;  // 16 B of padding per row: conflict-free ldmatrix
-    s.stage_bytes = 2 * kBlock * s.pitch;
-    s.q_half_bytes = mtiles * 16 * s.pitch;
+    s.stage_bytes = 2 * (head_dim / kBoxCols) * kBoxBytes;  // K boxes then V boxes
+    s.qpitch = head_dim * 2 + 16;                            // padded query rows
+    s.q_half_bytes = mtiles * 16 * s.qpitch;
     s.off_q = stages * s.stage_bytes;
     s.off_comb = s.off_q + 2 * s.q_half_bytes;
     s.off_m = s.off_comb + kConsumerWarps * slot_rows * head_dim * 4;
     s.off_l = s.off_m + kConsumerWarps * 16 * 4;
     s.off_bars = s.off_l + kConsumerWarps * 16 * 4;
     s.off_info = s.off_bars + (2 * kMaxStages + 4) * 8;
-    s.total = s.off_info + 2 * (int)sizeof(UnitInfo) + 16;
+    s.total = s.off_info + 2 * (int)sizeof(UnitInfo) + 16 + 1024;  // + alignment slack
     return s;
+}
+
+// Byte offset of element column `col` of box row `row` inside a stage half (K or V).
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+    const int box = col >> 6, chunk = (col & 63) >> 3;
+    return box * kBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
+        : "memory");
 }
 
 // bar.red.or over the 128 consumer threads (named barrier 1): every thread
@@ -235,10 +260,12 @@ __device__ __forceinline__ bool consumers_any(bool v) {
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const SmemLayout lay = smem_layout(D, p.stages, p.mtiles, p.slot_rows);
-    const int pitch = lay.pitch;
+    const int qpitch = lay.qpitch;
     constexpr int kRowBytes = D * 2;
+    constexpr int kBoxes = D / kBoxCols;  // boxes per K (or V) block
     uint8_t* stage_base = smem;
     uint8_t* qbuf = smem + lay.off_q;
     float* comb_o = reinterpret_cast<float*>(smem + lay.off_comb);
@@ -279,18 +306,30 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
         const uint64_t pol_stream = l2_policy_evict_first();
         const uint64_t pol_keep = l2_policy_evict_last();
         const int blocks_per_part = p.partition / kBlock;
-        const long long kv_row = (long long)p.num_kv_heads * D;  // elements per token row of the pool
         uint32_t k = 0;
         int ul = 0;
         bool ok = true;
-        for (long long u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++ul) {
-            const int e = (int)(u / p.num_kv_heads);
-            const int kvh = (int)(u - (long long)e * p.num_kv_heads);
-            const int2 sp = p.units[e];
-            const int L = p.context_lens[sp.x];
-            const int tok0 = sp.y * p.partition;
+        long long u = blockIdx.x;
+        // Work-entry metadata and the first 32 block ids of the next unit are fetched
+        // while the current unit streams, so a unit starts without dependent loads.
+        int4 cur = make_int4(0, 0, 0, 0);
+        int bids = 0;
+        if (u < total_units) {
+            cur = p.units[u / p.num_kv_heads];
+            const int nb0 = ((min(p.partition, cur.z - cur.y * p.partition)) + kBlock - 1) / kBlock;
+            if (lane < nb0)
+                bids = __ldg(p.block_tables + (long long)cur.x * p.max_blocks_per_seq +
+                             (long long)cur.y * blocks_per_part + lane);
+        }
+        for (; u < total_units && ok; u += gridDim.x, ++ul) {
+            const int kvh = (int)(u % p.num_kv_heads);
+            const int seq = cur.x, part = cur.y, L = cur.z;
+            const int tok0 = part * p.partition;
             const int ntok = min(p.partition, L - tok0);
             const int nblk = (ntok + kBlock - 1) / kBlock;
+            const long long un = u + gridDim.x;
+            const int4 nxt = un < total_units ? p.units[un / p.num_kv_heads] : make_int4(0, 0, 0, 0);
+            int nbids = 0;
             const int qb = ul & 1;
             if (ul >= 2 &&
                 !__all_sync(0xffffffffu, mbar_wait(qempty0 + 8 * qb, ((ul - 2) >> 1) & 1, &g_pa_error, abort_flag))) {
@@ -299,14 +338,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
             }
             if (lane == 0) {
                 UnitInfo ui;
-                ui.seq = sp.x;
-                ui.part = sp.y;
+                ui.seq = seq;
+                ui.part = part;
                 ui.len = L;
-                ui.nparts = (L + p.partition - 1) / p.partition;
-                ui.slot0 = p.part_start[sp.x];
+                ui.slot0 = cur.w;
                 ui.kvh = kvh;
                 ui.ntok = ntok;
-                ui.pad = 0;
+                ui.pad0 = ui.pad1 = 0;
                 info[qb] = ui;
                 mbar_arrive_expect_tx(qfull0 + 8 * qb, p.rows * kRowBytes);
             }
@@ -314,15 +352,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
             for (int r = lane; r < p.rows; r += 32) {
                 const int qi = r / p.group, hg = r - qi * p.group;
                 const T* src = static_cast<const T*>(p.query) +
-                               ((long long)(sp.x * p.q_len + qi) * p.num_heads + kvh * p.group + hg) * D;
-                bulk_g2s(smem_addr(qbuf + qb * lay.q_half_bytes + r * pitch), src, kRowBytes,
-                         qfull0 + 8 * qb, pol_keep);
+                               ((long long)(seq * p.q_len + qi) * p.num_heads + kvh * p.group + hg) * D;
+                bulk_g2s(smem_addr(qbuf + qb * lay.q_half_bytes + r * qpitch), src, kRowBytes, qfull0 + 8 * qb,
+                         pol_keep);
             }
-            const int* bt = p.block_tables + (long long)sp.x * p.max_blocks_per_seq +
-                            (long long)sp.y * blocks_per_part;
+            const int* bt = p.block_tables + (long long)seq * p.max_blocks_per_seq + (long long)part * blocks_per_part;
+            const int prefetch_at = min(nblk, 4) - 1;
             for (int c = 0; c < nblk && ok; c += 32) {
                 const bool have = c + lane < nblk;
-                const int bid = have ? __ldg(bt + c + lane) : 0;
+                const int bid = c == 0 ? bids : (have ? __ldg(bt + c + lane) : 0);
                 const bool bad = have && (bid < 0 || (long long)bid >= p.num_blocks);
                 if (bad) atomicOr(&g_pa_error, PA_DEVERR_BLOCK_ID);
                 const int cn = min(32, nblk - c);
@@ -337,28 +375,37 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
                     }
                     const int b = __shfl_sync(0xffffffffu, bid, jj);
                     const bool b_bad = __shfl_sync(0xffffffffu, (int)bad, jj) != 0;
-                    const int valid = b_bad ? 0 : min(kBlock, ntok - kBlock * j);
-                    if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * s, 2 * kBlock * kRowBytes);
-                    __syncwarp();
-                    // Lane r < 16 fetches K row r, lane 16 + r fetches V row r; rows past the
-                    // sequence's end (or of a rejected block) come from the zero buffer so the
-                    // P.V product never meets stale data.
-                    const int r = lane & 15;
-                    const bool is_v = lane >= 16;
-                    const void* src;
-                    if (r < valid) {
-                        const T* base = static_cast<const T*>(is_v ? p.value_cache : p.key_cache);
-                        src = base + ((long long)b * kBlock + r) * kv_row + (long long)kvh * D;
-                    } else {
-                        src = reinterpret_cast<const uint8_t*>(g_zero_rows) + r * kRowBytes;
+                    const int valid = min(kBlock, ntok - kBlock * j);
+                    if (lane == 0) {
+                        const uint32_t bar = full0 + 8 * s;
+                        if (b_bad) {
+                            mbar_arrive(bar);  // nothing to wait for; the consumers compute on stale data
+                        } else {
+                            mbar_arrive_expect_tx(bar, 2 * kBoxes * kBoxBytes);
+                            const uint32_t dst = smem_addr(stage_base + s * lay.stage_bytes);
+                            const int y0 = valid - kBlock;  // <= 0; rows before token 0 arrive as zeros
+#pragma unroll
+                            for (int bx = 0; bx < kBoxes; ++bx) {
+                                tma_load_4d(dst + bx * kBoxBytes, &p.tmap_k, bx * kBoxCols, kvh, y0, b, bar,
+                                            pol_stream);
+                                tma_load_4d(dst + (kBoxes + bx) * kBoxBytes, &p.tmap_v, bx * kBoxCols, kvh, y0, b,
+                                            bar, pol_stream);
+                            }
+                        }
                     }
-                    uint8_t* dst = stage_base + s * lay.stage_bytes + (is_v ? kBlock * pitch : 0) + r * pitch;
-                    bulk_g2s(smem_addr(dst), src, kRowBytes, full0 + 8 * s, pol_stream);
+                    if (c == 0 && jj == prefetch_at && un < total_units) {
+                        const int nb1 = (min(p.partition, nxt.z - nxt.y * p.partition) + kBlock - 1) / kBlock;
+                        if (lane < nb1)
+                            nbids = __ldg(p.block_tables + (long long)nxt.x * p.max_blocks_per_seq +
+                                          (long long)nxt.y * blocks_per_part + lane);
+                    }
                 }
             }
+            cur = nxt;
+            bids = nbids;
         }
-        // Never leave the CTA with bulk copies in flight: wait for the last fill of
-        // every stage and of both query buffers (immediate on the normal path).
+        // Never leave the CTA with copies in flight: wait for the last fill of every
+        // stage and of both query buffers (immediate on the normal path).
         for (int s = 0; s < stages; ++s) {
             if (k > (uint32_t)s) {
                 const uint32_t last = s + ((k - 1 - s) / stages) * stages;
@@ -373,8 +420,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
     }
 
     // ===================== consumer warps =====================
-    const int mt = warp / p.block_splits;  // row tile of this warp
-    const int bsg = warp % p.block_splits; // which of the tile's block-split warps
+    const int mt = warp / p.block_splits;   // row tile of this warp
+    const int bsg = warp % p.block_splits;  // which of the tile's block-split warps
     const int gid = lane >> 2, tig = lane & 3;
     const int row_lo = mt * 16 + gid, row_hi = row_lo + 8;
     const int rows_here = min(16, p.rows - mt * 16);
@@ -392,12 +439,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
         for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
         int nblk = 0;
         if (ok) {
-            const uint8_t* qrow = qbuf + qb * lay.q_half_bytes + mt * 16 * pitch;
+            const uint8_t* qrow = qbuf + qb * lay.q_half_bytes + mt * 16 * qpitch;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int rr = (lane & 7) + ((lane >> 3) & 1) * 8;
                 const int cc = kk * 16 + (lane >> 4) * 8;
-                ldsm_x4(smem_addr(qrow + rr * pitch + cc * 2), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+                ldsm_x4(smem_addr(qrow + rr * qpitch + cc * 2), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(qempty0 + 8 * qb);
@@ -418,8 +465,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
                     ok = false;
                     break;
                 }
-                const uint8_t* kst = stage_base + s * lay.stage_bytes;
-                const uint8_t* vst = kst + kBlock * pitch;
+                const uint32_t kst = smem_addr(stage_base + s * lay.stage_bytes);
+                const uint32_t vst = kst + kBoxes * kBoxBytes;
+                // smem row r holds token r - shift of this block (shift > 0 only for a short last block)
+                const int shift = kBlock - min(kBlock, ui.ntok - kBlock * j);
                 // S = Q K^T for 16 rows x 16 tokens.
                 float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
@@ -427,19 +476,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
                     uint32_t b0, b1, b2, b3;
                     const int tr = (lane >> 4) * 8 + (lane & 7);
                     const int cc = kk * 16 + ((lane >> 3) & 1) * 8;
-                    ldsm_x4(smem_addr(kst + tr * pitch + cc * 2), b0, b1, b2, b3);
+                    ldsm_x4(kst + swz(tr, cc), b0, b1, b2, b3);
                     Elem<T>::mma(sc[0], qa[kk], b0, b1);
                     Elem<T>::mma(sc[1], qa[kk], b2, b3);
                 }
                 // Scale into log2 units and mask positions past each row's limit.
-                const int tb = kBlock * j + 2 * tig;
+                const int tb = kBlock * j - shift + 2 * tig;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
+                        const int r = nt * 8 + 2 * tig + (c & 1);
                         const int tok = tb + nt * 8 + (c & 1);
                         const int lim = c < 2 ? lim_lo : lim_hi;
-                        sc[nt][c] = tok <= lim ? sc[nt][c] * p.scale_log2 : -INFINITY;
+                        sc[nt][c] = (r >= shift && tok <= lim) ? sc[nt][c] * p.scale_log2 : -INFINITY;
                     }
                 }
                 float mx_lo = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
@@ -475,25 +525,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
                 }
                 // P as the A operand in two 16-bit pieces (hi + residual): together they
                 // carry about 16 significant bits, so P.V loses nothing a single rounding
-                // of P would.
-                uint32_t ph[4], pl[4];
+                // of P would.  A-fragment order: (row lo, tokens 0-7), (row hi, 0-7),
+                // (row lo, 8-15), (row hi, 8-15).
+                uint32_t pa_hi[4], pa_lo[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int nt = q >> 1, c0 = (q & 1) * 2;
                     const float x0 = pr[nt][c0], x1 = pr[nt][c0 + 1];
                     const float h0 = Elem<T>::round_trip(x0), h1 = Elem<T>::round_trip(x1);
-                    ph[q] = Elem<T>::pack(h0, h1);
-                    pl[q] = Elem<T>::pack(x0 - h0, x1 - h1);
+                    pa_hi[q] = Elem<T>::pack(h0, h1);
+                    pa_lo[q] = Elem<T>::pack(x0 - h0, x1 - h1);
                 }
-                // A-fragment order: (row lo, tokens 0-7), (row hi, 0-7), (row lo, 8-15), (row hi, 8-15)
-                const uint32_t pa_hi[4] = {ph[0], ph[1], ph[2], ph[3]};
-                const uint32_t pa_lo[4] = {pl[0], pl[1], pl[2], pl[3]};
 #pragma unroll
                 for (int np = 0; np < D / 16; ++np) {
                     uint32_t v0, v1, v2, v3;
                     const int tr = (lane & 7) + ((lane >> 3) & 1) * 8;
                     const int cc = np * 16 + (lane >> 4) * 8;
-                    ldsm_x4_trans(smem_addr(vst + tr * pitch + cc * 2), v0, v1, v2, v3);
+                    ldsm_x4_trans(vst + swz(tr, cc), v0, v1, v2, v3);
                     Elem<T>::mma(o[2 * np], pa_hi, v0, v1);
                     Elem<T>::mma(o[2 * np], pa_lo, v0, v1);
                     Elem<T>::mma(o[2 * np + 1], pa_hi, v2, v3);
@@ -534,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
         // ordered before the reads below).
         if (consumers_any(!ok)) break;
         // Merge the block-split warps of each row tile; write the output or the partial.
+        const int nparts = (ui.len + p.partition - 1) / p.partition;
         const int nthreads = kConsumerWarps * 32;
         for (int idx = threadIdx.x; idx < p.rows * D; idx += nthreads) {
             const int r = idx / D, e = idx - r * D;
@@ -552,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
             const int qi = r / p.group;
             const int h = ui.kvh * p.group + (r - qi * p.group);
             const long long orow = (long long)(ui.seq * p.q_len + qi) * p.num_heads + h;
-            if (ui.nparts == 1) {
+            if (nparts == 1) {
                 static_cast<uint16_t*>(p.out)[orow * D + e] = Elem<T>::to_bits(acc / lsum);
             } else {
                 const long long prow = ((long long)(ui.slot0 + ui.part) * p.q_len + qi) * p.num_heads + h;
@@ -703,13 +752,50 @@ struct Profile {
     bool created = false;
 } g_prof;
 
+// cuTensorMapEncodeTiled, fetched from the driver at first use (no link-time libcuda dependency).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// The pool [num_blocks, 16, Hkv, D] as a 4-D tensor (innermost first: D, Hkv, 16, num_blocks);
+// one box = 64 elements of one kv head for the 16 tokens of one block, 128-byte swizzled.
+int make_kv_map(CUtensorMap* map, const void* base, int dtype, int64_t num_blocks, int num_kv_heads, int head_dim) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return PA_ERR_CUDA;
+    const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)kBlock,
+                                (cuuint64_t)num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_kv_heads * head_dim * 2,
+                                   (cuuint64_t)kBlock * num_kv_heads * head_dim * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)kBoxCols, 1, (cuuint32_t)kBlock, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                           4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_INVALID_ARG;
+}
+
 template <typename T, int D>
 int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches) {
     const WsLayout w = ws_layout(a.num_seqs, a.q_len, a.num_heads, D, a.max_context_len, a.partition);
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     int* header = reinterpret_cast<int*>(ws + w.header);
     int* part_start = reinterpret_cast<int*>(ws + w.part_start);
-    int2* units = reinterpret_cast<int2*>(ws + w.units);
+    int4* units = reinterpret_cast<int4*>(ws + w.units);
     float2* pml = reinterpret_cast<float2*>(ws + w.pml);
     float* pacc = reinterpret_cast<float*>(ws + w.pacc);
 
@@ -731,14 +817,12 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     *launches += 1;
 
     DecodeParams p;
+    if (int st = make_kv_map(&p.tmap_k, a.key_cache, a.dtype, a.num_blocks, a.num_kv_heads, D)) return st;
+    if (int st = make_kv_map(&p.tmap_v, a.value_cache, a.dtype, a.num_blocks, a.num_kv_heads, D)) return st;
     p.out = a.out;
     p.query = a.query;
-    p.key_cache = a.key_cache;
-    p.value_cache = a.value_cache;
     p.block_tables = a.block_tables;
-    p.context_lens = a.context_lens;
     p.header = header;
-    p.part_start = part_start;
     p.units = units;
     p.pml = pml;
     p.pacc = pacc;
