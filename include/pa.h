@@ -77,6 +77,7 @@ typedef enum {
 #define PA_DEVERR_CONTEXT  0x2  /* context_lens[i] < q_len, < 1, > max_context_len or beyond the table */
 #define PA_DEVERR_SLOT     0x4  /* slot_mapping[t] >= num_blocks * block_size */
 #define PA_DEVERR_TIMEOUT  0x8  /* a bounded wait inside a kernel gave up (internal error) */
+#define PA_DEVERR_INTERNAL 0x10 /* a kernel refused an inconsistent launch configuration (library bug) */
 
 #define PA_BLOCK_SIZE 16
 #define PA_DEFAULT_PARTITION 512  /* tokens per split-K partition */

@@ -42,7 +42,19 @@ __device__ int g_pa_error;                            // PA_DEVERR_* bits
 constexpr int kBlock = 16;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kMaxStages = 8;
+// Depth of the shared-memory ring (stages of one 16-token K+V block) and the
+// number of decode CTAs meant to share an SM; the launcher picks the deepest
+// ring that fits that many CTAs.
+#ifndef PA_MAX_STAGES
+#define PA_MAX_STAGES 8
+#endif
+#ifndef PA_CTAS_PER_SM_NT1
+#define PA_CTAS_PER_SM_NT1 4  // kernels whose warps own 8 query rows
+#endif
+#ifndef PA_CTAS_PER_SM_NT2
+#define PA_CTAS_PER_SM_NT2 2  // kernels whose warps own 16 query rows
+#endif
+constexpr int kMaxStages = PA_MAX_STAGES;
 
 // ---------------------------------------------------------------------------
 // KV append
@@ -213,11 +225,11 @@ struct SmemLayout {
 };
 
 // Offsets from a 1024-byte aligned base (the swizzled TMA boxes need that alignment).
-__host__ __device__ inline SmemLayout smem_layout(int head_dim, int stages, int mtiles, int slot_rows) {
+__host__ __device__ inline SmemLayout smem_layout(int head_dim, int stages, int mtiles, int tile_rows, int slot_rows) {
     SmemLayout s;
     s.stage_bytes = 2 * (head_dim / kBoxCols) * kBoxBytes;  // K boxes then V boxes
     s.qpitch = head_dim * 2 + 16;                            // padded query rows
-    s.q_half_bytes = mtiles * 16 * s.qpitch;
+    s.q_half_bytes = mtiles * tile_rows * s.qpitch;
     s.off_q = stages * s.stage_bytes;
     s.off_comb = s.off_q + 2 * s.q_half_bytes;
     s.off_m = s.off_comb + kConsumerWarps * slot_rows * head_dim * 4;
@@ -243,6 +255,14 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Transpose of an 8x8 matrix of 16-bit values held as the standard fragment
+// (lane holds row lane/4, columns 2*(lane%4) and +1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // bar.red.or over the 128 consumer threads (named barrier 1): every thread
 // gets the OR of `v` across them.
 __device__ __forceinline__ bool consumers_any(bool v) {
@@ -258,11 +278,12 @@ __device__ __forceinline__ bool consumers_any(bool v) {
     return r != 0;
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
+template <typename T, int D, int NT>
+__global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CTAS_PER_SM_NT2)
+    decode_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const SmemLayout lay = smem_layout(D, p.stages, p.mtiles, p.slot_rows);
+    const SmemLayout lay = smem_layout(D, p.stages, p.mtiles, 8 * NT, p.slot_rows);
     const int qpitch = lay.qpitch;
     constexpr int kRowBytes = D * 2;
     constexpr int kBoxes = D / kBoxCols;  // boxes per K (or V) block
@@ -280,6 +301,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
     const uint32_t qfull0 = empty0 + 8 * kMaxStages;
     const uint32_t qempty0 = qfull0 + 16;
     const int stages = p.stages;
+    if (stages < p.block_splits || stages % p.block_splits != 0 || stages > kMaxStages ||
+        p.mtiles * p.block_splits != kConsumerWarps) {
+        if (threadIdx.x == 0) atomicOr(&g_pa_error, PA_DEVERR_INTERNAL);  // launcher bug: refuse to run
+        return;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -420,11 +446,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
     }
 
     // ===================== consumer warps =====================
+    // Transposed tiles, so that the few query rows of a kv head fill the N side of
+    // the m16n8k16 tensor-core tile instead of padding its M side:
+    //   S^T  = K Q^T     M = 16 tokens,      N = 8 query rows, K = head dim
+    //   O^T += V^T P^T   M = 16 head-dim cols, N = 8 query rows, K = 16 tokens
+    // Each warp owns NT groups of 8 query rows (one row tile) and every
+    // block_splits-th block of the unit.
+    constexpr int TR = 8 * NT;               // query rows per warp
     const int mt = warp / p.block_splits;   // row tile of this warp
     const int bsg = warp % p.block_splits;  // which of the tile's block-split warps
     const int gid = lane >> 2, tig = lane & 3;
-    const int row_lo = mt * 16 + gid, row_hi = row_lo + 8;
-    const int rows_here = min(16, p.rows - mt * 16);
+    const int rows_here = min(TR, p.rows - mt * TR);  // <= 0 for an all-padding tile
     uint32_t k = 0;
     int ul = 0;
     for (long long u = blockIdx.x; u < total_units; u += gridDim.x, ++ul) {
@@ -432,31 +464,45 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
         // (all waits below are made warp-uniform: a timeout seen by one lane stops the warp)
         bool ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8 * qb, (ul >> 1) & 1, &g_pa_error, abort_flag));
         UnitInfo ui = info[qb];
-        uint32_t qa[D / 16][4];
-        float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
-        float o[D / 8][4];
+        uint32_t qf[NT][D / 16][2];      // Q^T as the B operand: Q[row][d 2t..2t+1], Q[row][d 2t+8..2t+9]
+        float m[NT][2], l[NT][2];        // running max (log2 units) and sum for rows 2t, 2t+1 of each group
+        float o[D / 16][NT][4];          // O^T: (d gid, row 2t), (d gid, row 2t+1), (d gid+8, 2t), (d gid+8, 2t+1)
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
+            m[nt][0] = m[nt][1] = -INFINITY;
+            l[nt][0] = l[nt][1] = 0.f;
+        }
+#pragma unroll
+        for (int dt = 0; dt < D / 16; ++dt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) o[dt][nt][0] = o[dt][nt][1] = o[dt][nt][2] = o[dt][nt][3] = 0.f;
         int nblk = 0;
         if (ok) {
-            const uint8_t* qrow = qbuf + qb * lay.q_half_bytes + mt * 16 * qpitch;
+            const uint8_t* qrow = qbuf + qb * lay.q_half_bytes + mt * TR * qpitch;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const int rr = (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int cc = kk * 16 + (lane >> 4) * 8;
-                ldsm_x4(smem_addr(qrow + rr * qpitch + cc * 2), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-            }
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int k2 = 0; k2 < D / 32; ++k2) {
+                    const int rr = nt * 8 + (lane & 7);
+                    const int cc = k2 * 32 + (lane >> 3) * 8;
+                    ldsm_x4(smem_addr(qrow + rr * qpitch + cc * 2), qf[nt][2 * k2][0], qf[nt][2 * k2][1],
+                            qf[nt][2 * k2 + 1][0], qf[nt][2 * k2 + 1][1]);
+                }
             __syncwarp();
             if (lane == 0) mbar_arrive(qempty0 + 8 * qb);
 
             nblk = (ui.ntok + kBlock - 1) / kBlock;
             const int tok0 = ui.part * p.partition;
-            // Last position (relative to the partition) each of this lane's two rows may see:
+            // Last position (relative to the partition) each of this lane's rows may see:
             // row j of the q_len-row chunk is position L - q_len + j.
-            const int qi_lo = min(row_lo / p.group, p.q_len - 1);
-            const int qi_hi = min(row_hi / p.group, p.q_len - 1);
-            const int lim_lo = ui.len - p.q_len + qi_lo - tok0;
-            const int lim_hi = ui.len - p.q_len + qi_hi - tok0;
+            int lim[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int r = mt * TR + nt * 8 + 2 * tig + c;
+                    lim[nt][c] = ui.len - p.q_len + min(r / p.group, p.q_len - 1) - tok0;
+                }
             const int first = (bsg - (int)(k % p.block_splits) + p.block_splits) % p.block_splits;
             for (int j = first; j < nblk; j += p.block_splits) {
                 const uint32_t kj = k + j;
@@ -467,116 +513,118 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
                 }
                 const uint32_t kst = smem_addr(stage_base + s * lay.stage_bytes);
                 const uint32_t vst = kst + kBoxes * kBoxBytes;
-                // smem row r holds token r - shift of this block (shift > 0 only for a short last block)
+                // smem row i holds token i - shift of this block (shift > 0 only for a short last block)
                 const int shift = kBlock - min(kBlock, ui.ntok - kBlock * j);
-                // S = Q K^T for 16 rows x 16 tokens.
-                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                float sc[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    uint32_t b0, b1, b2, b3;
-                    const int tr = (lane >> 4) * 8 + (lane & 7);
-                    const int cc = kk * 16 + ((lane >> 3) & 1) * 8;
-                    ldsm_x4(kst + swz(tr, cc), b0, b1, b2, b3);
-                    Elem<T>::mma(sc[0], qa[kk], b0, b1);
-                    Elem<T>::mma(sc[1], qa[kk], b2, b3);
-                }
-                // Scale into log2 units and mask positions past each row's limit.
-                const int tb = kBlock * j - shift + 2 * tig;
+                    uint32_t a[4];
+                    const int tr = (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const int cc = kk * 16 + (lane >> 4) * 8;
+                    ldsm_x4(kst + swz(tr, cc), a[0], a[1], a[2], a[3]);
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
+                    for (int nt = 0; nt < NT; ++nt) Elem<T>::mma(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+                }
+                // Scale into log2 units; mask positions past each row's limit (and the zero rows
+                // in front of a short block).
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const int r = nt * 8 + 2 * tig + (c & 1);
-                        const int tok = tb + nt * 8 + (c & 1);
-                        const int lim = c < 2 ? lim_lo : lim_hi;
-                        sc[nt][c] = (r >= shift && tok <= lim) ? sc[nt][c] * p.scale_log2 : -INFINITY;
+                        const int i = gid + (c >> 1) * 8;
+                        const int tok = kBlock * j + i - shift;
+                        sc[nt][c] = (i >= shift && tok <= lim[nt][c & 1]) ? sc[nt][c] * p.scale_log2 : -INFINITY;
                     }
-                }
-                float mx_lo = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-                float mx_hi = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-                mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-                mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-                mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-                mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-                const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-                const float base_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
-                const float base_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
-                const float a_lo = ex2(m_lo - base_lo), a_hi = ex2(m_hi - base_hi);
-                m_lo = mn_lo;
-                m_hi = mn_hi;
-                float pr[2][4];
+                float alpha[NT][2], pr[NT][4];
+                bool rescale = false;
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    pr[nt][0] = ex2(sc[nt][0] - base_lo);
-                    pr[nt][1] = ex2(sc[nt][1] - base_lo);
-                    pr[nt][2] = ex2(sc[nt][2] - base_hi);
-                    pr[nt][3] = ex2(sc[nt][3] - base_hi);
-                }
-                l_lo = l_lo * a_lo + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
-                l_hi = l_hi * a_hi + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
-                if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int n = 0; n < D / 8; ++n) {
-                        o[n][0] *= a_lo;
-                        o[n][1] *= a_lo;
-                        o[n][2] *= a_hi;
-                        o[n][3] *= a_hi;
+                    for (int c = 0; c < 2; ++c) {
+                        float mx = fmaxf(sc[nt][c], sc[nt][c + 2]);
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                        const float mn = fmaxf(m[nt][c], mx);
+                        const float base = mn == -INFINITY ? 0.f : mn;
+                        alpha[nt][c] = ex2(m[nt][c] - base);
+                        rescale |= alpha[nt][c] != 1.f;
+                        m[nt][c] = mn;
+                        pr[nt][c] = ex2(sc[nt][c] - base);
+                        pr[nt][c + 2] = ex2(sc[nt][c + 2] - base);
+                        l[nt][c] = l[nt][c] * alpha[nt][c] + (pr[nt][c] + pr[nt][c + 2]);
                     }
-                }
-                // P as the A operand in two 16-bit pieces (hi + residual): together they
-                // carry about 16 significant bits, so P.V loses nothing a single rounding
-                // of P would.  A-fragment order: (row lo, tokens 0-7), (row hi, 0-7),
-                // (row lo, 8-15), (row hi, 8-15).
-                uint32_t pa_hi[4], pa_lo[4];
+                if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int nt = q >> 1, c0 = (q & 1) * 2;
-                    const float x0 = pr[nt][c0], x1 = pr[nt][c0 + 1];
-                    const float h0 = Elem<T>::round_trip(x0), h1 = Elem<T>::round_trip(x1);
-                    pa_hi[q] = Elem<T>::pack(h0, h1);
-                    pa_lo[q] = Elem<T>::pack(x0 - h0, x1 - h1);
-                }
+                    for (int dt = 0; dt < D / 16; ++dt)
 #pragma unroll
-                for (int np = 0; np < D / 16; ++np) {
-                    uint32_t v0, v1, v2, v3;
-                    const int tr = (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const int cc = np * 16 + (lane >> 4) * 8;
-                    ldsm_x4_trans(vst + swz(tr, cc), v0, v1, v2, v3);
-                    Elem<T>::mma(o[2 * np], pa_hi, v0, v1);
-                    Elem<T>::mma(o[2 * np], pa_lo, v0, v1);
-                    Elem<T>::mma(o[2 * np + 1], pa_hi, v2, v3);
-                    Elem<T>::mma(o[2 * np + 1], pa_lo, v2, v3);
+                        for (int nt = 0; nt < NT; ++nt) {
+                            o[dt][nt][0] *= alpha[nt][0];
+                            o[dt][nt][1] *= alpha[nt][1];
+                            o[dt][nt][2] *= alpha[nt][0];
+                            o[dt][nt][3] *= alpha[nt][1];
+                        }
+                }
+                // P^T as the B operand, in two 16-bit pieces (hi + residual) that together carry
+                // about 16 significant bits.  The lane's (token, row-pair) values form the standard
+                // fragment of P^T's 8x8 sub-tiles; movmatrix transposes them into (row, token-pair).
+                uint32_t pb_hi[NT][2], pb_lo[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float x0 = pr[nt][2 * h], x1 = pr[nt][2 * h + 1];
+                        const float h0 = Elem<T>::round_trip(x0), h1 = Elem<T>::round_trip(x1);
+                        pb_hi[nt][h] = movmatrix_trans(Elem<T>::pack(h0, h1));
+                        pb_lo[nt][h] = movmatrix_trans(Elem<T>::pack(x0 - h0, x1 - h1));
+                    }
+#pragma unroll
+                for (int dt = 0; dt < D / 16; ++dt) {
+                    uint32_t a[4];
+                    const int tr = (lane & 7) + (lane >> 4) * 8;
+                    const int cc = dt * 16 + ((lane >> 3) & 1) * 8;
+                    ldsm_x4_trans(vst + swz(tr, cc), a[0], a[1], a[2], a[3]);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        Elem<T>::mma(o[dt][nt], a, pb_hi[nt][0], pb_hi[nt][1]);
+                        Elem<T>::mma(o[dt][nt], a, pb_lo[nt][0], pb_lo[nt][1]);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty0 + 8 * s);
             }
         }
         k += nblk;
-        // Row sums over the quad of lanes sharing a row.
-        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+        // Row sums over the eight lanes (same tig) that hold a row's tokens.
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                l[nt][c] += __shfl_xor_sync(0xffffffffu, l[nt][c], 4);
+                l[nt][c] += __shfl_xor_sync(0xffffffffu, l[nt][c], 8);
+                l[nt][c] += __shfl_xor_sync(0xffffffffu, l[nt][c], 16);
+            }
         if (ok) {
             float* co = comb_o + warp * p.slot_rows * D;
-            if (gid < rows_here) {
 #pragma unroll
-                for (int n = 0; n < D / 8; ++n)
-                    *reinterpret_cast<float2*>(co + gid * D + n * 8 + 2 * tig) = make_float2(o[n][0], o[n][1]);
-                if (tig == 0) {
-                    comb_m[warp * 16 + gid] = m_lo;
-                    comb_l[warp * 16 + gid] = l_lo;
-                }
-            }
-            if (gid + 8 < rows_here) {
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int n = 0; n < D / 8; ++n)
-                    *reinterpret_cast<float2*>(co + (gid + 8) * D + n * 8 + 2 * tig) = make_float2(o[n][2], o[n][3]);
-                if (tig == 0) {
-                    comb_m[warp * 16 + gid + 8] = m_hi;
-                    comb_l[warp * 16 + gid + 8] = l_hi;
+                for (int c = 0; c < 2; ++c) {
+                    const int row = nt * 8 + 2 * tig + c;
+                    if (row < rows_here) {
+#pragma unroll
+                        for (int dt = 0; dt < D / 16; ++dt) {
+                            co[row * D + dt * 16 + gid] = o[dt][nt][c];
+                            co[row * D + dt * 16 + gid + 8] = o[dt][nt][c + 2];
+                        }
+                        if (gid == 0) {
+                            comb_m[warp * 16 + row] = m[nt][c];
+                            comb_l[warp * 16 + row] = l[nt][c];
+                        }
+                    }
                 }
-            }
         }
         // All consumer warps agree on whether to go on (and the buffer writes above are
         // ordered before the reads below).
@@ -586,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
         const int nthreads = kConsumerWarps * 32;
         for (int idx = threadIdx.x; idx < p.rows * D; idx += nthreads) {
             const int r = idx / D, e = idx - r * D;
-            const int tile = r >> 4, rr = r & 15;
+            const int tile = r / TR, rr = r - tile * TR;
             float M = -INFINITY;
             for (int b = 0; b < p.block_splits; ++b) M = fmaxf(M, comb_m[(tile * p.block_splits + b) * 16 + rr]);
             float lsum = 0.f, acc = 0.f;
@@ -834,19 +882,33 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     p.group = a.num_heads / a.num_kv_heads;
     p.rows = p.group * a.q_len;
     p.partition = a.partition;
-    p.mtiles = (p.rows + 15) / 16;
-    p.block_splits = kConsumerWarps / p.mtiles;
-    p.slot_rows = std::min(16, p.rows);
     p.scale_log2 = a.scale * 1.4426950408889634f;
+    // Each consumer warp owns 8 (NT = 1) or 16 (NT = 2) query rows of the kv head; the row
+    // tiles per kv head are rounded up to a divisor of the consumer warp count (a third
+    // tile becomes a fourth, all-padding one) so that every consumer warp owns exactly one
+    // (row tile, block split) pair.
+    const int nt = p.rows <= 8 ? 1 : 2;
+    const int tile_rows = 8 * nt;
+    p.mtiles = (p.rows + tile_rows - 1) / tile_rows;
+    if (p.mtiles == 3) p.mtiles = 4;
+    if (p.mtiles > kConsumerWarps || kConsumerWarps % p.mtiles != 0) return PA_ERR_UNSUPPORTED;
+    p.block_splits = kConsumerWarps / p.mtiles;
+    p.slot_rows = std::min(tile_rows, p.rows);
 
-    // Deepest ring (a multiple of block_splits) that still lets two CTAs share an SM.
-    const void* fn = reinterpret_cast<const void*>(decode_kernel<T, D>);
-    int stages = kMaxStages;
-    SmemLayout lay = smem_layout(D, stages, p.mtiles, p.slot_rows);
-    const int per_sm_budget = 227 * 1024 / 2 - 1024;
+    const void* fn = nt == 1 ? reinterpret_cast<const void*>(decode_kernel<T, D, 1>)
+                             : reinterpret_cast<const void*>(decode_kernel<T, D, 2>);
+    const int ctas_target = nt == 1 ? PA_CTAS_PER_SM_NT1 : PA_CTAS_PER_SM_NT2;
+    // Deepest ring that still lets ctas_target CTAs share an SM.  Its length must be a
+    // multiple of block_splits: then every stage is always consumed by the same warps,
+    // which wait its phases strictly in order (a waiter two phases ahead of a barrier
+    // would see its parity as already complete).
+    int stages = (kMaxStages / p.block_splits) * p.block_splits;
+    if (stages < p.block_splits) return PA_ERR_UNSUPPORTED;
+    SmemLayout lay = smem_layout(D, stages, p.mtiles, tile_rows, p.slot_rows);
+    const int per_sm_budget = 228 * 1024 / ctas_target - 1024;
     while (stages > p.block_splits && lay.total > per_sm_budget) {
         stages -= p.block_splits;
-        lay = smem_layout(D, stages, p.mtiles, p.slot_rows);
+        lay = smem_layout(D, stages, p.mtiles, tile_rows, p.slot_rows);
     }
     if (lay.total > dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
     p.stages = stages;
@@ -857,7 +919,10 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
 
     const bool prof = g_prof.on && g_prof.n < 4096;
     if (prof) cudaEventRecord(g_prof.ev[2 * g_prof.n], stream);
-    decode_kernel<T, D><<<grid, kThreads, lay.total, stream>>>(p);
+    if (nt == 1)
+        decode_kernel<T, D, 1><<<grid, kThreads, lay.total, stream>>>(p);
+    else
+        decode_kernel<T, D, 2><<<grid, kThreads, lay.total, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (prof) {
         cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], stream);

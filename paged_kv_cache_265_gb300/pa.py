@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpa.so")
 
 PA_BF16, PA_FP16 = 0, 1
-PA_DEVERR_BLOCK_ID, PA_DEVERR_CONTEXT, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT = 1, 2, 4, 8
+PA_DEVERR_BLOCK_ID, PA_DEVERR_CONTEXT, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT, PA_DEVERR_INTERNAL = 1, 2, 4, 8, 16
 BLOCK_SIZE = 16
 DEFAULT_PARTITION = 512
 

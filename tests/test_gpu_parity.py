@@ -75,6 +75,7 @@ EDGE = [
     ([16, 40, 1200], 16, 1, 128, 1, "fp16"),                # 16 rows: one full row tile
     ([9, 64, 999], 32, 4, 128, 3, "bf16"),                  # 24 rows: two row tiles
     ([12, 300, 1600], 8, 1, 64, 8, "bf16"),                 # 64 rows: four row tiles
+    ([5, 77, 1300], 16, 2, 128, 5, "bf16"),                 # 40 rows: three row tiles (+1 padding tile)
 ]
 
 
