@@ -171,6 +171,40 @@ int pa_decode_attention_ex(void* out, const void* query, const void* key_cache, 
                            int max_context_len, float scale, int dtype, int partition_size,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Decode attention that allocates nothing, not even a workspace argument.
+ * (The pages describe no such call; it exists for callers of this library.)
+ *
+ * Some callers cannot hand the library a workspace: a host program that reaches
+ * the GPU only through this C ABI and has no device allocator of its own, or a
+ * serving process whose allocator has reserved all device memory up front (the
+ * pages' gpu_memory_utilization budget) and allows no further cudaMalloc, whose
+ * implicit device-wide synchronisation would also stall a decode loop.  This
+ * variant computes exactly what pa_decode_attention_ex computes, with the same
+ * arguments minus the workspace, and takes its split-K scratch from a fixed
+ * array inside the library:
+ *   - the array holds PA_NOALLOC_WORKSPACE_BYTES (32 MiB) on every GPU that
+ *     loads the library, until the process exits;
+ *   - a call whose pa_decode_workspace_size_ex() exceeds that returns
+ *     PA_ERR_WORKSPACE and enqueues nothing (use pa_decode_attention_ex then);
+ *   - the first call on each device looks up the array's device address (a
+ *     runtime symbol query, no allocation) with that device current; make that
+ *     first call before any stream capture;
+ *   - every call on a device shares the one array, which keeps the last call's
+ *     contents (each call rewrites all of it that it reads, so nothing needs
+ *     clearing); calls that overlap on the GPU, on different streams or from
+ *     different threads, race on it and must be serialised by the caller.
+ * No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+#define PA_NOALLOC_WORKSPACE_BYTES (32u << 20)
+
+int pa_decode_attention_noalloc(void* out, const void* query, const void* key_cache,
+                                const void* value_cache, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                                int q_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                int64_t num_blocks, int max_context_len, float scale, int dtype,
+                                int partition_size, void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* pa_status_string(int status);
 

@@ -151,6 +151,27 @@ int pa_decode_attention_multiquery(void* out, const void* query, const void* key
                                   num_blocks, max_context_len, scale, dtype, 0, workspace, workspace_bytes, stream);
 }
 
+int pa_decode_attention_noalloc(void* out, const void* query, const void* key_cache, const void* value_cache,
+                                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                                int num_seqs, int q_len, int num_heads, int num_kv_heads, int head_dim,
+                                int block_size, int64_t num_blocks, int max_context_len, float scale, int dtype,
+                                int partition_size, void* stream) {
+    t_last_launches = 0;
+    const int st = check_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                                context_lens, num_seqs, q_len, num_heads, num_kv_heads, head_dim, block_size,
+                                num_blocks, max_context_len, scale, dtype, partition_size);
+    if (st != PA_OK || num_seqs == 0) return st;
+    const int partition = partition_size == 0 ? PA_DEFAULT_PARTITION : partition_size;
+    const size_t need = pa::ws_layout(num_seqs, q_len, num_heads, head_dim, max_context_len, partition).total;
+    if (need > (size_t)PA_NOALLOC_WORKSPACE_BYTES) return PA_ERR_WORKSPACE;  // too big for the fixed scratch
+    void* scratch = nullptr;
+    if (const int ws = pa::noalloc_workspace(&scratch)) return ws;
+    return pa_decode_attention_ex(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                                  context_lens, num_seqs, q_len, num_heads, num_kv_heads, head_dim, block_size,
+                                  num_blocks, max_context_len, scale, dtype, partition_size, scratch,
+                                  (size_t)PA_NOALLOC_WORKSPACE_BYTES, stream);
+}
+
 int pa_get_device_error(int32_t* host_flags, int clear, void* stream) {
     if (!host_flags) return PA_ERR_INVALID_ARG;
     return pa::read_device_error(host_flags, clear, static_cast<cudaStream_t>(stream));

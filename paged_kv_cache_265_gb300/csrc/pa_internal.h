@@ -77,6 +77,10 @@ int launch_reshape_and_cache(const void* key, const void* value, void* key_cache
 int launch_decode(const DecodeArgs& a, cudaStream_t stream, int* launches);
 int read_device_error(int32_t* flags, int clear, cudaStream_t stream);
 
+// Device address of the library's fixed scratch array on the current device
+// (looked up on the first call per device, then cached).
+int noalloc_workspace(void** ptr);
+
 // Benchmark timing hook around the main decode kernel.
 int profile_enable(int on);
 int profile_read(float* total_ms, int* launches);

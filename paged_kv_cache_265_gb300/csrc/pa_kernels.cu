@@ -1024,4 +1024,36 @@ int profile_read(float* total_ms, int* launches) {
     return PA_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Fixed scratch for pa_decode_attention_noalloc.
+//
+// Callers that must not allocate device memory get their split-K workspace from
+// this array instead of passing one in.  It is a module global: every GPU that
+// loads the library holds PA_NOALLOC_WORKSPACE_BYTES of it until the process
+// exits.  In host code `g_noalloc_workspace` only names the array; its device
+// address is looked up once per device with cudaGetSymbolAddress (with that
+// device current) and cached.  All calls share the array and it keeps the last
+// call's contents; the decode kernels rewrite every byte they read from it on
+// each call (work list, partials), so nothing needs clearing between calls.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_workspace[PA_NOALLOC_WORKSPACE_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+}  // namespace
+
+int noalloc_workspace(void** ptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || !p) return PA_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return PA_OK;
+}
+
 }  // namespace pa

@@ -21,6 +21,7 @@ PA_BF16, PA_FP16 = 0, 1
 PA_DEVERR_BLOCK_ID, PA_DEVERR_CONTEXT, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT, PA_DEVERR_INTERNAL = 1, 2, 4, 8, 16
 BLOCK_SIZE = 16
 DEFAULT_PARTITION = 512
+NOALLOC_WORKSPACE_BYTES = 32 << 20
 
 _DT = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16}
 
@@ -37,6 +38,8 @@ _SIGS = {
                                                 _vp]),
     "pa_decode_attention_ex": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int,
                                         _c_int, _c_int, _c_i64, _c_int, _c_f, _c_int, _c_int, _vp, _c_sz, _vp]),
+    "pa_decode_attention_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int,
+                                             _c_int, _c_int, _c_i64, _c_int, _c_f, _c_int, _c_int, _vp]),
     "pa_status_string": (ctypes.c_char_p, [_c_int]),
     "pa_get_device_error": (_c_int, [ctypes.POINTER(ctypes.c_int32), _c_int, _vp]),
     "pa_profile_enable": (_c_int, [_c_int]),
@@ -156,6 +159,40 @@ def decode_attention(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Te
         hq, hkv, d, bs, nb, int(max_context_len), float(scale), dtype_code(query), int(partition_size),
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream))
     _check("pa_decode_attention_ex", st)
+    return out
+
+
+def decode_attention_noalloc(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                             value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                             scale: float, max_context_len: int, partition_size: int = 0, stream=None) -> torch.Tensor:
+    """decode_attention without a workspace argument, for callers that cannot allocate device
+    memory: the split-K scratch comes from the library's fixed 32 MiB device array.  Calls share
+    that array, so calls that overlap on the GPU must not be issued; a problem needing more
+    scratch than the array holds raises PaError (status PA_ERR_WORKSPACE)."""
+    if query.dim() == 3:
+        n, hq, d = query.shape
+        q_len = 1
+    elif query.dim() == 4:
+        n, q_len, hq, d = query.shape
+    else:
+        raise ValueError("query must be [N, Hq, d] or [N, q_len, Hq, d]")
+    if out.shape != query.shape or out.dtype != query.dtype:
+        raise ValueError("out must match query in shape and dtype")
+    nb, bs, hkv, d2 = key_cache.shape
+    if d2 != d or value_cache.shape != key_cache.shape:
+        raise ValueError("cache shape mismatch")
+    if query.dtype != key_cache.dtype or value_cache.dtype != key_cache.dtype:
+        raise ValueError("query and caches must share one dtype")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != n or context_lens.shape != (n,):
+        raise ValueError("block_tables must be [N, max_blocks] and context_lens [N]")
+    st = lib().pa_decode_attention_noalloc(
+        _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(block_tables, "block_tables"), block_tables.shape[1], _dev(context_lens, "context_lens"), n, q_len,
+        hq, hkv, d, bs, nb, int(max_context_len), float(scale), dtype_code(query), int(partition_size),
+        _stream(stream))
+    _check("pa_decode_attention_noalloc", st)
     return out
 
 
