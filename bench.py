@@ -319,8 +319,7 @@ def run_ours(args, rank, world, local):
     if step_bytes < 2 * L2_BYTES:   # small working set: flush L2 between steps
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
 
-    # --- device-resident timed region
-    pa.profile_enable(True)
+    # --- device-resident timed region (the hot path exactly as a caller runs it)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     flush_ms = 0.0
     with ClockSampler(local) as clocks:
@@ -334,8 +333,6 @@ def run_ours(args, rank, world, local):
         stop.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
-    pa.profile_enable(False)
-    kern_ms_total, kern_n = pa.profile_read()
     total_ms = start.elapsed_time(stop)
     if flush is not None:
         fs, fe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -347,6 +344,21 @@ def run_ours(args, rank, world, local):
         flush_ms = fs.elapsed_time(fe)
     step_ms_local = max(1e-9, (total_ms - flush_ms) / args.steps)
     step_ms = max_over_ranks(step_ms_local, world, dev)
+
+    # --- partition-kernel time for the roofline: the same steps again, with the library's
+    # CUDA-event pair recorded around every partition-kernel launch on the launch stream.
+    # (Events between launches suspend the programmatic overlap of launch set-up, which is
+    # why the step itself is timed without them.)
+    prof_steps = min(args.steps, 4096)
+    pa.profile_enable(True)
+    pa.profile_read()
+    for _ in range(prof_steps):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    pa.profile_enable(False)
+    kern_ms_total, kern_n = pa.profile_read()
     err = pa.get_device_error(clear=True)
 
     # --- end to end through the public API: host inputs in, host output back, every step
@@ -406,6 +418,7 @@ def run_ours(args, rank, world, local):
                      "kernel": "decode_kernel (partition pass)", "kernel_ms": kern_ms,
                      "traffic": traffic},
         "gpu_launches": launches_per_step * args.steps,
+        "roofline_steps": kern_n,
         "clocks": clocks.summary(),
         "device_error_flags": err,
         "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,

@@ -9,7 +9,8 @@
 namespace pa {
 
 // Workspace of one decode call (byte offsets from the workspace base).
-//   header      int32[64]: [0] = number of (sequence, partition) work entries
+//   header      int32[64]: [0] = number of (sequence, partition) work entries,
+//               [1] = dynamic work counter
 //   part_start  int32[N+1]: first partial slot of each sequence (exclusive scan)
 //   units       int4[N * Pmax]: work entries (sequence, partition, context length,
 //               first partial slot), full partitions first, then each

@@ -28,6 +28,7 @@
 #include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <utility>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -66,6 +67,7 @@ __global__ void __launch_bounds__(256) reshape_kernel(const uint4* __restrict__ 
                                                       const long long* __restrict__ slots,
                                                       long long num_tokens, int row_vecs,
                                                       long long num_slots) {
+    griddep_launch_dependents();
     const long long per_token = 2LL * row_vecs;
     const long long total = num_tokens * per_token;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
@@ -91,10 +93,11 @@ __global__ void __launch_bounds__(256) reshape_kernel(const uint4* __restrict__ 
 // ---------------------------------------------------------------------------
 struct PlanParams {
     const int* context_lens;
-    int* header;
+    int* header;        // [0] work entries, [1] dynamic work counter (reset here)
     int* part_start;
     int4* units;
     int num_seqs;
+    int num_kv_heads;
     int q_len;
     int partition;
     int max_blocks_per_seq;
@@ -128,52 +131,71 @@ __device__ int block_exclusive_scan(int v, int* scratch32, int& total) {
     return before + x - v;
 }
 
-__device__ __forceinline__ void seq_parts(const PlanParams& p, int i, int& full, int& partial) {
-    full = partial = 0;
-    if (i >= p.num_seqs) return;
+__device__ __forceinline__ int seq_parts(const PlanParams& p, int i) {
+    if (i >= p.num_seqs) return 0;
     const int L = p.context_lens[i];
     const bool ok = L >= 1 && L >= p.q_len && L <= p.max_context_len &&
                     (L + kBlock - 1) / kBlock <= p.max_blocks_per_seq;
     if (!ok) {
         atomicOr(&g_pa_error, PA_DEVERR_CONTEXT);
-        return;
+        return 0;
     }
-    full = L / p.partition;
-    partial = (L % p.partition) != 0;
+    return (L + p.partition - 1) / p.partition;
 }
 
+// Size bucket of a partition: its block count, capped; larger buckets go first.
+constexpr int kPlanBuckets = 64;
+__device__ __forceinline__ int part_bucket(const PlanParams& p, int L, int part) {
+    const int nb = (min(p.partition, L - part * p.partition) + kBlock - 1) / kBlock;
+    return min(nb, kPlanBuckets - 1);
+}
+
+// One CTA: numbers each sequence's partitions (part_start), then lays the
+// (sequence, partition) entries out largest first (a counting sort on block
+// count), so that CTAs taking entries in order finish close together.  The
+// order within a size bucket does not affect any result.
 __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
+    griddep_launch_dependents();  // the partition pass may start its set-up now ...
+    griddep_wait();               // ... but the lengths may come from the kernel before this one
     __shared__ int scratch[32];
-    // Pass 1: number of full partitions (they go first in the list).
-    int total_full = 0;
-    for (int base = 0; base < p.num_seqs; base += 1024) {
-        int full, partial, tot;
-        seq_parts(p, base + threadIdx.x, full, partial);
-        block_exclusive_scan(full, scratch, tot);
-        total_full += tot;
-    }
-    // Pass 2: slots, full entries, partial entries.
-    int carry_slot = 0, carry_full = 0, carry_part = 0;
+    __shared__ int hist[kPlanBuckets];
+    if (threadIdx.x < kPlanBuckets) hist[threadIdx.x] = 0;
+    __syncthreads();
+    int carry = 0;
     for (int base = 0; base < p.num_seqs; base += 1024) {
         const int i = base + threadIdx.x;
-        int full, partial, t_slot, t_full, t_part;
-        seq_parts(p, i, full, partial);
-        const int slot = carry_slot + block_exclusive_scan(full + partial, scratch, t_slot);
-        const int fpos = carry_full + block_exclusive_scan(full, scratch, t_full);
-        const int ppos = carry_part + block_exclusive_scan(partial, scratch, t_part);
+        const int np = seq_parts(p, i);
+        int tot;
+        const int slot = carry + block_exclusive_scan(np, scratch, tot);
         if (i < p.num_seqs) {
             p.part_start[i] = slot;
             const int L = p.context_lens[i];
-            for (int c = 0; c < full; ++c) p.units[fpos + c] = make_int4(i, c, L, slot);
-            if (partial) p.units[total_full + ppos] = make_int4(i, full, L, slot);
+            for (int c = 0; c < np; ++c) atomicAdd(&hist[part_bucket(p, L, c)], 1);
         }
-        carry_slot += t_slot;
-        carry_full += t_full;
-        carry_part += t_part;
+        carry += tot;
     }
+    __syncthreads();
     if (threadIdx.x == 0) {
-        p.part_start[p.num_seqs] = carry_slot;
-        p.header[0] = carry_full + carry_part;
+        int run = 0;  // bucket starts, largest bucket first
+        for (int b = kPlanBuckets - 1; b >= 0; --b) {
+            const int n = hist[b];
+            hist[b] = run;
+            run += n;
+        }
+        p.part_start[p.num_seqs] = carry;
+        p.header[0] = carry;
+        p.header[1] = 0;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) {
+        const int np = seq_parts(p, i);
+        if (np == 0) continue;
+        const int L = p.context_lens[i];
+        const int slot = p.part_start[i];
+        for (int c = 0; c < np; ++c) {
+            const int pos = atomicAdd(&hist[part_bucket(p, L, c)], 1);
+            p.units[pos] = make_int4(i, c, L, slot);
+        }
     }
 }
 
@@ -190,14 +212,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
 constexpr int kBoxCols = 64;                       // elements per box row (128 B)
 constexpr int kBoxBytes = kBlock * kBoxCols * 2;   // 2 KB
 
-struct alignas(64) DecodeParams {
+struct alignas(128) DecodeParams {
     CUtensorMap tmap_k;  // [num_blocks, 16, Hkv, D] viewed as 4-D, box {64, 1, 16, 1}
     CUtensorMap tmap_v;
     void* out;
     const void* query;
     const int* block_tables;
     const int* header;
-    const int4* units;   // (seq, partition, context_len, first partial slot)
+    int* work_counter;   // next work unit to hand out (reset by the plan kernel)
+    const int4* units;   // (seq, partition, context_len, first partial slot), largest first
     float2* pml;
     float* pacc;
     long long num_blocks;
@@ -325,6 +348,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CT
     fence_proxy_async_smem();
     __syncthreads();
 
+    griddep_launch_dependents();  // the merge kernel may be scheduled as CTAs retire
+    griddep_wait();               // the work list (and the appended K/V) must be complete
     const long long total_units = (long long)p.header[0] * p.num_kv_heads;
 
     if (warp == kConsumerWarps) {
@@ -335,9 +360,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CT
         uint32_t k = 0;
         int ul = 0;
         bool ok = true;
-        long long u = blockIdx.x;
-        // Work-entry metadata and the first 32 block ids of the next unit are fetched
-        // while the current unit streams, so a unit starts without dependent loads.
+        // Units are handed out dynamically, largest first.  The next unit's number, its
+        // work entry and its first 32 block ids are fetched while the current unit
+        // streams, so a unit starts without dependent loads.
+        long long u = 0;
+        if (lane == 0) u = atomicAdd(p.work_counter, 1);
+        u = __shfl_sync(0xffffffffu, u, 0);
         int4 cur = make_int4(0, 0, 0, 0);
         int bids = 0;
         if (u < total_units) {
@@ -347,21 +375,33 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CT
                 bids = __ldg(p.block_tables + (long long)cur.x * p.max_blocks_per_seq +
                              (long long)cur.y * blocks_per_part + lane);
         }
-        for (; u < total_units && ok; u += gridDim.x, ++ul) {
-            const int kvh = (int)(u % p.num_kv_heads);
-            const int seq = cur.x, part = cur.y, L = cur.z;
-            const int tok0 = part * p.partition;
-            const int ntok = min(p.partition, L - tok0);
-            const int nblk = (ntok + kBlock - 1) / kBlock;
-            const long long un = u + gridDim.x;
-            const int4 nxt = un < total_units ? p.units[un / p.num_kv_heads] : make_int4(0, 0, 0, 0);
-            int nbids = 0;
+        for (; ok; ++ul) {
             const int qb = ul & 1;
             if (ul >= 2 &&
                 !__all_sync(0xffffffffu, mbar_wait(qempty0 + 8 * qb, ((ul - 2) >> 1) & 1, &g_pa_error, abort_flag))) {
                 ok = false;
                 break;
             }
+            if (u >= total_units) {  // no work left: hand the consumers an end marker
+                if (lane == 0) {
+                    info[qb].seq = -1;
+                    mbar_arrive(qfull0 + 8 * qb);
+                }
+                ++ul;
+                break;
+            }
+            const int kvh = (int)(u % p.num_kv_heads);
+            const int seq = cur.x, part = cur.y, L = cur.z;
+            const int tok0 = part * p.partition;
+            const int ntok = min(p.partition, L - tok0);
+            const int nblk = (ntok + kBlock - 1) / kBlock;
+            // Next unit: its number is requested now and read two blocks later, its entry is
+            // loaded then and its block ids two blocks after that, so no step waits.
+            int un_req = 0;
+            if (lane == 0) un_req = atomicAdd(p.work_counter, 1);
+            long long un = total_units;
+            int4 nxt = make_int4(0, 0, 0, 0);
+            int nbids = 0;
             if (lane == 0) {
                 UnitInfo ui;
                 ui.seq = seq;
@@ -383,7 +423,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CT
                          pol_keep);
             }
             const int* bt = p.block_tables + (long long)seq * p.max_blocks_per_seq + (long long)part * blocks_per_part;
-            const int prefetch_at = min(nblk, 4) - 1;
+            const int next_at = min(nblk, 2) - 1;      // read the next unit's number, load its entry
+            const int prefetch_at = min(nblk, 4) - 1;  // load its first 32 block ids
             for (int c = 0; c < nblk && ok; c += 32) {
                 const bool have = c + lane < nblk;
                 const int bid = c == 0 ? bids : (have ? __ldg(bt + c + lane) : 0);
@@ -419,6 +460,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CT
                             }
                         }
                     }
+                    if (c == 0 && jj == next_at) {
+                        un = __shfl_sync(0xffffffffu, un_req, 0);
+                        if (un < total_units) nxt = p.units[un / p.num_kv_heads];
+                    }
                     if (c == 0 && jj == prefetch_at && un < total_units) {
                         const int nb1 = (min(p.partition, nxt.z - nxt.y * p.partition) + kBlock - 1) / kBlock;
                         if (lane < nb1)
@@ -427,8 +472,25 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CT
                     }
                 }
             }
+            // Pad the unit to a multiple of block_splits stages with data-free ones, so every
+            // unit starts at a stage counter divisible by block_splits: block j of a unit is
+            // then always computed by warp j % block_splits, whichever CTA gets the unit, and
+            // the result does not depend on the order in which units are handed out.
+            const int nblk_pad = ((nblk + p.block_splits - 1) / p.block_splits) * p.block_splits;
+            for (int j = nblk; j < nblk_pad && ok; ++j, ++k) {
+                const int s = (int)(k % stages);
+                if (k >= (uint32_t)stages &&
+                    !__all_sync(0xffffffffu,
+                                mbar_wait(empty0 + 8 * s, ((k / stages) - 1) & 1, &g_pa_error, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive(full0 + 8 * s);
+                __syncwarp();
+            }
             cur = nxt;
             bids = nbids;
+            u = un;
         }
         // Never leave the CTA with copies in flight: wait for the last fill of every
         // stage and of both query buffers (immediate on the normal path).
@@ -459,11 +521,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CT
     const int rows_here = min(TR, p.rows - mt * TR);  // <= 0 for an all-padding tile
     uint32_t k = 0;
     int ul = 0;
-    for (long long u = blockIdx.x; u < total_units; u += gridDim.x, ++ul) {
+    for (;; ++ul) {
         const int qb = ul & 1;
         // (all waits below are made warp-uniform: a timeout seen by one lane stops the warp)
         bool ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8 * qb, (ul >> 1) & 1, &g_pa_error, abort_flag));
-        UnitInfo ui = info[qb];
+        const UnitInfo ui = info[qb];
+        const bool done = ok && ui.seq < 0;  // end marker: no unit follows
         uint32_t qf[NT][D / 16][2];      // Q^T as the B operand: Q[row][d 2t..2t+1], Q[row][d 2t+8..2t+9]
         float m[NT][2], l[NT][2];        // running max (log2 units) and sum for rows 2t, 2t+1 of each group
         float o[D / 16][NT][4];          // O^T: (d gid, row 2t), (d gid, row 2t+1), (d gid+8, 2t), (d gid+8, 2t+1)
@@ -476,8 +539,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CT
         for (int dt = 0; dt < D / 16; ++dt)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) o[dt][nt][0] = o[dt][nt][1] = o[dt][nt][2] = o[dt][nt][3] = 0.f;
-        int nblk = 0;
-        if (ok) {
+        int nblk = 0, nblk_pad = 0;
+        if (ok && !done) {
             const uint8_t* qrow = qbuf + qb * lay.q_half_bytes + mt * TR * qpitch;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -492,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CT
             if (lane == 0) mbar_arrive(qempty0 + 8 * qb);
 
             nblk = (ui.ntok + kBlock - 1) / kBlock;
+            nblk_pad = ((nblk + p.block_splits - 1) / p.block_splits) * p.block_splits;
             const int tok0 = ui.part * p.partition;
             // Last position (relative to the partition) each of this lane's rows may see:
             // row j of the q_len-row chunk is position L - q_len + j.
@@ -503,100 +567,103 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CT
                     const int r = mt * TR + nt * 8 + 2 * tig + c;
                     lim[nt][c] = ui.len - p.q_len + min(r / p.group, p.q_len - 1) - tok0;
                 }
-            const int first = (bsg - (int)(k % p.block_splits) + p.block_splits) % p.block_splits;
-            for (int j = first; j < nblk; j += p.block_splits) {
+            // Units start at a stage counter divisible by block_splits (the producer pads
+            // them), so this warp's blocks are j = bsg, bsg + block_splits, ...
+            for (int j = bsg; j < nblk_pad; j += p.block_splits) {
                 const uint32_t kj = k + j;
                 const int s = (int)(kj % stages);
                 if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (kj / stages) & 1, &g_pa_error, abort_flag))) {
                     ok = false;
                     break;
                 }
-                const uint32_t kst = smem_addr(stage_base + s * lay.stage_bytes);
-                const uint32_t vst = kst + kBoxes * kBoxBytes;
-                // smem row i holds token i - shift of this block (shift > 0 only for a short last block)
-                const int shift = kBlock - min(kBlock, ui.ntok - kBlock * j);
-                float sc[NT][4];
+                if (j < nblk) {  // data-free padding stages are only waited for and released
+                    const uint32_t kst = smem_addr(stage_base + s * lay.stage_bytes);
+                    const uint32_t vst = kst + kBoxes * kBoxBytes;
+                    // smem row i holds token i - shift of this block (shift > 0 only for a short last block)
+                    const int shift = kBlock - min(kBlock, ui.ntok - kBlock * j);
+                    float sc[NT][4];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                    for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    uint32_t a[4];
-                    const int tr = (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const int cc = kk * 16 + (lane >> 4) * 8;
-                    ldsm_x4(kst + swz(tr, cc), a[0], a[1], a[2], a[3]);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        uint32_t a[4];
+                        const int tr = (lane & 7) + ((lane >> 3) & 1) * 8;
+                        const int cc = kk * 16 + (lane >> 4) * 8;
+                        ldsm_x4(kst + swz(tr, cc), a[0], a[1], a[2], a[3]);
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) Elem<T>::mma(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
-                }
-                // Scale into log2 units; mask positions past each row's limit (and the zero rows
-                // in front of a short block).
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int i = gid + (c >> 1) * 8;
-                        const int tok = kBlock * j + i - shift;
-                        sc[nt][c] = (i >= shift && tok <= lim[nt][c & 1]) ? sc[nt][c] * p.scale_log2 : -INFINITY;
+                        for (int nt = 0; nt < NT; ++nt) Elem<T>::mma(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
                     }
-                float alpha[NT][2], pr[NT][4];
-                bool rescale = false;
+                    // Scale into log2 units; mask positions past each row's limit (and the zero rows
+                    // in front of a short block).
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        float mx = fmaxf(sc[nt][c], sc[nt][c + 2]);
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                        const float mn = fmaxf(m[nt][c], mx);
-                        const float base = mn == -INFINITY ? 0.f : mn;
-                        alpha[nt][c] = ex2(m[nt][c] - base);
-                        rescale |= alpha[nt][c] != 1.f;
-                        m[nt][c] = mn;
-                        pr[nt][c] = ex2(sc[nt][c] - base);
-                        pr[nt][c + 2] = ex2(sc[nt][c + 2] - base);
-                        l[nt][c] = l[nt][c] * alpha[nt][c] + (pr[nt][c] + pr[nt][c + 2]);
+                        for (int c = 0; c < 4; ++c) {
+                            const int i = gid + (c >> 1) * 8;
+                            const int tok = kBlock * j + i - shift;
+                            sc[nt][c] = (i >= shift && tok <= lim[nt][c & 1]) ? sc[nt][c] * p.scale_log2 : -INFINITY;
+                        }
+                    float alpha[NT][2], pr[NT][4];
+                    bool rescale = false;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            float mx = fmaxf(sc[nt][c], sc[nt][c + 2]);
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                            const float mn = fmaxf(m[nt][c], mx);
+                            const float base = mn == -INFINITY ? 0.f : mn;
+                            alpha[nt][c] = ex2(m[nt][c] - base);
+                            rescale |= alpha[nt][c] != 1.f;
+                            m[nt][c] = mn;
+                            pr[nt][c] = ex2(sc[nt][c] - base);
+                            pr[nt][c + 2] = ex2(sc[nt][c + 2] - base);
+                            l[nt][c] = l[nt][c] * alpha[nt][c] + (pr[nt][c] + pr[nt][c + 2]);
+                        }
+                    if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                        for (int dt = 0; dt < D / 16; ++dt)
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                o[dt][nt][0] *= alpha[nt][0];
+                                o[dt][nt][1] *= alpha[nt][1];
+                                o[dt][nt][2] *= alpha[nt][0];
+                                o[dt][nt][3] *= alpha[nt][1];
+                            }
                     }
-                if (__any_sync(0xffffffffu, rescale)) {
+                    // P^T as the B operand, in two 16-bit pieces (hi + residual) that together carry
+                    // about 16 significant bits.  The lane's (token, row-pair) values form the standard
+                    // fragment of P^T's 8x8 sub-tiles; movmatrix transposes them into (row, token-pair).
+                    uint32_t pb_hi[NT][2], pb_lo[NT][2];
 #pragma unroll
-                    for (int dt = 0; dt < D / 16; ++dt)
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const float x0 = pr[nt][2 * h], x1 = pr[nt][2 * h + 1];
+                            const float h0 = Elem<T>::round_trip(x0), h1 = Elem<T>::round_trip(x1);
+                            pb_hi[nt][h] = movmatrix_trans(Elem<T>::pack(h0, h1));
+                            pb_lo[nt][h] = movmatrix_trans(Elem<T>::pack(x0 - h0, x1 - h1));
+                        }
+#pragma unroll
+                    for (int dt = 0; dt < D / 16; ++dt) {
+                        uint32_t a[4];
+                        const int tr = (lane & 7) + (lane >> 4) * 8;
+                        const int cc = dt * 16 + ((lane >> 3) & 1) * 8;
+                        ldsm_x4_trans(vst + swz(tr, cc), a[0], a[1], a[2], a[3]);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            o[dt][nt][0] *= alpha[nt][0];
-                            o[dt][nt][1] *= alpha[nt][1];
-                            o[dt][nt][2] *= alpha[nt][0];
-                            o[dt][nt][3] *= alpha[nt][1];
+                            Elem<T>::mma(o[dt][nt], a, pb_hi[nt][0], pb_hi[nt][1]);
+                            Elem<T>::mma(o[dt][nt], a, pb_lo[nt][0], pb_lo[nt][1]);
                         }
-                }
-                // P^T as the B operand, in two 16-bit pieces (hi + residual) that together carry
-                // about 16 significant bits.  The lane's (token, row-pair) values form the standard
-                // fragment of P^T's 8x8 sub-tiles; movmatrix transposes them into (row, token-pair).
-                uint32_t pb_hi[NT][2], pb_lo[NT][2];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const float x0 = pr[nt][2 * h], x1 = pr[nt][2 * h + 1];
-                        const float h0 = Elem<T>::round_trip(x0), h1 = Elem<T>::round_trip(x1);
-                        pb_hi[nt][h] = movmatrix_trans(Elem<T>::pack(h0, h1));
-                        pb_lo[nt][h] = movmatrix_trans(Elem<T>::pack(x0 - h0, x1 - h1));
-                    }
-#pragma unroll
-                for (int dt = 0; dt < D / 16; ++dt) {
-                    uint32_t a[4];
-                    const int tr = (lane & 7) + (lane >> 4) * 8;
-                    const int cc = dt * 16 + ((lane >> 3) & 1) * 8;
-                    ldsm_x4_trans(vst + swz(tr, cc), a[0], a[1], a[2], a[3]);
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        Elem<T>::mma(o[dt][nt], a, pb_hi[nt][0], pb_hi[nt][1]);
-                        Elem<T>::mma(o[dt][nt], a, pb_lo[nt][0], pb_lo[nt][1]);
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty0 + 8 * s);
             }
         }
-        k += nblk;
+        k += nblk_pad;
         // Row sums over the eight lanes (same tig) that hold a row's tokens.
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -606,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CT
                 l[nt][c] += __shfl_xor_sync(0xffffffffu, l[nt][c], 8);
                 l[nt][c] += __shfl_xor_sync(0xffffffffu, l[nt][c], 16);
             }
-        if (ok) {
+        if (ok && !done) {
             float* co = comb_o + warp * p.slot_rows * D;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -628,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CT
         }
         // All consumer warps agree on whether to go on (and the buffer writes above are
         // ordered before the reads below).
-        if (consumers_any(!ok)) break;
+        if (consumers_any(!ok || done)) break;
         // Merge the block-split warps of each row tile; write the output or the partial.
         const int nparts = (ui.len + p.partition - 1) / p.partition;
         const int nthreads = kConsumerWarps * 32;
@@ -677,9 +744,13 @@ struct MergeParams {
     int max_context_len;
 };
 
-// One warp per output row (sequence, query row, head).
+// One warp per output row (sequence, query row, head) of a split sequence.  The
+// partitions' (max, sum) pairs are read lane-parallel and turned into weights
+// e^{m_p - M} / sum_p' e^{m_p' - M} l_p' once; the unnormalised partial outputs
+// are then summed in partition order, so the result does not depend on timing.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
+    griddep_wait();  // the partition pass must have finished
     constexpr int kPer = D / 32;
     const long long row = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -697,18 +768,25 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
     for (int i = lane; i < nparts; i += 32) M = fmaxf(M, p.pml[(slot0 + i) * per_seq + rem].x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float lsum = 0.f;
+    for (int i = lane; i < nparts; i += 32) {
+        const float2 ml = p.pml[(slot0 + i) * per_seq + rem];
+        lsum += ml.y * ex2(ml.x - M);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
     float acc[kPer];
 #pragma unroll
     for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
-    float lsum = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll 4
-        for (int i = 0; i < nparts; ++i) {
-            const long long prow = (slot0 + i) * per_seq + rem;
-            const float2 ml = p.pml[prow];
-            const float f = ex2(ml.x - M);
-            lsum += ml.y * f;
-            const float* src = p.pacc + prow * D + lane * kPer;
+    for (int base = 0; base < nparts; base += 32) {
+        const int mine = base + lane;
+        const float f_mine = mine < nparts ? ex2(p.pml[(slot0 + mine) * per_seq + rem].x - M) * inv : 0.f;
+        const int cnt = min(32, nparts - base);
+#pragma unroll 8
+        for (int j = 0; j < cnt; ++j) {
+            const float f = __shfl_sync(0xffffffffu, f_mine, j);
+            const float* src = p.pacc + ((slot0 + base + j) * per_seq + rem) * D + lane * kPer;
             if constexpr (kPer == 4) {
                 const float4 v = *reinterpret_cast<const float4*>(src);
                 acc[0] += v.x * f;
@@ -724,7 +802,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
     }
     uint16_t* dst = static_cast<uint16_t*>(p.out) + row * D + lane * kPer;
 #pragma unroll
-    for (int c = 0; c < kPer; ++c) dst[c] = Elem<T>::to_bits(acc[c] / lsum);
+    for (int c = 0; c < kPer; ++c) dst[c] = Elem<T>::to_bits(acc[c]);
 }
 
 // ---------------------------------------------------------------------------
@@ -800,6 +878,24 @@ struct Profile {
     bool created = false;
 } g_prof;
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// before its predecessor finishes; it orders itself with griddep_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // cuTensorMapEncodeTiled, fetched from the driver at first use (no link-time libcuda dependency).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -856,12 +952,12 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     pp.part_start = part_start;
     pp.units = units;
     pp.num_seqs = a.num_seqs;
+    pp.num_kv_heads = a.num_kv_heads;
     pp.q_len = a.q_len;
     pp.partition = a.partition;
     pp.max_blocks_per_seq = a.max_blocks_per_seq;
     pp.max_context_len = a.max_context_len;
-    plan_kernel<<<1, 1024, 0, stream>>>(pp);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, pp) != cudaSuccess) return PA_ERR_CUDA;
     *launches += 1;
 
     DecodeParams p;
@@ -871,6 +967,7 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     p.query = a.query;
     p.block_tables = a.block_tables;
     p.header = header;
+    p.work_counter = header + 1;
     p.units = units;
     p.pml = pml;
     p.pacc = pacc;
@@ -919,11 +1016,9 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
 
     const bool prof = g_prof.on && g_prof.n < 4096;
     if (prof) cudaEventRecord(g_prof.ev[2 * g_prof.n], stream);
-    if (nt == 1)
-        decode_kernel<T, D, 1><<<grid, kThreads, lay.total, stream>>>(p);
-    else
-        decode_kernel<T, D, 2><<<grid, kThreads, lay.total, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    const cudaError_t le = nt == 1 ? launch_pdl(decode_kernel<T, D, 1>, dim3(grid), dim3(kThreads), lay.total, stream, p)
+                                   : launch_pdl(decode_kernel<T, D, 2>, dim3(grid), dim3(kThreads), lay.total, stream, p);
+    if (le != cudaSuccess) return PA_ERR_CUDA;
     if (prof) {
         cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], stream);
         g_prof.n++;
@@ -943,9 +1038,8 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
         mp.partition = a.partition;
         mp.max_context_len = a.max_context_len;
         const long long rows = (long long)a.num_seqs * a.q_len * a.num_heads;
-        const long long blocks = (rows * 32 + 127) / 128;
-        merge_kernel<T, D><<<(unsigned)blocks, 128, 0, stream>>>(mp);
-        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+        const unsigned blocks = (unsigned)((rows * 32 + 127) / 128);
+        if (launch_pdl(merge_kernel<T, D>, dim3(blocks), dim3(128), 0, stream, mp) != cudaSuccess) return PA_ERR_CUDA;
         *launches += 1;
     }
     return PA_OK;

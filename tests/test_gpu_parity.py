@@ -188,7 +188,8 @@ def test_bad_slot_sets_flag_and_writes_nothing():
 
 
 def test_launch_counts():
-    """Append = 1 kernel; attention = plan + partition kernels, + merge when any sequence can split."""
+    """Append = 1 kernel; attention = plan + partition kernels, + the merge kernel when a sequence
+    can span more than one partition."""
     w = named(1)                                  # longest context 100 < one 512-token partition
     step = G.GpuStep(w)
     step.append()
