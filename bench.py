@@ -299,6 +299,7 @@ def run_ours(args, rank, world, local):
     bt = torch.from_numpy(w.block_tables).to(dev)
     cl = torch.from_numpy(w.context_lens).to(dev)
     ws = pa.alloc_workspace(w.num_seqs, w.q_len, w.num_heads, w.head_dim, w.max_context_len, device=dev)
+    pa.set_decode_math(args.math)
     stream = torch.cuda.current_stream(dev)
     pa.get_device_error(clear=True)
 
@@ -408,7 +409,7 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": DESCR[cfg], "seq_tokens_per_step": seq_tokens, "bytes_per_step": step_bytes,
-                   "attention_bytes": attn_bytes, "partition_tokens": 512,
+                   "attention_bytes": attn_bytes, "partition_tokens": 512, "math": args.math,
                    "l2": "flushed between steps" if flush is not None else
                    f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step vs 129 MB L2)",
                    "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
@@ -437,6 +438,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa_batch128")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--math", choices=["auto", "fma", "tensor"], default="auto",
+                    help="decode consumer arithmetic (auto: CUDA cores for one row per kv head, else tensor cores)")
     args = ap.parse_args()
     rank, world, local = dist_setup(args)
     try:

@@ -215,6 +215,20 @@ const char* pa_status_string(int status);
 int pa_get_device_error(int32_t* host_flags, int clear, void* stream);
 
 /*
+ * Arithmetic of the decode partition kernel, process-wide:
+ *   0 (default, auto): CUDA-core fp32 FMA dot products with warp-shuffle
+ *      reductions when each kv head has one query row (MHA, single token);
+ *      tensor-core tiles (mma.sync m16n8k16, fp32 accumulation) for grouped
+ *      heads and multi-query chunks, where they stream faster;
+ *   1: CUDA-core FMA wherever a kv head has at most 8 query rows;
+ *   2: tensor-core tiles everywhere.
+ * All give results within fp32 rounding of each other.  Returns
+ * PA_ERR_INVALID_ARG for other values.  Not thread safe: set it before
+ * launching work.
+ */
+int pa_set_decode_math(int math);
+
+/*
  * Timing hook for benchmarks.  pa_profile_enable(1) makes every following
  * decode call record a CUDA event pair around its main (partition) kernel on
  * the call's stream (up to 4096 pairs); pa_profile_read() waits for the

@@ -177,6 +177,8 @@ int pa_get_device_error(int32_t* host_flags, int clear, void* stream) {
     return pa::read_device_error(host_flags, clear, static_cast<cudaStream_t>(stream));
 }
 
+int pa_set_decode_math(int math) { return pa::set_decode_math(math); }
+
 int pa_profile_enable(int on) { return pa::profile_enable(on); }
 
 int pa_profile_read(float* total_ms, int* launches) {

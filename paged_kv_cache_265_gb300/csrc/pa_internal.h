@@ -82,6 +82,9 @@ int read_device_error(int32_t* flags, int clear, cudaStream_t stream);
 // (looked up on the first call per device, then cached).
 int noalloc_workspace(void** ptr);
 
+// Consumer arithmetic of the partition kernel: 0 auto, 1 CUDA-core FMA, 2 tensor cores.
+int set_decode_math(int math);
+
 // Benchmark timing hook around the main decode kernel.
 int profile_enable(int on);
 int profile_read(float* total_ms, int* launches);

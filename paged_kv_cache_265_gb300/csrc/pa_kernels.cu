@@ -244,11 +244,16 @@ struct UnitInfo {
 
 struct SmemLayout {
     int stage_bytes, qpitch, q_half_bytes;
-    int off_q, off_comb, off_m, off_l, off_bars, off_info, total;
+    int off_q, off_comb, off_m, off_l, off_bars, off_info, off_fma, total;
 };
 
 // Offsets from a 1024-byte aligned base (the swizzled TMA boxes need that alignment).
-__host__ __device__ inline SmemLayout smem_layout(int head_dim, int stages, int mtiles, int tile_rows, int slot_rows) {
+// Per consumer warp, the CUDA-core path exchanges P (8 rows x 16 tokens) and the
+// 8 rows' rescale factors through shared memory.
+constexpr int kFmaWarpFloats = 8 * 16 + 8;
+
+__host__ __device__ inline SmemLayout smem_layout(int head_dim, int stages, int mtiles, int tile_rows, int slot_rows,
+                                                  bool fma = false) {
     SmemLayout s;
     s.stage_bytes = 2 * (head_dim / kBoxCols) * kBoxBytes;  // K boxes then V boxes
     s.qpitch = head_dim * 2 + 16;                            // padded query rows
@@ -259,7 +264,8 @@ __host__ __device__ inline SmemLayout smem_layout(int head_dim, int stages, int 
     s.off_l = s.off_m + kConsumerWarps * 16 * 4;
     s.off_bars = s.off_l + kConsumerWarps * 16 * 4;
     s.off_info = s.off_bars + (2 * kMaxStages + 4) * 8;
-    s.total = s.off_info + 2 * (int)sizeof(UnitInfo) + 16 + 1024;  // + alignment slack
+    s.off_fma = s.off_info + 2 * (int)sizeof(UnitInfo) + 16;
+    s.total = s.off_fma + (fma ? kConsumerWarps * kFmaWarpFloats * 4 : 0) + 1024;  // + alignment slack
     return s;
 }
 
@@ -301,12 +307,64 @@ __device__ __forceinline__ bool consumers_any(bool v) {
     return r != 0;
 }
 
-template <typename T, int D, int NT>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CTAS_PER_SM_NT2)
+// Eight 16-bit values (one 16-byte chunk) widened to fp32.
+template <typename T>
+__device__ __forceinline__ void unpack8(const uint4 raw, float (&f)[8]) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (Elem<T>::kDtype == PA_BF16) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        } else {
+            const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            f[2 * i] = v.x;
+            f[2 * i + 1] = v.y;
+        }
+    }
+}
+
+// Sum of 8 per-row partials over the 2^LCH lanes of a lane group, transposed: three
+// halving exchange stages on lane bits LCH-1, LCH-2, LCH-3 leave each lane with the total
+// of row ((lane >> (LCH-3)) & 7); remaining lower bits are summed as a plain all-reduce.
+template <int LCH>
+__device__ __forceinline__ float transpose_reduce8(const float (&part)[8], int lane) {
+    constexpr int b0 = LCH - 1, b1 = LCH - 2, b2 = LCH - 3;
+    float a4[4], a2[2];
+    const bool h0 = (lane >> b0) & 1;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = h0 ? part[i] : part[i + 4];
+        const float keep = h0 ? part[i + 4] : part[i];
+        a4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1 << b0);
+    }
+    const bool h1 = (lane >> b1) & 1;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = h1 ? a4[i] : a4[i + 2];
+        const float keep = h1 ? a4[i + 2] : a4[i];
+        a2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1 << b1);
+    }
+    const bool h2 = (lane >> b2) & 1;
+    float v = (h2 ? a2[1] : a2[0]) + __shfl_xor_sync(0xffffffffu, h2 ? a2[0] : a2[1], 1 << b2);
+#pragma unroll
+    for (int b = b2 - 1; b >= 0; --b) v += __shfl_xor_sync(0xffffffffu, v, 1 << b);
+    return v;
+}
+
+// Resident CTAs per SM each kernel variant is built for (its register budget).
+__host__ __device__ constexpr int decode_ctas_per_sm(int nt, int rt) {
+    return rt == 0 ? (nt == 1 ? PA_CTAS_PER_SM_NT1 : PA_CTAS_PER_SM_NT2) : (rt <= 2 ? 4 : (rt == 4 ? 3 : 2));
+}
+
+// NT: query rows per consumer warp / 8 on the tensor-core path (RT == 0).
+// RT > 0 selects the CUDA-core path for up to RT (1, 2, 4 or 8) query rows per kv head.
+template <typename T, int D, int NT, int RT>
+__global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT))
     decode_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const SmemLayout lay = smem_layout(D, p.stages, p.mtiles, 8 * NT, p.slot_rows);
+    const SmemLayout lay = smem_layout(D, p.stages, p.mtiles, 8 * NT, p.slot_rows, RT > 0);
     const int qpitch = lay.qpitch;
     constexpr int kRowBytes = D * 2;
     constexpr int kBoxes = D / kBoxCols;  // boxes per K (or V) block
@@ -514,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CT
     //   O^T += V^T P^T   M = 16 head-dim cols, N = 8 query rows, K = 16 tokens
     // Each warp owns NT groups of 8 query rows (one row tile) and every
     // block_splits-th block of the unit.
-    constexpr int TR = 8 * NT;               // query rows per warp
+    constexpr int TR = 8 * NT;               // query rows per warp (8 on the CUDA-core path)
     const int mt = warp / p.block_splits;   // row tile of this warp
     const int bsg = warp % p.block_splits;  // which of the tile's block-split warps
     const int gid = lane >> 2, tig = lane & 3;
@@ -527,171 +585,314 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? PA_CTAS_PER_SM_NT1 : PA_CT
         bool ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8 * qb, (ul >> 1) & 1, &g_pa_error, abort_flag));
         const UnitInfo ui = info[qb];
         const bool done = ok && ui.seq < 0;  // end marker: no unit follows
-        uint32_t qf[NT][D / 16][2];      // Q^T as the B operand: Q[row][d 2t..2t+1], Q[row][d 2t+8..2t+9]
-        float m[NT][2], l[NT][2];        // running max (log2 units) and sum for rows 2t, 2t+1 of each group
-        float o[D / 16][NT][4];          // O^T: (d gid, row 2t), (d gid, row 2t+1), (d gid+8, 2t), (d gid+8, 2t+1)
+        if constexpr (RT == 0) {
+            uint32_t qf[NT][D / 16][2];      // Q^T as the B operand: Q[row][d 2t..2t+1], Q[row][d 2t+8..2t+9]
+            float m[NT][2], l[NT][2];        // running max (log2 units) and sum for rows 2t, 2t+1 of each group
+            float o[D / 16][NT][4];          // O^T: (d gid, row 2t), (d gid, row 2t+1), (d gid+8, 2t), (d gid+8, 2t+1)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            m[nt][0] = m[nt][1] = -INFINITY;
-            l[nt][0] = l[nt][1] = 0.f;
-        }
+            for (int nt = 0; nt < NT; ++nt) {
+                m[nt][0] = m[nt][1] = -INFINITY;
+                l[nt][0] = l[nt][1] = 0.f;
+            }
 #pragma unroll
-        for (int dt = 0; dt < D / 16; ++dt)
+            for (int dt = 0; dt < D / 16; ++dt)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) o[dt][nt][0] = o[dt][nt][1] = o[dt][nt][2] = o[dt][nt][3] = 0.f;
-        int nblk = 0, nblk_pad = 0;
-        if (ok && !done) {
-            const uint8_t* qrow = qbuf + qb * lay.q_half_bytes + mt * TR * qpitch;
+                for (int nt = 0; nt < NT; ++nt) o[dt][nt][0] = o[dt][nt][1] = o[dt][nt][2] = o[dt][nt][3] = 0.f;
+            int nblk = 0, nblk_pad = 0;
+            if (ok && !done) {
+                const uint8_t* qrow = qbuf + qb * lay.q_half_bytes + mt * TR * qpitch;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int k2 = 0; k2 < D / 32; ++k2) {
-                    const int rr = nt * 8 + (lane & 7);
-                    const int cc = k2 * 32 + (lane >> 3) * 8;
-                    ldsm_x4(smem_addr(qrow + rr * qpitch + cc * 2), qf[nt][2 * k2][0], qf[nt][2 * k2][1],
-                            qf[nt][2 * k2 + 1][0], qf[nt][2 * k2 + 1][1]);
-                }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(qempty0 + 8 * qb);
-
-            nblk = (ui.ntok + kBlock - 1) / kBlock;
-            nblk_pad = ((nblk + p.block_splits - 1) / p.block_splits) * p.block_splits;
-            const int tok0 = ui.part * p.partition;
-            // Last position (relative to the partition) each of this lane's rows may see:
-            // row j of the q_len-row chunk is position L - q_len + j.
-            int lim[NT][2];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int r = mt * TR + nt * 8 + 2 * tig + c;
-                    lim[nt][c] = ui.len - p.q_len + min(r / p.group, p.q_len - 1) - tok0;
-                }
-            // Units start at a stage counter divisible by block_splits (the producer pads
-            // them), so this warp's blocks are j = bsg, bsg + block_splits, ...
-            for (int j = bsg; j < nblk_pad; j += p.block_splits) {
-                const uint32_t kj = k + j;
-                const int s = (int)(kj % stages);
-                if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (kj / stages) & 1, &g_pa_error, abort_flag))) {
-                    ok = false;
-                    break;
-                }
-                if (j < nblk) {  // data-free padding stages are only waited for and released
-                    const uint32_t kst = smem_addr(stage_base + s * lay.stage_bytes);
-                    const uint32_t vst = kst + kBoxes * kBoxBytes;
-                    // smem row i holds token i - shift of this block (shift > 0 only for a short last block)
-                    const int shift = kBlock - min(kBlock, ui.ntok - kBlock * j);
-                    float sc[NT][4];
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        uint32_t a[4];
-                        const int tr = (lane & 7) + ((lane >> 3) & 1) * 8;
-                        const int cc = kk * 16 + (lane >> 4) * 8;
-                        ldsm_x4(kst + swz(tr, cc), a[0], a[1], a[2], a[3]);
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) Elem<T>::mma(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+                    for (int k2 = 0; k2 < D / 32; ++k2) {
+                        const int rr = nt * 8 + (lane & 7);
+                        const int cc = k2 * 32 + (lane >> 3) * 8;
+                        ldsm_x4(smem_addr(qrow + rr * qpitch + cc * 2), qf[nt][2 * k2][0], qf[nt][2 * k2][1],
+                                qf[nt][2 * k2 + 1][0], qf[nt][2 * k2 + 1][1]);
                     }
-                    // Scale into log2 units; mask positions past each row's limit (and the zero rows
-                    // in front of a short block).
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const int i = gid + (c >> 1) * 8;
-                            const int tok = kBlock * j + i - shift;
-                            sc[nt][c] = (i >= shift && tok <= lim[nt][c & 1]) ? sc[nt][c] * p.scale_log2 : -INFINITY;
-                        }
-                    float alpha[NT][2], pr[NT][4];
-                    bool rescale = false;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            float mx = fmaxf(sc[nt][c], sc[nt][c + 2]);
-                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                            const float mn = fmaxf(m[nt][c], mx);
-                            const float base = mn == -INFINITY ? 0.f : mn;
-                            alpha[nt][c] = ex2(m[nt][c] - base);
-                            rescale |= alpha[nt][c] != 1.f;
-                            m[nt][c] = mn;
-                            pr[nt][c] = ex2(sc[nt][c] - base);
-                            pr[nt][c + 2] = ex2(sc[nt][c + 2] - base);
-                            l[nt][c] = l[nt][c] * alpha[nt][c] + (pr[nt][c] + pr[nt][c + 2]);
-                        }
-                    if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-                        for (int dt = 0; dt < D / 16; ++dt)
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                o[dt][nt][0] *= alpha[nt][0];
-                                o[dt][nt][1] *= alpha[nt][1];
-                                o[dt][nt][2] *= alpha[nt][0];
-                                o[dt][nt][3] *= alpha[nt][1];
-                            }
-                    }
-                    // P^T as the B operand, in two 16-bit pieces (hi + residual) that together carry
-                    // about 16 significant bits.  The lane's (token, row-pair) values form the standard
-                    // fragment of P^T's 8x8 sub-tiles; movmatrix transposes them into (row, token-pair).
-                    uint32_t pb_hi[NT][2], pb_lo[NT][2];
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const float x0 = pr[nt][2 * h], x1 = pr[nt][2 * h + 1];
-                            const float h0 = Elem<T>::round_trip(x0), h1 = Elem<T>::round_trip(x1);
-                            pb_hi[nt][h] = movmatrix_trans(Elem<T>::pack(h0, h1));
-                            pb_lo[nt][h] = movmatrix_trans(Elem<T>::pack(x0 - h0, x1 - h1));
-                        }
-#pragma unroll
-                    for (int dt = 0; dt < D / 16; ++dt) {
-                        uint32_t a[4];
-                        const int tr = (lane & 7) + (lane >> 4) * 8;
-                        const int cc = dt * 16 + ((lane >> 3) & 1) * 8;
-                        ldsm_x4_trans(vst + swz(tr, cc), a[0], a[1], a[2], a[3]);
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            Elem<T>::mma(o[dt][nt], a, pb_hi[nt][0], pb_hi[nt][1]);
-                            Elem<T>::mma(o[dt][nt], a, pb_lo[nt][0], pb_lo[nt][1]);
-                        }
-                    }
-                }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty0 + 8 * s);
-            }
-        }
-        k += nblk_pad;
-        // Row sums over the eight lanes (same tig) that hold a row's tokens.
+                if (lane == 0) mbar_arrive(qempty0 + 8 * qb);
+
+                nblk = (ui.ntok + kBlock - 1) / kBlock;
+                nblk_pad = ((nblk + p.block_splits - 1) / p.block_splits) * p.block_splits;
+                const int tok0 = ui.part * p.partition;
+                // Last position (relative to the partition) each of this lane's rows may see:
+                // row j of the q_len-row chunk is position L - q_len + j.
+                int lim[NT][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                l[nt][c] += __shfl_xor_sync(0xffffffffu, l[nt][c], 4);
-                l[nt][c] += __shfl_xor_sync(0xffffffffu, l[nt][c], 8);
-                l[nt][c] += __shfl_xor_sync(0xffffffffu, l[nt][c], 16);
-            }
-        if (ok && !done) {
-            float* co = comb_o + warp * p.slot_rows * D;
+                    for (int c = 0; c < 2; ++c) {
+                        const int r = mt * TR + nt * 8 + 2 * tig + c;
+                        lim[nt][c] = ui.len - p.q_len + min(r / p.group, p.q_len - 1) - tok0;
+                    }
+                // Units start at a stage counter divisible by block_splits (the producer pads
+                // them), so this warp's blocks are j = bsg, bsg + block_splits, ...
+                for (int j = bsg; j < nblk_pad; j += p.block_splits) {
+                    const uint32_t kj = k + j;
+                    const int s = (int)(kj % stages);
+                    if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (kj / stages) & 1, &g_pa_error, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    if (j < nblk) {  // data-free padding stages are only waited for and released
+                        const uint32_t kst = smem_addr(stage_base + s * lay.stage_bytes);
+                        const uint32_t vst = kst + kBoxes * kBoxBytes;
+                        // smem row i holds token i - shift of this block (shift > 0 only for a short last block)
+                        const int shift = kBlock - min(kBlock, ui.ntok - kBlock * j);
+                        float sc[NT][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+                        for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int row = nt * 8 + 2 * tig + c;
-                    if (row < rows_here) {
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            uint32_t a[4];
+                            const int tr = (lane & 7) + ((lane >> 3) & 1) * 8;
+                            const int cc = kk * 16 + (lane >> 4) * 8;
+                            ldsm_x4(kst + swz(tr, cc), a[0], a[1], a[2], a[3]);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) Elem<T>::mma(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+                        }
+                        // Scale into log2 units; mask positions past each row's limit (and the zero rows
+                        // in front of a short block).
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const int i = gid + (c >> 1) * 8;
+                                const int tok = kBlock * j + i - shift;
+                                sc[nt][c] = (i >= shift && tok <= lim[nt][c & 1]) ? sc[nt][c] * p.scale_log2 : -INFINITY;
+                            }
+                        float alpha[NT][2], pr[NT][4];
+                        bool rescale = false;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int c = 0; c < 2; ++c) {
+                                float mx = fmaxf(sc[nt][c], sc[nt][c + 2]);
+                                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                                const float mn = fmaxf(m[nt][c], mx);
+                                const float base = mn == -INFINITY ? 0.f : mn;
+                                alpha[nt][c] = ex2(m[nt][c] - base);
+                                rescale |= alpha[nt][c] != 1.f;
+                                m[nt][c] = mn;
+                                pr[nt][c] = ex2(sc[nt][c] - base);
+                                pr[nt][c + 2] = ex2(sc[nt][c + 2] - base);
+                                l[nt][c] = l[nt][c] * alpha[nt][c] + (pr[nt][c] + pr[nt][c + 2]);
+                            }
+                        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                            for (int dt = 0; dt < D / 16; ++dt)
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    o[dt][nt][0] *= alpha[nt][0];
+                                    o[dt][nt][1] *= alpha[nt][1];
+                                    o[dt][nt][2] *= alpha[nt][0];
+                                    o[dt][nt][3] *= alpha[nt][1];
+                                }
+                        }
+                        // P^T as the B operand, in two 16-bit pieces (hi + residual) that together carry
+                        // about 16 significant bits.  The lane's (token, row-pair) values form the standard
+                        // fragment of P^T's 8x8 sub-tiles; movmatrix transposes them into (row, token-pair).
+                        uint32_t pb_hi[NT][2], pb_lo[NT][2];
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const float x0 = pr[nt][2 * h], x1 = pr[nt][2 * h + 1];
+                                const float h0 = Elem<T>::round_trip(x0), h1 = Elem<T>::round_trip(x1);
+                                pb_hi[nt][h] = movmatrix_trans(Elem<T>::pack(h0, h1));
+                                pb_lo[nt][h] = movmatrix_trans(Elem<T>::pack(x0 - h0, x1 - h1));
+                            }
 #pragma unroll
                         for (int dt = 0; dt < D / 16; ++dt) {
-                            co[row * D + dt * 16 + gid] = o[dt][nt][c];
-                            co[row * D + dt * 16 + gid + 8] = o[dt][nt][c + 2];
-                        }
-                        if (gid == 0) {
-                            comb_m[warp * 16 + row] = m[nt][c];
-                            comb_l[warp * 16 + row] = l[nt][c];
+                            uint32_t a[4];
+                            const int tr = (lane & 7) + (lane >> 4) * 8;
+                            const int cc = dt * 16 + ((lane >> 3) & 1) * 8;
+                            ldsm_x4_trans(vst + swz(tr, cc), a[0], a[1], a[2], a[3]);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                Elem<T>::mma(o[dt][nt], a, pb_hi[nt][0], pb_hi[nt][1]);
+                                Elem<T>::mma(o[dt][nt], a, pb_lo[nt][0], pb_lo[nt][1]);
+                            }
                         }
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty0 + 8 * s);
                 }
+            }
+            k += nblk_pad;
+            // Row sums over the eight lanes (same tig) that hold a row's tokens.
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    l[nt][c] += __shfl_xor_sync(0xffffffffu, l[nt][c], 4);
+                    l[nt][c] += __shfl_xor_sync(0xffffffffu, l[nt][c], 8);
+                    l[nt][c] += __shfl_xor_sync(0xffffffffu, l[nt][c], 16);
+                }
+            if (ok && !done) {
+                float* co = comb_o + warp * p.slot_rows * D;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int row = nt * 8 + 2 * tig + c;
+                        if (row < rows_here) {
+#pragma unroll
+                            for (int dt = 0; dt < D / 16; ++dt) {
+                                co[row * D + dt * 16 + gid] = o[dt][nt][c];
+                                co[row * D + dt * 16 + gid + 8] = o[dt][nt][c + 2];
+                            }
+                            if (gid == 0) {
+                                comb_m[warp * 16 + row] = m[nt][c];
+                                comb_l[warp * 16 + row] = l[nt][c];
+                            }
+                        }
+                    }
+            }
+        } else {
+            // ---------- CUDA-core path: fp32 FMA dot products and warp-shuffle reductions ----------
+            // Lane = (column chunk c of 8 head-dim elements, token parity tp).  For every token
+            // the lane forms partial dot products of its 8 columns with all RT query rows; a
+            // transposing butterfly over the CH lanes of the row leaves each lane holding the
+            // full score of one row rr.  P and the rescale factors are exchanged through shared
+            // memory for P.V, which every lane accumulates for all rows over its 8 columns.
+            constexpr int CH = D / 8, TPI = 32 / CH, ITERS = kBlock / TPI;
+            constexpr int LCH = D == 128 ? 4 : 3;
+            const int c = lane % CH, tp = lane / CH;
+            const int rr = (c >> (LCH - 3)) & 7;
+            const bool row_owner = LCH == 3 || (c & 1) == 0;
+            float* pbuf = reinterpret_cast<float*>(smem + lay.off_fma) + warp * kFmaWarpFloats;
+            float qv[RT][8], o[RT][8];
+            float m_r = -INFINITY, l_r = 0.f;
+#pragma unroll
+            for (int r = 0; r < RT; ++r)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[r][e] = 0.f;
+            int nblk = 0, nblk_pad = 0;
+            if (ok && !done) {
+                const uint8_t* qrow = qbuf + qb * lay.q_half_bytes;
+#pragma unroll
+                for (int r = 0; r < RT; ++r) unpack8<T>(*reinterpret_cast<const uint4*>(qrow + r * qpitch + c * 16), qv[r]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qempty0 + 8 * qb);
+                nblk = (ui.ntok + kBlock - 1) / kBlock;
+                nblk_pad = ((nblk + p.block_splits - 1) / p.block_splits) * p.block_splits;
+                const int lim_r = ui.len - p.q_len + min(rr / p.group, p.q_len - 1) - ui.part * p.partition;
+                for (int j = bsg; j < nblk_pad; j += p.block_splits) {
+                    const uint32_t kj = k + j;
+                    const int s = (int)(kj % stages);
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(full0 + 8 * s, (kj / stages) & 1, &g_pa_error, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    if (j < nblk) {
+                        const uint8_t* kst = stage_base + s * lay.stage_bytes;
+                        const uint8_t* vst = kst + (D / kBoxCols) * kBoxBytes;
+                        const int shift = kBlock - min(kBlock, ui.ntok - kBlock * j);
+                        float sv[ITERS];
+#pragma unroll
+                        for (int it = 0; it < ITERS; ++it) {
+                            const int i = it * TPI + tp;
+                            float kf[8], part[8];
+                            unpack8<T>(*reinterpret_cast<const uint4*>(kst + swz(i, c * 8)), kf);
+#pragma unroll
+                            for (int r = 0; r < 8; ++r) {
+                                float acc = 0.f;
+                                if (r < RT) {
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) acc = fmaf(qv[r < RT ? r : 0][e], kf[e], acc);
+                                }
+                                part[r] = acc;
+                            }
+                            sv[it] = transpose_reduce8<LCH>(part, lane);
+                        }
+                        float mx = -INFINITY;
+#pragma unroll
+                        for (int it = 0; it < ITERS; ++it) {
+                            const int i = it * TPI + tp;
+                            const int tok = kBlock * j + i - shift;
+                            sv[it] = (i >= shift && tok <= lim_r) ? sv[it] * p.scale_log2 : -INFINITY;
+                            mx = fmaxf(mx, sv[it]);
+                        }
+#pragma unroll
+                        for (int o2 = CH; o2 < 32; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+                        const float mn = fmaxf(m_r, mx);
+                        const float base = mn == -INFINITY ? 0.f : mn;
+                        const float alpha = ex2(m_r - base);
+                        m_r = mn;
+                        float psum = 0.f;
+#pragma unroll
+                        for (int it = 0; it < ITERS; ++it) {
+                            sv[it] = ex2(sv[it] - base);
+                            psum += sv[it];
+                        }
+                        l_r = l_r * alpha + psum;
+                        if (row_owner) {
+#pragma unroll
+                            for (int it = 0; it < ITERS; ++it) pbuf[rr * 16 + tp * ITERS + it] = sv[it];
+                            if (tp == 0) pbuf[128 + rr] = alpha;
+                        }
+                        __syncwarp();
+                        bool rescale = false;
+                        float al[RT];
+#pragma unroll
+                        for (int r = 0; r < RT; ++r) {
+                            al[r] = pbuf[128 + r];
+                            rescale |= al[r] != 1.f;
+                        }
+                        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                            for (int r = 0; r < RT; ++r)
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) o[r][e] *= al[r];
+                        }
+#pragma unroll
+                        for (int it = 0; it < ITERS; ++it) {
+                            const int i = it * TPI + tp;
+                            float vf[8];
+                            unpack8<T>(*reinterpret_cast<const uint4*>(vst + swz(i, c * 8)), vf);
+#pragma unroll
+                            for (int r = 0; r < RT; ++r) {
+                                const float pr = pbuf[r * 16 + tp * ITERS + it];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) o[r][e] = fmaf(pr, vf[e], o[r][e]);
+                            }
+                        }
+                        __syncwarp();  // pbuf is rewritten by the next block
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+                }
+            }
+            k += nblk_pad;
+            // Sum over the token-parity lanes.
+#pragma unroll
+            for (int o2 = CH; o2 < 32; o2 <<= 1) {
+                l_r += __shfl_xor_sync(0xffffffffu, l_r, o2);
+#pragma unroll
+                for (int r = 0; r < RT; ++r)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[r][e] += __shfl_xor_sync(0xffffffffu, o[r][e], o2);
+            }
+            if (ok && !done) {
+                float* co = comb_o + warp * p.slot_rows * D;
+                if (tp == 0) {
+#pragma unroll
+                    for (int r = 0; r < RT; ++r)
+                        if (r < rows_here) {
+                            *reinterpret_cast<float4*>(co + r * D + c * 8) = make_float4(o[r][0], o[r][1], o[r][2], o[r][3]);
+                            *reinterpret_cast<float4*>(co + r * D + c * 8 + 4) = make_float4(o[r][4], o[r][5], o[r][6], o[r][7]);
+                        }
+                    if (row_owner && rr < rows_here) {
+                        comb_m[warp * 16 + rr] = m_r;
+                        comb_l[warp * 16 + rr] = l_r;
+                    }
+                }
+            }
         }
         // All consumer warps agree on whether to go on (and the buffer writes above are
         // ordered before the reads below).
@@ -870,6 +1071,8 @@ int decode_blocks_per_sm(const void* fn, int smem, int& blocks) {
     return PA_OK;
 }
 
+int g_decode_math = 0;  // 0: auto, 1: CUDA-core FMA (up to 8 rows per kv head), 2: tensor-core tiles
+
 struct Profile {
     bool on = false;
     int dev = -1;
@@ -984,6 +1187,13 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     // tiles per kv head are rounded up to a divisor of the consumer warp count (a third
     // tile becomes a fourth, all-padding one) so that every consumer warp owns exactly one
     // (row tile, block split) pair.
+    // Consumer arithmetic.  Measured on GB300 (partition kernel, CUDA events): with one query
+    // row per kv head both paths stream at the same rate (MHA workload 6.33 vs 6.35 TB/s), so
+    // that case stays on CUDA-core FMA; with grouped heads the tensor-core tiles win
+    // (4 rows: 5.99 vs 3.79 TB/s, 8 rows: 5.88 vs 1.91 TB/s).
+    int rt = 0;
+    if (g_decode_math == 1 && p.rows <= 8) rt = p.rows <= 1 ? 1 : p.rows <= 2 ? 2 : p.rows <= 4 ? 4 : 8;
+    if (g_decode_math == 0 && p.rows == 1) rt = 1;
     const int nt = p.rows <= 8 ? 1 : 2;
     const int tile_rows = 8 * nt;
     p.mtiles = (p.rows + tile_rows - 1) / tile_rows;
@@ -992,20 +1202,26 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     p.block_splits = kConsumerWarps / p.mtiles;
     p.slot_rows = std::min(tile_rows, p.rows);
 
-    const void* fn = nt == 1 ? reinterpret_cast<const void*>(decode_kernel<T, D, 1>)
-                             : reinterpret_cast<const void*>(decode_kernel<T, D, 2>);
-    const int ctas_target = nt == 1 ? PA_CTAS_PER_SM_NT1 : PA_CTAS_PER_SM_NT2;
+    using KernelFn = void (*)(DecodeParams);
+    const KernelFn kfn = rt == 1   ? decode_kernel<T, D, 1, 1>
+                         : rt == 2 ? decode_kernel<T, D, 1, 2>
+                         : rt == 4 ? decode_kernel<T, D, 1, 4>
+                         : rt == 8 ? decode_kernel<T, D, 1, 8>
+                         : nt == 1 ? decode_kernel<T, D, 1, 0>
+                                   : decode_kernel<T, D, 2, 0>;
+    const void* fn = reinterpret_cast<const void*>(kfn);
+    const int ctas_target = decode_ctas_per_sm(nt, rt);
     // Deepest ring that still lets ctas_target CTAs share an SM.  Its length must be a
     // multiple of block_splits: then every stage is always consumed by the same warps,
     // which wait its phases strictly in order (a waiter two phases ahead of a barrier
     // would see its parity as already complete).
     int stages = (kMaxStages / p.block_splits) * p.block_splits;
     if (stages < p.block_splits) return PA_ERR_UNSUPPORTED;
-    SmemLayout lay = smem_layout(D, stages, p.mtiles, tile_rows, p.slot_rows);
+    SmemLayout lay = smem_layout(D, stages, p.mtiles, tile_rows, p.slot_rows, rt > 0);
     const int per_sm_budget = 228 * 1024 / ctas_target - 1024;
     while (stages > p.block_splits && lay.total > per_sm_budget) {
         stages -= p.block_splits;
-        lay = smem_layout(D, stages, p.mtiles, tile_rows, p.slot_rows);
+        lay = smem_layout(D, stages, p.mtiles, tile_rows, p.slot_rows, rt > 0);
     }
     if (lay.total > dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
     p.stages = stages;
@@ -1016,8 +1232,7 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
 
     const bool prof = g_prof.on && g_prof.n < 4096;
     if (prof) cudaEventRecord(g_prof.ev[2 * g_prof.n], stream);
-    const cudaError_t le = nt == 1 ? launch_pdl(decode_kernel<T, D, 1>, dim3(grid), dim3(kThreads), lay.total, stream, p)
-                                   : launch_pdl(decode_kernel<T, D, 2>, dim3(grid), dim3(kThreads), lay.total, stream, p);
+    const cudaError_t le = launch_pdl(kfn, dim3(grid), dim3(kThreads), lay.total, stream, p);
     if (le != cudaSuccess) return PA_ERR_CUDA;
     if (prof) {
         cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], stream);
@@ -1088,6 +1303,12 @@ int read_device_error(int32_t* flags, int clear, cudaStream_t stream) {
         if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ERR_CUDA;
     }
     *flags = v;
+    return PA_OK;
+}
+
+int set_decode_math(int math) {
+    if (math < 0 || math > 2) return PA_ERR_INVALID_ARG;
+    g_decode_math = math;
     return PA_OK;
 }
 

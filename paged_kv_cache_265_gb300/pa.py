@@ -42,6 +42,7 @@ _SIGS = {
                                              _c_int, _c_int, _c_i64, _c_int, _c_f, _c_int, _c_int, _vp]),
     "pa_status_string": (ctypes.c_char_p, [_c_int]),
     "pa_get_device_error": (_c_int, [ctypes.POINTER(ctypes.c_int32), _c_int, _vp]),
+    "pa_set_decode_math": (_c_int, [_c_int]),
     "pa_profile_enable": (_c_int, [_c_int]),
     "pa_profile_read": (_c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
     "pa_last_launch_count": (_c_int, []),
@@ -200,6 +201,13 @@ def get_device_error(clear: bool = True, stream=None) -> int:
     v = ctypes.c_int32(0)
     _check("pa_get_device_error", lib().pa_get_device_error(ctypes.byref(v), int(clear), _stream(stream)))
     return int(v.value)
+
+
+def set_decode_math(math: str) -> None:
+    """'auto' (default): CUDA-core FMA for one query row per kv head, tensor-core tiles otherwise;
+    'fma': CUDA-core FMA up to 8 query rows per kv head; 'tensor': tensor-core tiles everywhere.
+    Process-wide."""
+    _check("pa_set_decode_math", lib().pa_set_decode_math({"auto": 0, "fma": 1, "tensor": 2}[math]))
 
 
 def profile_enable(on: bool = True) -> None:

@@ -135,17 +135,23 @@ def test_shared_prefix_equals_private_copies():
     assert np.array_equal(a, b)
 
 
-def test_gqa_equals_replicated_mha():
-    """GQA (4 query heads per kv head) equals MHA over kv heads repeated 4 times, bit for bit."""
+@pytest.mark.parametrize("math", ["tensor", "fma"])
+def test_gqa_equals_replicated_mha(math):
+    """GQA (4 query heads per kv head) equals MHA over kv heads repeated 4 times, bit for bit,
+    with either consumer arithmetic (each row's sums do not depend on the other rows)."""
     w = W.make_workload("gqa", [40, 333, 1000], num_heads=8, num_kv_heads=2, head_dim=128, num_blocks=120,
                         seed=21)
-    a = G.GpuStep(w).run()
     mha = W.Workload(**{**w.__dict__, "num_kv_heads": 8,
                         "key_cache": np.ascontiguousarray(np.repeat(w.key_cache, 4, axis=2)),
                         "value_cache": np.ascontiguousarray(np.repeat(w.value_cache, 4, axis=2)),
                         "new_key": np.ascontiguousarray(np.repeat(w.new_key, 4, axis=1)),
                         "new_value": np.ascontiguousarray(np.repeat(w.new_value, 4, axis=1))})
-    b = G.GpuStep(mha).run()
+    pa.set_decode_math(math)
+    try:
+        a = G.GpuStep(w).run()
+        b = G.GpuStep(mha).run()
+    finally:
+        pa.set_decode_math("auto")
     assert np.array_equal(a, b)
 
 
@@ -199,3 +205,46 @@ def test_launch_counts():
     step16 = G.GpuStep(w, partition_size=16)
     step16.attend()
     assert pa.last_launch_count() == 3
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 5])
+def test_cuda_core_path_matches_oracle(cfg):
+    """The CUDA-core FMA consumers, forced on grouped heads too, reach the same results as the
+    tensor-core tiles: within tolerance of the oracle and within one ulp of its rounding."""
+    w = named(cfg)
+    pa.set_decode_math("fma")
+    try:
+        got = G.GpuStep(w).run()
+    finally:
+        pa.set_decode_math("auto")
+    _, _, ref = G.oracle_step(w)
+    G.compare(got, ref, w.dtype, f"{w.name} (CUDA-core path)")
+    assert G.ulps_from_rounded_oracle(got, ref, w.dtype) <= 1
+
+
+@pytest.mark.parametrize("case", [1, 3])
+def test_cuda_core_path_edge_shapes(case):
+    lens, hq, hkv, d, q_len, dt = EDGE[case]
+    w = W.make_workload(f"edge{case}", lens, num_heads=hq, num_kv_heads=hkv, head_dim=d, dtype=dt, q_len=q_len,
+                        num_blocks=sum((l + 15) // 16 for l in lens) + 7, seed=300 + case)
+    pa.set_decode_math("fma")
+    try:
+        got = G.GpuStep(w, partition_size=32).run()
+    finally:
+        pa.set_decode_math("auto")
+    _, _, ref = G.oracle_step(w)
+    G.compare(got, ref, w.dtype, f"edge{case} (CUDA-core path)")
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_tensor_path_on_single_row_heads(cfg):
+    """MHA workloads run on CUDA cores by default; the tensor-core tiles stay correct there too."""
+    w = named(cfg)
+    pa.set_decode_math("tensor")
+    try:
+        got = G.GpuStep(w).run()
+    finally:
+        pa.set_decode_math("auto")
+    _, _, ref = G.oracle_step(w)
+    G.compare(got, ref, w.dtype, f"{w.name} (tensor-core path)")
+    assert G.ulps_from_rounded_oracle(got, ref, w.dtype) <= 1
