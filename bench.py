@@ -430,6 +430,49 @@ def run_ours(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def run_copy_blocks(args, rank, world, local):
+    """Copy-on-write block copy on the GQA pool shape: 8192 random (src, dst) pairs per step,
+    each moving a 32 KB K block and a 32 KB V block (read + write)."""
+    import torch
+
+    from paged_kv_cache_265_gb300 import build as B
+    from paged_kv_cache_265_gb300 import pa
+
+    B.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    nb, hkv, d, pairs = 40000, 8, 128, 8192
+    kc = torch.randn((nb, 16, hkv, d), device=dev).to(torch.bfloat16)
+    vc = torch.randn((nb, 16, hkv, d), device=dev).to(torch.bfloat16)
+    g = np.random.Generator(np.random.PCG64(2656))
+    perm = g.permutation(nb)
+    mapping = torch.from_numpy(np.stack([perm[:pairs], perm[pairs:2 * pairs]], 1).astype(np.int64)).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        pa.copy_blocks(kc, vc, mapping, stream=stream)
+    torch.cuda.synchronize(dev)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        s0.record(stream)
+        for _ in range(args.steps):
+            pa.copy_blocks(kc, vc, mapping, stream=stream)
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = s0.elapsed_time(s1) / args.steps
+    nbytes = pairs * 2 * (16 * hkv * d * 2) * 2   # K and V blocks, read and written
+    peak, kind = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({"metric": "copy-on-write block copy: achieved HBM GB/s", "value": gbs, "unit": "GB/s",
+                      "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                      "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                      "config": {"workload": f"{pairs} pairs of 16x{hkv}x{d} bf16 K and V blocks in a {nb}-block pool",
+                                 "bytes_per_step": nbytes},
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                                   "peak_source": f"{kind} copy bandwidth"},
+                      "clocks": clocks.summary(), "device_error_flags": pa.get_device_error(clear=True)}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -438,6 +481,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa_batch128")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["decode_step", "copy_blocks"], default="decode_step",
+                    help="decode_step: the timed hot path; copy_blocks: the copy-on-write block copy alone")
     ap.add_argument("--math", choices=["auto", "fma", "tensor"], default="auto",
                     help="decode consumer arithmetic (auto: CUDA cores for one row per kv head, else tensor cores)")
     args = ap.parse_args()
@@ -445,6 +490,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.op == "copy_blocks":
+            run_copy_blocks(args, rank, world, local)
         else:
             run_ours(args, rank, world, local)
     finally:

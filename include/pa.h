@@ -100,6 +100,23 @@ int pa_reshape_and_cache(const void* key, const void* value, void* key_cache, vo
                          int head_dim, int block_size, int64_t num_blocks, int dtype, void* stream);
 
 /*
+ * Copy-on-write block copy ([P1] section on paged KV: blocks shared by several
+ * sequences carry a reference count; a sequence about to write into a shared
+ * block first gets its own copy, and only that one block is copied).  For every
+ * pair i of block_mapping [num_pairs, 2] int64 = (src, dst):
+ *   key_cache[dst] = key_cache[src], value_cache[dst] = value_cache[src]
+ * whole [block_size, num_kv_heads, head_dim] blocks, byte for byte.
+ * Contract: the dst blocks are distinct and none is also a src of the same call
+ * (the caller's block manager copies into freshly allocated blocks); otherwise
+ * the result depends on copy order.  Pairs with an id outside [0, num_blocks)
+ * set PA_DEVERR_BLOCK_ID and copy nothing.  num_pairs == 0 is a no-op.
+ * The table update (and the following pa_reshape_and_cache) are the caller's.
+ */
+int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_mapping, int64_t num_pairs,
+                   int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, int dtype,
+                   void* stream);
+
+/*
  * Bytes of device workspace pa_decode_attention* needs for these sizes and the
  * default partition (PA_DEFAULT_PARTITION tokens).  The workspace holds the
  * per-call work list and the split-K partials (fp32 m, l and unnormalised o

@@ -76,6 +76,9 @@ class Oracle:
             _u16p, _u16p, _u16p, _u16p, _i64p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, ctypes.c_int64,
         ]
+        lib.oracle_copy_blocks.restype = ctypes.c_int
+        lib.oracle_copy_blocks.argtypes = [_u16p, _u16p, _i64p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int64]
         lib.oracle_bits_to_double_vec.restype = None
         lib.oracle_bits_to_double_vec.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int, _f64p]
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -125,6 +128,15 @@ class Oracle:
         return int(self._lib.oracle_reshape_and_cache(
             _ptr(k, _u16p), _ptr(v, _u16p), _ptr(key_cache, _u16p), _ptr(value_cache, _u16p),
             _ptr(sm, _i64p), t, hkv, d, bs, nb))
+
+
+    def copy_blocks(self, key_cache, value_cache, block_mapping) -> int:
+        """Copy-on-write block copies IN PLACE; returns the count of pairs with an id outside the pool."""
+        bm = np.ascontiguousarray(block_mapping, dtype=np.int64).reshape(-1, 2)
+        assert key_cache.flags["C_CONTIGUOUS"] and value_cache.flags["C_CONTIGUOUS"]
+        nb, bs, hkv, d = key_cache.shape
+        return int(self._lib.oracle_copy_blocks(_ptr(key_cache, _u16p), _ptr(value_cache, _u16p),
+                                                _ptr(bm, _i64p), bm.shape[0], hkv, d, bs, nb))
 
 
 def load(plant: int = 0) -> Oracle:

@@ -247,6 +247,30 @@ int oracle_reshape_and_cache(const uint16_t* key, const uint16_t* value,
     return bad;
 }
 
+/*
+ * Copy-on-write block copy ("每生成一个字都要把全部权重读一遍：从 vLLM 看 LLM 推理提速",
+ * paged-KV section, the reference-count paragraph: a sequence about to write into a
+ * block it shares first gets its own copy of that block).  For every pair
+ * (src, dst) of block_mapping [num_pairs, 2], the whole K block and V block
+ * [block_size, num_kv_heads, head_dim] are copied byte for byte from src to dst.
+ * Pairs with an id outside [0, num_blocks) are skipped and counted in the return
+ * value.  Pairs are applied in order.
+ */
+int oracle_copy_blocks(uint16_t* key_cache, uint16_t* value_cache, const int64_t* block_mapping,
+                       int64_t num_pairs, int num_kv_heads, int head_dim, int block_size,
+                       int64_t num_blocks)
+{
+    const int64_t blk = (int64_t)block_size * num_kv_heads * head_dim;
+    int bad = 0;
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        int64_t src = block_mapping[2 * i], dst = block_mapping[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) { ++bad; continue; }
+        memmove(key_cache + dst * blk, key_cache + src * blk, sizeof(uint16_t) * blk);
+        memmove(value_cache + dst * blk, value_cache + src * blk, sizeof(uint16_t) * blk);
+    }
+    return bad;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

@@ -80,6 +80,24 @@ int pa_reshape_and_cache(const void* key, const void* value, void* key_cache, vo
     return st;
 }
 
+int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_mapping, int64_t num_pairs,
+                   int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, int dtype, void* stream) {
+    t_last_launches = 0;
+    if (num_pairs < 0 || num_kv_heads < 1 || num_blocks < 1) return PA_ERR_INVALID_ARG;
+    if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_INVALID_ARG;
+    if (block_size != PA_BLOCK_SIZE || !supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PA_OK;
+    if (!key_cache || !value_cache || !block_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key_cache) || !aligned16(value_cache) || (reinterpret_cast<uintptr_t>(block_mapping) & 7u) != 0)
+        return PA_ERR_INVALID_ARG;
+    int launches = 0;
+    const int st = pa::launch_copy_blocks(key_cache, value_cache, block_mapping, num_pairs,
+                                          block_size * num_kv_heads * head_dim * 2, num_blocks,
+                                          static_cast<cudaStream_t>(stream), &launches);
+    t_last_launches = launches;
+    return st;
+}
+
 size_t pa_decode_workspace_size_ex(int num_seqs, int q_len, int num_heads, int head_dim, int max_context_len,
                                    int partition_size) {
     if (num_seqs < 0 || q_len < 1 || num_heads < 1 || head_dim < 1 || max_context_len < 1) return 0;

@@ -76,6 +76,8 @@ int launch_reshape_and_cache(const void* key, const void* value, void* key_cache
                              const int64_t* slot_mapping, int64_t num_tokens, int row_bytes,
                              int64_t num_slots, cudaStream_t stream, int* launches);
 int launch_decode(const DecodeArgs& a, cudaStream_t stream, int* launches);
+int launch_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_mapping, int64_t num_pairs,
+                       int block_bytes, int64_t num_blocks, cudaStream_t stream, int* launches);
 int read_device_error(int32_t* flags, int clear, cudaStream_t stream);
 
 // Device address of the library's fixed scratch array on the current device

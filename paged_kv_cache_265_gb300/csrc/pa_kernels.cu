@@ -89,6 +89,33 @@ __global__ void __launch_bounds__(256) reshape_kernel(const uint4* __restrict__ 
 }
 
 // ---------------------------------------------------------------------------
+// Copy-on-write block copy: whole K and V blocks from src to dst, per pair.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ key_cache,
+                                                          uint4* __restrict__ value_cache,
+                                                          const long long* __restrict__ mapping,
+                                                          long long num_pairs, int block_vecs,
+                                                          long long num_blocks) {
+    griddep_launch_dependents();
+    const long long per_pair = 2LL * block_vecs;
+    const long long total = num_pairs * per_pair;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long pr = idx / per_pair;
+        const int rem = (int)(idx - pr * per_pair);
+        const int which = rem >= block_vecs;  // 0 = K, 1 = V
+        const int v = rem - which * block_vecs;
+        const long long src = __ldg(mapping + 2 * pr), dst = __ldg(mapping + 2 * pr + 1);
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            if (rem == 0) atomicOr(&g_pa_error, PA_DEVERR_BLOCK_ID);
+            continue;
+        }
+        uint4* base = which ? value_cache : key_cache;
+        base[dst * block_vecs + v] = base[src * block_vecs + v];
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Work list
 // ---------------------------------------------------------------------------
 struct PlanParams {
@@ -1275,6 +1302,22 @@ int launch_reshape_and_cache(const void* key, const void* value, void* key_cache
                                              static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache),
                                              reinterpret_cast<const long long*>(slot_mapping), num_tokens,
                                              row_vecs, num_slots);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    *launches += 1;
+    return PA_OK;
+}
+
+int launch_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_mapping, int64_t num_pairs,
+                       int block_bytes, int64_t num_blocks, cudaStream_t stream, int* launches) {
+    DeviceInfo dev;
+    if (int st = device_info(dev)) return st;
+    const int block_vecs = block_bytes / 16;
+    const long long total = (long long)num_pairs * 2 * block_vecs;
+    const long long want = (total + 255) / 256;
+    const int grid = (int)std::max(1LL, std::min<long long>(want, (long long)dev.sms * 16));
+    copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache),
+                                                 reinterpret_cast<const long long*>(block_mapping), num_pairs,
+                                                 block_vecs, num_blocks);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     *launches += 1;
     return PA_OK;

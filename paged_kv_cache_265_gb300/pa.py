@@ -29,6 +29,7 @@ _c_int, _c_i64, _c_sz, _c_f, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 
 _SIGS = {
     "pa_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_int, _vp]),
+    "pa_copy_blocks": (_c_int, [_vp, _vp, _vp, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_int, _vp]),
     "pa_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "pa_decode_workspace_size_ex": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "pa_decode_attention": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
@@ -117,6 +118,21 @@ def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.T
         _dev(slot_mapping, "slot_mapping"), slot_mapping.shape[0], hkv, d, bs, nb, dtype_code(key_cache),
         _stream(stream))
     _check("pa_reshape_and_cache", st)
+
+
+def copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, block_mapping: torch.Tensor,
+                stream=None) -> None:
+    """Copy-on-write: for each (src, dst) row of block_mapping (int64 [M, 2]) copy the whole K and V
+    block src to dst.  dst blocks must be distinct and not sources of the same call."""
+    nb, bs, hkv, d = key_cache.shape
+    if value_cache.shape != key_cache.shape or value_cache.dtype != key_cache.dtype:
+        raise ValueError("key_cache and value_cache must match")
+    if block_mapping.dtype != torch.int64 or block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
+        raise ValueError("block_mapping must be int64 [num_pairs, 2]")
+    st = lib().pa_copy_blocks(_dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+                              _dev(block_mapping, "block_mapping"), block_mapping.shape[0], hkv, d, bs, nb,
+                              dtype_code(key_cache), _stream(stream))
+    _check("pa_copy_blocks", st)
 
 
 def workspace_size(num_seqs: int, q_len: int, num_heads: int, head_dim: int, max_context_len: int,

@@ -294,11 +294,65 @@ def pin_append_completes_the_pool(orc):
     assert np.array_equal(vc, whole.value_cache)
 
 
+def pin_copy_blocks_matches_numpy_assignment(orc):
+    """Copy-on-write block copies equal numpy whole-block assignment over the pool; pairs with an
+    id outside the pool are skipped and counted."""
+    w = W.make_workload("cow", [40, 70, 33], num_heads=4, num_kv_heads=2, head_dim=8, append_len=0,
+                        num_blocks=24, seed=16)
+    mapping = np.array([[w.block_tables[0, 0], 20], [w.block_tables[1, 3], 21], [w.block_tables[2, 2], 22],
+                        [5, 99]], dtype=np.int64)
+    kc, vc = w.key_cache.copy(), w.value_cache.copy()
+    assert orc.copy_blocks(kc, vc, mapping) == 1
+    ek, ev = w.key_cache.copy(), w.value_cache.copy()
+    good = mapping[:3]
+    ek[good[:, 1]] = w.key_cache[good[:, 0]]
+    ev[good[:, 1]] = w.value_cache[good[:, 0]]
+    assert np.array_equal(kc, ek) and np.array_equal(vc, ev)
+
+
+def pin_copy_on_write_fork(orc):
+    """Two sequences share a 40-token prefix whose last block is partly filled.  Each copies that
+    block before appending its own token 40 (copy-on-write); each then attends exactly over
+    the prefix plus its own token (SDPA on contiguous arrays), and the shared block is untouched."""
+    g = np.random.Generator(np.random.PCG64(17))
+    hkv, d, hq, nb = 2, 8, 4, 12
+    bits = lambda *shape: _bf16_bits(g.standard_normal(shape).astype(np.float32))
+    kc = np.full((nb, 16, hkv, d), W.NAN_BITS["bf16"], np.uint16)
+    vc = kc.copy()
+    pk, pv = bits(40, hkv, d), bits(40, hkv, d)
+    shared = [7, 2, 9]
+    for p_ in range(40):
+        kc[shared[p_ // 16], p_ % 16], vc[shared[p_ // 16], p_ % 16] = pk[p_], pv[p_]
+    before = kc[9].copy()
+    nk, nv = bits(2, hkv, d), bits(2, hkv, d)
+    copies = [4, 11]
+    assert orc.copy_blocks(kc, vc, np.array([[9, copies[0]], [9, copies[1]]])) == 0
+    bt = np.array([[7, 2, copies[0]], [7, 2, copies[1]]], np.int32)
+    slots = np.array([copies[0] * 16 + 8, copies[1] * 16 + 8], np.int64)
+    assert orc.reshape_and_cache(nk, nv, kc, vc, slots) == 0
+    assert np.array_equal(kc[9], before)
+    q = bits(2, 1, hq, d)
+    lens = np.array([41, 41], np.int32)
+    out, bad = orc.decode_attention(q, kc, vc, bt, lens, 1 / math.sqrt(d), "bf16")
+    assert bad == 0
+    lk = [np.concatenate([pk, nk[i:i + 1]]) for i in range(2)]
+    lv = [np.concatenate([pv, nv[i:i + 1]]) for i in range(2)]
+    ref_w = W.Workload(name="fork", dtype="bf16", num_heads=hq, num_kv_heads=hkv, head_dim=d, q_len=1,
+                       block_size=16, num_blocks=nb, scale=1 / math.sqrt(d), context_lens=lens, block_tables=bt,
+                       query=q, key_cache=kc, value_cache=vc, new_key=nk, new_value=nv, slot_mapping=slots,
+                       logical_key=lk, logical_value=lv)
+    assert np.max(np.abs(out - _sdpa_reference(ref_w))) <= 1e-12
+
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
 ALL_PINS = [
     pin_bf16_widening, pin_fp16_widening, pin_sdpa_tiny_named, pin_sdpa_random_small,
     pin_single_token_is_its_value, pin_identical_values, pin_zero_query_is_mean, pin_dominant_key,
     pin_two_keys_closed_form,
     pin_block_permutation, pin_sharing_equals_duplication, pin_gqa_equals_replicated_mha,
     pin_chunk_rows_are_shorter_decodes, pin_append_matches_numpy_assignment,
-    pin_append_completes_the_pool,
+    pin_append_completes_the_pool, pin_copy_blocks_matches_numpy_assignment, pin_copy_on_write_fork,
 ]
