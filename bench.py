@@ -473,6 +473,53 @@ def run_copy_blocks(args, rank, world, local):
           flush=True)
 
 
+def run_spec_verify(args, rank, world, local):
+    """Speculative-decoding verification on 64 sequences x (4 drafts + 1), vocabulary 32000:
+    the accept/reject scan and the final draw, in one launch."""
+    import torch
+
+    from paged_kv_cache_265_gb300 import build as B
+    from paged_kv_cache_265_gb300 import pa
+
+    B.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    x = W.spec_verify_inputs(num_seqs=64, k=4, vocab=32000)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    tp, dp, dt, ua, us = d(x.target_probs), d(x.draft_probs), d(x.draft_tokens), d(x.u_accept), d(x.u_sample)
+    acc = torch.empty(64, dtype=torch.int32, device=dev)
+    out = torch.empty((64, 5), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+    for _ in range(max(3, args.warmup)):
+        pa.spec_verify(tp, dp, dt, ua, us, acc, out, stream=stream)
+    torch.cuda.synchronize(dev)
+    # algorithmic bytes: the rows each sequence's draw reads (two at a rejection, one for the bonus)
+    na = acc.cpu().numpy()
+    rows = sum(2 if a < 4 else 1 for a in na)
+    nbytes = rows * 32000 * 4 + 64 * 4 * (8 + 4 + 4) + 64 * 4 * 6
+    tot = 0.0
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for _ in range(args.steps):
+        flush.zero_()
+        ev[0].record(stream)
+        pa.spec_verify(tp, dp, dt, ua, us, acc, out, stream=stream)
+        ev[1].record(stream)
+        torch.cuda.synchronize(dev)
+        tot += ev[0].elapsed_time(ev[1])
+    ms = tot / args.steps
+    peak, kind = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({"metric": "speculative verification: achieved HBM GB/s", "value": gbs, "unit": "GB/s",
+                      "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                      "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+                      "config": {"workload": "64 sequences, 4 drafts + 1, vocabulary 32000, L2 flushed per launch",
+                                 "bytes_per_step": nbytes, "accepted_histogram": np.bincount(na, minlength=5).tolist()},
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                                   "peak_source": f"{kind} copy bandwidth"},
+                      "device_error_flags": pa.get_device_error(clear=True)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -481,8 +528,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa_batch128")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["decode_step", "copy_blocks"], default="decode_step",
-                    help="decode_step: the timed hot path; copy_blocks: the copy-on-write block copy alone")
+    ap.add_argument("--op", choices=["decode_step", "copy_blocks", "spec_verify"], default="decode_step",
+                    help="decode_step: the timed hot path; copy_blocks / spec_verify: those steps alone")
     ap.add_argument("--math", choices=["auto", "fma", "tensor"], default="auto",
                     help="decode consumer arithmetic (auto: CUDA cores for one row per kv head, else tensor cores)")
     args = ap.parse_args()
@@ -492,6 +539,8 @@ def main():
             run_reference(args, rank, world)
         elif args.op == "copy_blocks":
             run_copy_blocks(args, rank, world, local)
+        elif args.op == "spec_verify":
+            run_spec_verify(args, rank, world, local)
         else:
             run_ours(args, rank, world, local)
     finally:

@@ -78,6 +78,7 @@ typedef enum {
 #define PA_DEVERR_SLOT     0x4  /* slot_mapping[t] >= num_blocks * block_size */
 #define PA_DEVERR_TIMEOUT  0x8  /* a bounded wait inside a kernel gave up (internal error) */
 #define PA_DEVERR_INTERNAL 0x10 /* a kernel refused an inconsistent launch configuration (library bug) */
+#define PA_DEVERR_TOKEN    0x20 /* a draft token outside [0, vocab) (treated as rejected) */
 
 #define PA_BLOCK_SIZE 16
 #define PA_DEFAULT_PARTITION 512  /* tokens per split-K partition */
@@ -115,6 +116,31 @@ int pa_reshape_and_cache(const void* key, const void* value, void* key_cache, vo
 int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_mapping, int64_t num_pairs,
                    int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, int dtype,
                    void* stream);
+
+/*
+ * Speculative-decoding verification ([P2] section 2.4 Speculative Decoding, steps
+ * 3-4; [P1] section "对症下药" on checking gamma + 1 positions in one forward).
+ * Per sequence n, with k = num_draft draft tokens:
+ *   scan i = 0 .. k-1: t = draft_tokens[n][i];
+ *     accept if p_large[i][t] >= p_draft[i][t], else accept if
+ *     u_accept[n][i] < p_large[i][t] / p_draft[i][t] (IEEE fp32 division);
+ *     at the first rejection stop and draw a token from (p_large[i] - p_draft[i])+
+ *     (from p_large[i] if that residual is all zero);
+ *   if all k drafts are accepted, draw the bonus token from p_large[k].
+ * A draw with uniform u over weights w takes the smallest v whose prefix sum of
+ * w exceeds u times the total, computed on w converted exactly to 2^-40 fixed
+ * point and u to 2^-24 (integer-exact, order independent).
+ *   num_accepted [N] int32, written: accepted drafts, 0..k
+ *   out_tokens   [N, k+1] int32, written: accepted drafts, the drawn token, then -1
+ *   target_probs [N, k+1, V] fp32; draft_probs [N, k, V] fp32; draft_tokens [N, k]
+ *   int32; u_accept [N, k] fp32 in [0,1); u_sample [N] fp32 in [0,1) (the caller
+ *   draws the random numbers).
+ * 0 <= num_draft <= 64; V <= 262,144.  A draft token outside [0, V) sets PA_DEVERR_TOKEN and
+ * counts as a rejection.
+ */
+int pa_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* target_probs,
+                   const float* draft_probs, const int32_t* draft_tokens, const float* u_accept,
+                   const float* u_sample, int num_seqs, int num_draft, int vocab, void* stream);
 
 /*
  * Bytes of device workspace pa_decode_attention* needs for these sizes and the

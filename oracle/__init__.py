@@ -79,6 +79,10 @@ class Oracle:
         lib.oracle_copy_blocks.restype = ctypes.c_int
         lib.oracle_copy_blocks.argtypes = [_u16p, _u16p, _i64p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int64]
+        _f32p = ctypes.POINTER(ctypes.c_float)
+        lib.oracle_spec_verify.restype = ctypes.c_int
+        lib.oracle_spec_verify.argtypes = [_i32p, _i32p, _f32p, _f32p, _i32p, _f32p, _f32p, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int]
         lib.oracle_bits_to_double_vec.restype = None
         lib.oracle_bits_to_double_vec.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int, _f64p]
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -137,6 +141,26 @@ class Oracle:
         nb, bs, hkv, d = key_cache.shape
         return int(self._lib.oracle_copy_blocks(_ptr(key_cache, _u16p), _ptr(value_cache, _u16p),
                                                 _ptr(bm, _i64p), bm.shape[0], hkv, d, bs, nb))
+
+
+    def spec_verify(self, target_probs, draft_probs, draft_tokens, u_accept, u_sample):
+        """Speculative-decoding verification.  target [N, k+1, V] f32, draft [N, k, V] f32,
+        draft_tokens [N, k] i32, u_accept [N, k] f32, u_sample [N] f32.
+        Returns (num_accepted [N] i32, out_tokens [N, k+1] i32)."""
+        f32p = ctypes.POINTER(ctypes.c_float)
+        tp = np.ascontiguousarray(target_probs, dtype=np.float32)
+        dp = np.ascontiguousarray(draft_probs, dtype=np.float32)
+        dt = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+        ua = np.ascontiguousarray(u_accept, dtype=np.float32)
+        us = np.ascontiguousarray(u_sample, dtype=np.float32)
+        n, k1, v = tp.shape
+        k = k1 - 1
+        assert dp.shape == (n, k, v) and dt.shape == (n, k) and ua.shape == (n, k) and us.shape == (n,)
+        acc = np.empty(n, np.int32)
+        out = np.empty((n, k1), np.int32)
+        self._lib.oracle_spec_verify(_ptr(acc, _i32p), _ptr(out, _i32p), _ptr(tp, f32p), _ptr(dp, f32p),
+                                     _ptr(dt, _i32p), _ptr(ua, f32p), _ptr(us, f32p), n, k, v)
+        return acc, out
 
 
 def load(plant: int = 0) -> Oracle:

@@ -271,6 +271,95 @@ int oracle_copy_blocks(uint16_t* key_cache, uint16_t* value_cache, const int64_t
     return bad;
 }
 
+/*
+ * Speculative-decoding verification ("现代 LLM 推理引擎剖析", section 2.4 Speculative
+ * Decoding, steps 3 and 4; the gamma + 1 positions of "每生成一个字都要把全部权重读一遍",
+ * section "对症下药").  For each sequence, with k draft tokens:
+ *   scan i = 0 .. k-1 left to right, t = draft_tokens[i]:
+ *     accept if p_large[i][t] >= p_draft[i][t];
+ *     else accept if u_accept[i] < p_large[i][t] / p_draft[i][t]  (probability p_large/p_draft);
+ *     at the first rejection stop and draw one token from (p_large[i] - p_draft[i])+;
+ *   if all k are accepted, draw a bonus token from p_large[k].
+ * A draw from weights w[0..V) with uniform u takes the smallest v whose prefix sum
+ * of w exceeds u times the total.  Reading (the pages give no sampling procedure):
+ * the weights are fp32; each is converted exactly to a fixed-point integer
+ * floor(w * 2^40), u to floor(u * 2^24), the threshold is floor(u24 * total / 2^24),
+ * so prefix sums are integer-exact and independent of summation order.  A residual
+ * whose integer total is 0 falls back to p_large[i].
+ * Outputs: num_accepted[n] in [0, k]; out_tokens[n][0..k]: the accepted drafts,
+ * then the drawn token, then -1.
+ */
+static uint64_t fixed40(float w) { return (uint64_t)floor((double)w * 1099511627776.0); }  /* 2^40 */
+
+static int draw_fixed(const float* a, const float* b, int vocab, float u)
+{
+    /* weights a - b clamped at 0 (b == NULL: a itself) */
+    uint64_t total = 0;
+    for (int v = 0; v < vocab; ++v) {
+#if PLANT == 9
+        float w = b ? b[v] - a[v] : a[v];   /* planted: residual taken the wrong way round */
+#else
+        float w = b ? a[v] - b[v] : a[v];
+#endif
+        if (!(w > 0.0f)) w = 0.0f;
+        total += fixed40(w);
+    }
+    if (total == 0) return -1;
+    uint64_t u24 = (uint64_t)floor((double)u * 16777216.0);          /* 2^24 */
+    unsigned __int128 prod = (unsigned __int128)u24 * total;
+    uint64_t thresh = (uint64_t)(prod >> 24);
+    uint64_t run = 0;
+    for (int v = 0; v < vocab; ++v) {
+        float w = b ? a[v] - b[v] : a[v];
+        if (!(w > 0.0f)) w = 0.0f;
+#if PLANT == 9
+        w = b ? b[v] - a[v] : a[v];
+        if (!(w > 0.0f)) w = 0.0f;
+#endif
+        run += fixed40(w);
+        if (run > thresh) return v;
+    }
+    return vocab - 1;
+}
+
+int oracle_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* target_probs,
+                       const float* draft_probs, const int32_t* draft_tokens, const float* u_accept,
+                       const float* u_sample, int num_seqs, int k, int vocab)
+{
+    for (int n = 0; n < num_seqs; ++n) {
+        const float* pl = target_probs + (int64_t)n * (k + 1) * vocab;
+        const float* pd = draft_probs + (int64_t)n * k * vocab;
+        int32_t* out = out_tokens + (int64_t)n * (k + 1);
+        int i = 0;
+        for (; i < k; ++i) {
+            int t = draft_tokens[(int64_t)n * k + i];
+            float a = pl[(int64_t)i * vocab + t], b = pd[(int64_t)i * vocab + t];
+            int accept = a >= b;
+            if (!accept) {
+#if PLANT == 8
+                volatile float ratio = b / a;   /* planted: ratio inverted */
+#else
+                volatile float ratio = a / b;   /* IEEE single-precision division */
+#endif
+                accept = u_accept[(int64_t)n * k + i] < ratio;
+            }
+            if (!accept) break;
+            out[i] = t;
+        }
+        int tok;
+        if (i < k) {
+            tok = draw_fixed(pl + (int64_t)i * vocab, pd + (int64_t)i * vocab, vocab, u_sample[n]);
+            if (tok < 0) tok = draw_fixed(pl + (int64_t)i * vocab, NULL, vocab, u_sample[n]);
+        } else {
+            tok = draw_fixed(pl + (int64_t)k * vocab, NULL, vocab, u_sample[n]);
+        }
+        out[i] = tok;
+        for (int j = i + 1; j <= k; ++j) out[j] = -1;
+        num_accepted[n] = i;
+    }
+    return 0;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

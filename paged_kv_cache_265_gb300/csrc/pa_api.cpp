@@ -98,6 +98,26 @@ int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_mapp
     return st;
 }
 
+int pa_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* target_probs, const float* draft_probs,
+                   const int32_t* draft_tokens, const float* u_accept, const float* u_sample, int num_seqs,
+                   int num_draft, int vocab, void* stream) {
+    t_last_launches = 0;
+    if (num_seqs < 0 || num_draft < 0 || num_draft > 64 || vocab < 1) return PA_ERR_INVALID_ARG;
+    if (vocab > 262144) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!num_accepted || !out_tokens || !target_probs || !u_sample) return PA_ERR_INVALID_ARG;
+    if (num_draft > 0 && (!draft_probs || !draft_tokens || !u_accept)) return PA_ERR_INVALID_ARG;
+    const void* ptrs[] = {num_accepted, out_tokens, target_probs, draft_probs, draft_tokens, u_accept, u_sample};
+    for (const void* q : ptrs)
+        if ((reinterpret_cast<uintptr_t>(q) & 3u) != 0) return PA_ERR_INVALID_ARG;
+    int launches = 0;
+    const int st = pa::launch_spec_verify(num_accepted, out_tokens, target_probs, draft_probs, draft_tokens, u_accept,
+                                          u_sample, num_seqs, num_draft, vocab, static_cast<cudaStream_t>(stream),
+                                          &launches);
+    t_last_launches = launches;
+    return st;
+}
+
 size_t pa_decode_workspace_size_ex(int num_seqs, int q_len, int num_heads, int head_dim, int max_context_len,
                                    int partition_size) {
     if (num_seqs < 0 || q_len < 1 || num_heads < 1 || head_dim < 1 || max_context_len < 1) return 0;

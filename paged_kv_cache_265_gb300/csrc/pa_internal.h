@@ -76,6 +76,9 @@ int launch_reshape_and_cache(const void* key, const void* value, void* key_cache
                              const int64_t* slot_mapping, int64_t num_tokens, int row_bytes,
                              int64_t num_slots, cudaStream_t stream, int* launches);
 int launch_decode(const DecodeArgs& a, cudaStream_t stream, int* launches);
+int launch_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* target_probs,
+                       const float* draft_probs, const int32_t* draft_tokens, const float* u_accept,
+                       const float* u_sample, int num_seqs, int k, int vocab, cudaStream_t stream, int* launches);
 int launch_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_mapping, int64_t num_pairs,
                        int block_bytes, int64_t num_blocks, cudaStream_t stream, int* launches);
 int read_device_error(int32_t* flags, int clear, cudaStream_t stream);

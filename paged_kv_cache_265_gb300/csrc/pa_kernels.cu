@@ -116,6 +116,186 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ ke
 }
 
 // ---------------------------------------------------------------------------
+// Speculative-decoding verification ("现代 LLM 推理引擎剖析", section 2.4): accept
+// drafts left to right (p_large >= p_draft, else with probability
+// p_large / p_draft), then draw the correction from (p_large - p_draft)+ at the
+// first rejection, or a bonus token from p_large[k] if all were accepted.
+// Draws are inverse-CDF over weights converted exactly to 2^-40 fixed point, so
+// prefix sums are integer-exact whatever the summation order.
+// ---------------------------------------------------------------------------
+struct SpecParams {
+    int* num_accepted;
+    int* out_tokens;
+    const float* target;
+    const float* draft;
+    const int* draft_tokens;
+    const float* u_accept;
+    const float* u_sample;
+    int k;
+    int vocab;
+};
+
+// floor(x * 2^shift) for a non-negative fp32 x < 2, from its bits (integer-only:
+// fp64 is slow on this GPU).  Exact: the mathematical value, as the oracle's fp64 floor.
+__device__ __forceinline__ unsigned long long fixed_from_float(float x, int shift) {
+    const unsigned bits = __float_as_uint(x);
+    const int ebits = (bits >> 23) & 0xff;
+    if (ebits == 0) return 0ull;  // zero or subnormal: below 2^-126, floor gives 0 for shift <= 64
+    const unsigned long long m = (bits & 0x7fffffu) | 0x800000u;
+    const int e = ebits - 127 - 23 + shift;  // value = m * 2^e
+    if (e >= 0) return m << e;
+    if (e <= -64) return 0ull;
+    return m >> (-e);
+}
+
+__device__ __forceinline__ float draw_weight(const float* a, const float* b, int v) {
+    const float w = b ? a[v] - b[v] : a[v];
+    return w > 0.f ? w : 0.f;
+}
+
+constexpr int kSpecThreads = 1024;
+constexpr int kSpecChunk = 4 * kSpecThreads;  // vocabulary entries per pass
+constexpr int kSpecMaxChunks = 64;            // vocabulary up to 262,144
+
+struct DrawSmem {
+    unsigned long long red[kSpecThreads / 32][kSpecMaxChunks];
+    unsigned long long chunk_prefix[kSpecMaxChunks + 1];
+    unsigned long long scan[kSpecThreads / 32];
+    int tok;
+    int chunk;
+};
+
+// Inverse-CDF draw with uniform u over weights (a - b)+ (or a): the smallest v whose prefix
+// sum of floor(w * 2^40) exceeds floor(floor(u * 2^24) * total / 2^24).  Pass 1 sums each
+// 4096-entry chunk (thread t takes entries c * 1024 + t of it, coalesced); the chunk holding
+// the threshold is then scanned in order, 1024 entries at a time.  Returns -1 when all weights
+// are 0.  Every thread of the block must call it.
+__device__ int block_draw(const float* a, const float* b, int vocab, float u, DrawSmem& sm) {
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int chunks = (vocab + kSpecChunk - 1) / kSpecChunk;
+#pragma unroll 4
+    for (int j = 0; j < chunks; ++j) {
+        float w[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // all loads of the chunk first
+            const int v = j * kSpecChunk + c * kSpecThreads + t;
+            w[c] = v < vocab ? draw_weight(a, b, v) : 0.f;
+        }
+        unsigned long long s = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s += fixed_from_float(w[c], 40);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) sm.red[warp][j] = s;
+    }
+    __syncthreads();
+    if (t < chunks) {
+        unsigned long long s = 0;
+        for (int w = 0; w < kSpecThreads / 32; ++w) s += sm.red[w][t];
+        sm.chunk_prefix[t + 1] = s;
+    }
+    __syncthreads();
+    if (t == 0) {
+        sm.chunk_prefix[0] = 0;
+        for (int j = 1; j <= chunks; ++j) sm.chunk_prefix[j] += sm.chunk_prefix[j - 1];
+        sm.tok = -1;
+        sm.chunk = -1;
+        const unsigned long long total = sm.chunk_prefix[chunks];
+        if (total) {
+            const unsigned long long u24 = fixed_from_float(u, 24);
+            const unsigned long long thresh = (__umul64hi(u24, total) << 40) | ((u24 * total) >> 24);
+            sm.chunk_prefix[kSpecMaxChunks] = thresh;
+            for (int j = 0; j < chunks; ++j)
+                if (sm.chunk_prefix[j + 1] > thresh) {
+                    sm.chunk = j;
+                    break;
+                }
+        }
+    }
+    __syncthreads();
+    const int j = sm.chunk;
+    if (j >= 0) {
+        const unsigned long long thresh = sm.chunk_prefix[kSpecMaxChunks];
+        unsigned long long base = sm.chunk_prefix[j];
+        for (int c = 0; c < 4; ++c) {
+            const int v = j * kSpecChunk + c * kSpecThreads + t;
+            const unsigned long long x0 = v < vocab ? fixed_from_float(draw_weight(a, b, v), 40) : 0ull;
+            unsigned long long x = x0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (lane == 31) sm.scan[warp] = x;
+            __syncthreads();
+            unsigned long long before = base, sub = 0;
+            for (int w = 0; w < kSpecThreads / 32; ++w) {
+                if (w < warp) before += sm.scan[w];
+                sub += sm.scan[w];
+            }
+            if (v < vocab && before + x > thresh && before + x - x0 <= thresh) sm.tok = v;
+            __syncthreads();
+            if (sm.tok >= 0) break;
+            base += sub;
+        }
+    }
+    __syncthreads();
+    const int tok = sm.tok;
+    __syncthreads();
+    if (j < 0) return -1;
+    return tok < 0 ? vocab - 1 : tok;
+}
+
+// One CTA per sequence.
+__global__ void __launch_bounds__(kSpecThreads) spec_verify_kernel(const SpecParams p) {
+    griddep_launch_dependents();
+    __shared__ DrawSmem sm;
+    __shared__ int s_pos;
+    __shared__ int s_ok[64];
+    __shared__ int s_tokv[64];
+    const int n = blockIdx.x;
+    const long long V = p.vocab;
+    const float* pl = p.target + (long long)n * (p.k + 1) * V;
+    const float* pd = p.draft + (long long)n * p.k * V;
+    int* out = p.out_tokens + (long long)n * (p.k + 1);
+    // Every draft position's accept decision in parallel (thread i), then the left-to-right
+    // scan for the first rejection on the flags.
+    if (threadIdx.x < p.k) {
+        const int i = threadIdx.x;
+        const int t = p.draft_tokens[(long long)n * p.k + i];
+        bool accept = false;
+        if (t < 0 || t >= p.vocab) {  // not a token: counts as a rejection
+            atomicOr(&g_pa_error, PA_DEVERR_TOKEN);
+        } else {
+            const float a = pl[i * V + t], b = pd[i * V + t];
+            accept = a >= b;
+            if (!accept) accept = p.u_accept[(long long)n * p.k + i] < __fdiv_rn(a, b);
+        }
+        s_ok[i] = accept;
+        s_tokv[i] = t;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int i = 0;
+        while (i < p.k && s_ok[i]) {
+            out[i] = s_tokv[i];
+            ++i;
+        }
+        s_pos = i;
+    }
+    __syncthreads();
+    const int i = s_pos;
+    const float u = p.u_sample[n];
+    int tok = block_draw(pl + i * V, i < p.k ? pd + i * V : nullptr, p.vocab, u, sm);
+    if (tok < 0 && i < p.k) tok = block_draw(pl + i * V, nullptr, p.vocab, u, sm);
+    if (threadIdx.x == 0) {
+        out[i] = tok;
+        for (int jj = i + 1; jj <= p.k; ++jj) out[jj] = -1;
+        p.num_accepted[n] = i;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Work list
 // ---------------------------------------------------------------------------
 struct PlanParams {
@@ -1318,6 +1498,25 @@ int launch_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_
     copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache),
                                                  reinterpret_cast<const long long*>(block_mapping), num_pairs,
                                                  block_vecs, num_blocks);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    *launches += 1;
+    return PA_OK;
+}
+
+int launch_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* target_probs,
+                       const float* draft_probs, const int32_t* draft_tokens, const float* u_accept,
+                       const float* u_sample, int num_seqs, int k, int vocab, cudaStream_t stream, int* launches) {
+    SpecParams p;
+    p.num_accepted = num_accepted;
+    p.out_tokens = out_tokens;
+    p.target = target_probs;
+    p.draft = draft_probs;
+    p.draft_tokens = draft_tokens;
+    p.u_accept = u_accept;
+    p.u_sample = u_sample;
+    p.k = k;
+    p.vocab = vocab;
+    spec_verify_kernel<<<num_seqs, kSpecThreads, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     *launches += 1;
     return PA_OK;

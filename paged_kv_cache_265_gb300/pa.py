@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libpa.so")
 
 PA_BF16, PA_FP16 = 0, 1
 PA_DEVERR_BLOCK_ID, PA_DEVERR_CONTEXT, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT, PA_DEVERR_INTERNAL = 1, 2, 4, 8, 16
+PA_DEVERR_TOKEN = 32
 BLOCK_SIZE = 16
 DEFAULT_PARTITION = 512
 NOALLOC_WORKSPACE_BYTES = 32 << 20
@@ -29,6 +30,7 @@ _c_int, _c_i64, _c_sz, _c_f, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 
 _SIGS = {
     "pa_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_int, _vp]),
+    "pa_spec_verify": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp]),
     "pa_copy_blocks": (_c_int, [_vp, _vp, _vp, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_int, _vp]),
     "pa_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "pa_decode_workspace_size_ex": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
@@ -133,6 +135,32 @@ def copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, block_mappin
                               _dev(block_mapping, "block_mapping"), block_mapping.shape[0], hkv, d, bs, nb,
                               dtype_code(key_cache), _stream(stream))
     _check("pa_copy_blocks", st)
+
+
+def spec_verify(target_probs: torch.Tensor, draft_probs: torch.Tensor, draft_tokens: torch.Tensor,
+                u_accept: torch.Tensor, u_sample: torch.Tensor, num_accepted: torch.Tensor = None,
+                out_tokens: torch.Tensor = None, stream=None):
+    """Speculative-decoding verification.  target [N, k+1, V] f32, draft [N, k, V] f32,
+    draft_tokens [N, k] i32, u_accept [N, k] f32, u_sample [N] f32.
+    Returns (num_accepted [N] i32, out_tokens [N, k+1] i32)."""
+    n, k1, v = target_probs.shape
+    k = k1 - 1
+    if target_probs.dtype != torch.float32 or draft_probs.dtype != torch.float32:
+        raise ValueError("probabilities must be float32")
+    if draft_probs.shape != (n, k, v) or draft_tokens.shape != (n, k) or draft_tokens.dtype != torch.int32:
+        raise ValueError("draft shapes/dtypes")
+    if u_accept.shape != (n, k) or u_sample.shape != (n,):
+        raise ValueError("uniform shapes")
+    if num_accepted is None:
+        num_accepted = torch.empty(n, dtype=torch.int32, device=target_probs.device)
+    if out_tokens is None:
+        out_tokens = torch.empty((n, k1), dtype=torch.int32, device=target_probs.device)
+    st = lib().pa_spec_verify(_dev(num_accepted, "num_accepted"), _dev(out_tokens, "out_tokens"),
+                              _dev(target_probs, "target_probs"), _dev(draft_probs, "draft_probs"),
+                              _dev(draft_tokens, "draft_tokens"), _dev(u_accept, "u_accept"),
+                              _dev(u_sample, "u_sample"), n, k, v, _stream(stream))
+    _check("pa_spec_verify", st)
+    return num_accepted, out_tokens
 
 
 def workspace_size(num_seqs: int, q_len: int, num_heads: int, head_dim: int, max_context_len: int,

@@ -267,6 +267,41 @@ WORKLOADS = {
 }
 
 
+@dataclasses.dataclass
+class SpecInputs:
+    """Inputs of one speculative-verification step: the target model's distributions at the
+    k draft positions plus one, the draft model's distributions and sampled draft tokens, and
+    the uniforms the accept/reject rule and the final draw consume."""
+    target_probs: np.ndarray   # f32 [N, k+1, V]
+    draft_probs: np.ndarray    # f32 [N, k, V]
+    draft_tokens: np.ndarray   # i32 [N, k]
+    u_accept: np.ndarray       # f32 [N, k]
+    u_sample: np.ndarray       # f32 [N]
+
+
+def spec_verify_inputs(num_seqs: int = 64, k: int = 4, vocab: int = 32000, seed: int = 2664,
+                       draft_temp: float = 1.0, noise: float = 1.0) -> SpecInputs:
+    """Synthetic model outputs: draft logits ~ N(0, 2^2) per token; target logits = draft logits
+    + N(0, noise^2), so the two models agree partly; both turned into distributions by a
+    softmax; draft tokens are drawn from the draft distributions; uniforms in [0, 1)."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed)))
+    dl = g.normal(0.0, 2.0, size=(num_seqs, k + 1, vocab))
+    tl = dl + g.normal(0.0, noise, size=dl.shape)
+
+    def softmax(x):
+        e = np.exp(x - x.max(axis=-1, keepdims=True))
+        return e / e.sum(axis=-1, keepdims=True)
+
+    target = softmax(tl).astype(np.float32)
+    draft = softmax(dl[:, :k] / draft_temp).astype(np.float32)
+    cdf = np.cumsum(draft.astype(np.float64), axis=-1)
+    r = g.random((num_seqs, k, 1)) * cdf[..., -1:]
+    tokens = np.minimum((cdf < r).sum(axis=-1), vocab - 1).astype(np.int32)
+    return SpecInputs(target_probs=target, draft_probs=draft, draft_tokens=tokens,
+                      u_accept=g.random((num_seqs, k), dtype=np.float32),
+                      u_sample=g.random(num_seqs, dtype=np.float32))
+
+
 def kv_bytes_per_token(num_layers: int, num_kv_heads: int, head_dim: int, elem_bytes: int) -> int:
     """Logical KV bytes one token occupies: 2 (K and V) x layers x kv heads x head dim x bytes.
 

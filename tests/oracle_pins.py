@@ -344,6 +344,53 @@ def pin_copy_on_write_fork(orc):
     assert np.max(np.abs(out - _sdpa_reference(ref_w))) <= 1e-12
 
 
+def pin_spec_verify_closed_forms(orc):
+    """Equal target and draft distributions accept every draft, then draw the bonus token from
+    the target's last row; a draft token the target gives probability 0 is rejected and the
+    replacement comes from the positive part of target - draft."""
+    v = 4
+    pl = np.array([[0.1, 0.2, 0.3, 0.4]] * 3, np.float32)[None]           # [1, k+1=3, V]
+    pd = pl[:, :2].copy()
+    acc, out = orc.spec_verify(pl, pd, np.array([[3, 1]], np.int32), np.array([[0.9, 0.9]], np.float32),
+                               np.array([0.25], np.float32))
+    assert acc[0] == 2 and list(out[0]) == [3, 1, 1]                      # prefix 0.1, 0.3 > 0.25
+    pl2 = np.array([[[0.5, 0.0, 0.25, 0.25]] * 2], np.float32)
+    pd2 = np.array([[[0.0, 1.0, 0.0, 0.0]]], np.float32)
+    acc, out = orc.spec_verify(pl2, pd2, np.array([[1]], np.int32), np.array([[0.0]], np.float32),
+                               np.array([0.6], np.float32))
+    assert acc[0] == 0 and list(out[0]) == [2, -1]                        # residual (0.5, 0, .25, .25)
+    assert v == pl.shape[-1]
+
+
+def pin_spec_verify_output_follows_target(orc):
+    """The page's guarantee: the emitted tokens are distributed exactly as target-model samples.
+    200,000 trials of a 6-token vocabulary, k = 2, independent positions: the first emitted token
+    follows target row 0, the second (when emitted) follows target row 1, and the first draft is
+    accepted with probability sum_t min(target, draft)."""
+    n, k, v = 200_000, 2, 6
+    g = np.random.Generator(np.random.PCG64(18))
+    pl = np.array([[0.05, 0.3, 0.1, 0.25, 0.2, 0.1], [0.4, 0.1, 0.1, 0.1, 0.2, 0.1],
+                   [0.2, 0.2, 0.2, 0.2, 0.1, 0.1]], np.float32)
+    pd = np.array([[0.3, 0.1, 0.2, 0.1, 0.1, 0.2], [0.1, 0.4, 0.1, 0.2, 0.1, 0.1]], np.float32)
+    tp = np.broadcast_to(pl, (n, k + 1, v)).copy()
+    dp = np.broadcast_to(pd, (n, k, v)).copy()
+    pd64 = pd.astype(np.float64)
+    tokens = np.stack([g.choice(v, size=n, p=pd64[i] / pd64[i].sum()) for i in range(k)], 1)
+    acc, out = orc.spec_verify(tp, dp, tokens.astype(np.int32), g.random((n, k), dtype=np.float32),
+                               g.random(n, dtype=np.float32))
+
+    def close(freq, p, m):
+        return np.all(np.abs(freq - p) <= 5 * np.sqrt(p * (1 - p) / m) + 1e-9)
+
+    f0 = np.bincount(out[:, 0], minlength=v) / n
+    assert close(f0, pl[0], n), f0
+    second = out[:, 1][out[:, 1] >= 0]
+    f1 = np.bincount(second, minlength=v) / second.size
+    assert close(f1, pl[1], second.size), f1
+    p_acc = float(np.minimum(pl[0], pd[0]).sum())
+    assert abs(np.mean(acc >= 1) - p_acc) <= 5 * np.sqrt(p_acc * (1 - p_acc) / n)
+
+
 def _bf16_bits(x: np.ndarray) -> np.ndarray:
     return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
@@ -355,4 +402,5 @@ ALL_PINS = [
     pin_block_permutation, pin_sharing_equals_duplication, pin_gqa_equals_replicated_mha,
     pin_chunk_rows_are_shorter_decodes, pin_append_matches_numpy_assignment,
     pin_append_completes_the_pool, pin_copy_blocks_matches_numpy_assignment, pin_copy_on_write_fork,
+    pin_spec_verify_closed_forms, pin_spec_verify_output_follows_target,
 ]

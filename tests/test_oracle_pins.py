@@ -18,8 +18,9 @@ def test_pin(orc, pin):
 # Each build plants one plausible mistake in the oracle (see the PLANT notes in
 # pa_oracle.c): 1 scale dropped, 2 interleaved head groups, 3 causal limit off
 # by one, 4 offsets reversed inside a block, 5 a softmax term left out of the
-# denominator, 6 chunk rows reversed, 7 V read from the K cache.
-@pytest.mark.parametrize("plant", [1, 2, 3, 4, 5, 6, 7])
+# denominator, 6 chunk rows reversed, 7 V read from the K cache, 8 the speculative
+# acceptance ratio inverted, 9 the speculative residual taken the wrong way round.
+@pytest.mark.parametrize("plant", [1, 2, 3, 4, 5, 6, 7, 8, 9])
 def test_planted_mistake_is_caught(plant):
     bad = oracle.load(plant)
     caught = []
