@@ -71,6 +71,7 @@ class Oracle:
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_double,
             ctypes.c_int, ctypes.c_int,
         ]
+        _f32p = ctypes.POINTER(ctypes.c_float)
         lib.oracle_reshape_and_cache.restype = ctypes.c_int
         lib.oracle_reshape_and_cache.argtypes = [
             _u16p, _u16p, _u16p, _u16p, _i64p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
@@ -83,6 +84,20 @@ class Oracle:
         lib.oracle_spec_verify.restype = ctypes.c_int
         lib.oracle_spec_verify.argtypes = [_i32p, _i32p, _f32p, _f32p, _i32p, _f32p, _f32p, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int]
+        _u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.oracle_e4m3_encode_vec.restype = None
+        lib.oracle_e4m3_encode_vec.argtypes = [_f32p, ctypes.c_int64, _u8p]
+        lib.oracle_e4m3_decode_vec.restype = None
+        lib.oracle_e4m3_decode_vec.argtypes = [_u8p, ctypes.c_int64, _f64p]
+        lib.oracle_reshape_and_cache_fp8.restype = ctypes.c_int
+        lib.oracle_reshape_and_cache_fp8.argtypes = [_u16p, _u16p, _u8p, _u8p, _i64p, ctypes.c_int64, ctypes.c_int,
+                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                                     ctypes.c_float, ctypes.c_float]
+        lib.oracle_decode_attention_fp8.restype = ctypes.c_int
+        lib.oracle_decode_attention_fp8.argtypes = [
+            _f64p, _u16p, _u8p, _u8p, _i32p, ctypes.c_int, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_int,
+            ctypes.c_float, ctypes.c_float, ctypes.c_int]
         lib.oracle_bits_to_double_vec.restype = None
         lib.oracle_bits_to_double_vec.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int, _f64p]
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -161,6 +176,51 @@ class Oracle:
         self._lib.oracle_spec_verify(_ptr(acc, _i32p), _ptr(out, _i32p), _ptr(tp, f32p), _ptr(dp, f32p),
                                      _ptr(dt, _i32p), _ptr(ua, f32p), _ptr(us, f32p), n, k, v)
         return acc, out
+
+
+    def e4m3_encode(self, x) -> np.ndarray:
+        a = np.ascontiguousarray(x, dtype=np.float32)
+        out = np.empty(a.shape, np.uint8)
+        self._lib.oracle_e4m3_encode_vec(_ptr(a, ctypes.POINTER(ctypes.c_float)), a.size,
+                                         _ptr(out, ctypes.POINTER(ctypes.c_uint8)))
+        return out
+
+    def e4m3_decode(self, b) -> np.ndarray:
+        a = np.ascontiguousarray(b, dtype=np.uint8)
+        out = np.empty(a.shape, np.float64)
+        self._lib.oracle_e4m3_decode_vec(_ptr(a, ctypes.POINTER(ctypes.c_uint8)), a.size, _ptr(out, _f64p))
+        return out
+
+    def reshape_and_cache_fp8(self, key, value, key_cache, value_cache, slot_mapping, dtype: str,
+                              k_scale: float, v_scale: float) -> int:
+        """Quantising append into uint8 (e4m3) caches, IN PLACE."""
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        k = np.ascontiguousarray(key, dtype=np.uint16)
+        v = np.ascontiguousarray(value, dtype=np.uint16)
+        sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        assert key_cache.dtype == np.uint8 and key_cache.flags["C_CONTIGUOUS"] and value_cache.flags["C_CONTIGUOUS"]
+        nb, bs, hkv, d = key_cache.shape
+        return int(self._lib.oracle_reshape_and_cache_fp8(
+            _ptr(k, _u16p), _ptr(v, _u16p), _ptr(key_cache, u8p), _ptr(value_cache, u8p), _ptr(sm, _i64p),
+            sm.shape[0], hkv, d, bs, nb, DTYPES[dtype], float(k_scale), float(v_scale)))
+
+    def decode_attention_fp8(self, query, key_cache, value_cache, block_tables, context_lens, scale: float,
+                             dtype: str, k_scale: float, v_scale: float, num_threads: int = 0):
+        """Attention over uint8 (e4m3) caches; query 16-bit bits of `dtype`.  Returns (out fp64, bad)."""
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        q = np.ascontiguousarray(query, dtype=np.uint16)
+        kc = np.ascontiguousarray(key_cache, dtype=np.uint8)
+        vc = np.ascontiguousarray(value_cache, dtype=np.uint8)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        n, q_len, hq, d = q.shape
+        nb, bs, hkv, _ = kc.shape
+        out = np.empty((n, q_len, hq, d), dtype=np.float64)
+        bad = self._lib.oracle_decode_attention_fp8(
+            _ptr(out, _f64p), _ptr(q, _u16p), _ptr(kc, u8p), _ptr(vc, u8p), _ptr(bt, _i32p), bt.shape[1],
+            _ptr(cl, _i32p), n, q_len, hq, hkv, d, bs, nb, float(scale), DTYPES[dtype], float(k_scale),
+            float(v_scale), int(num_threads))
+        return out, int(bad)
 
 
 def load(plant: int = 0) -> Oracle:

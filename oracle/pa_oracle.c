@@ -360,6 +360,160 @@ int oracle_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* 
     return 0;
 }
 
+/*
+ * FP8 KV cache ("LLM 推理优化的系统视角", section 4.1: quantising the KV cache reduces its
+ * bytes).  Reading (the pages fix no format): OCP FP8 E4M3 (1 sign, 4 exponent bits,
+ * bias 7, 3 mantissa bits, no infinities, S.1111.111 = NaN, largest finite 448) with
+ * one fp32 scale per cache tensor; stored byte = e4m3(x / scale) with the quotient in
+ * fp32 and rounded to nearest even, saturating to +-448; read value = e4m3 * scale.
+ */
+static double round_half_even(double x)
+{
+    double f = floor(x), d = x - f;
+    if (d > 0.5) return f + 1.0;
+    if (d < 0.5) return f;
+    return fmod(f, 2.0) == 0.0 ? f : f + 1.0;
+}
+
+uint8_t oracle_e4m3_encode(float v)
+{
+    if (v != v) return 0x7f;
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    const double a = fabs((double)v);
+    if (a >= 448.0) return sign | 0x7e;                       /* saturate */
+    if (a < ldexp(1.0, -6)) {                                 /* subnormal: units of 2^-9 */
+        double r = round_half_even(a / ldexp(1.0, -9));
+        return sign | (uint8_t)r;                             /* r == 8 is exponent field 1, mantissa 0 */
+    }
+    int E;
+    frexp(a, &E);                                             /* a = f * 2^E, f in [0.5, 1) */
+    int e = E - 1;                                            /* a in [2^e, 2^(e+1)) */
+    double r = round_half_even((a / ldexp(1.0, e) - 1.0) * 8.0);
+    if (r == 8.0) { e += 1; r = 0.0; }
+    return sign | (uint8_t)((e + 7) << 3) | (uint8_t)r;
+}
+
+double oracle_e4m3_decode(uint8_t b)
+{
+    const int sign = b >> 7, field = (b >> 3) & 0xf, mant = b & 7;
+    double v;
+    if (field == 15 && mant == 7) return NAN;
+    if (field == 0) v = ldexp((double)mant, -9);
+    else v = ldexp(1.0 + mant / 8.0, field - 7);
+    return sign ? -v : v;
+}
+
+void oracle_e4m3_encode_vec(const float* x, int64_t n, uint8_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(x[i]);
+}
+
+void oracle_e4m3_decode_vec(const uint8_t* b, int64_t n, double* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(b[i]);
+}
+
+/* Append into FP8 caches: row t of key / value (16-bit, dtype) quantised with the scales. */
+int oracle_reshape_and_cache_fp8(const uint16_t* key, const uint16_t* value, uint8_t* key_cache,
+                                 uint8_t* value_cache, const int64_t* slot_mapping, int64_t num_tokens,
+                                 int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                 int dtype, float k_scale, float v_scale)
+{
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    int bad = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * block_size) { ++bad; continue; }
+        for (int64_t e = 0; e < row; ++e) {
+            float k = (float)oracle_bits_to_double(key[t * row + e], dtype);
+            float v = (float)oracle_bits_to_double(value[t * row + e], dtype);
+            key_cache[slot * row + e] = oracle_e4m3_encode(k / k_scale);
+            value_cache[slot * row + e] = oracle_e4m3_encode(v / v_scale);
+        }
+    }
+    return bad;
+}
+
+/*
+ * Paged decode attention over FP8 caches: as oracle_decode_attention, with every K
+ * element read as e4m3 * k_scale and every V element as e4m3 * v_scale (fp64).
+ */
+int oracle_decode_attention_fp8(double* out, const uint16_t* query, const uint8_t* key_cache,
+                                const uint8_t* value_cache, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                                int q_len, int num_heads, int num_kv_heads, int head_dim,
+                                int block_size, int64_t num_blocks, double scale, int dtype,
+                                float k_scale, float v_scale, int num_threads)
+{
+    const int group = num_heads / num_kv_heads;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    int bad = 0;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+    (void)num_threads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+    for (int i = 0; i < num_seqs; ++i) {
+        const int L = context_lens[i];
+        double* o_seq = out + (int64_t)i * q_len * num_heads * head_dim;
+        int ok = L >= q_len && L >= 1 && head_dim <= 1024 && (L + block_size - 1) / block_size <= max_blocks_per_seq;
+        double *K = NULL, *V = NULL, *s = NULL;
+        if (ok) {
+            K = (double*)malloc(sizeof(double) * L * row);
+            V = (double*)malloc(sizeof(double) * L * row);
+            s = (double*)malloc(sizeof(double) * L);
+            const int32_t* table = block_tables + (int64_t)i * max_blocks_per_seq;
+            ok = K && V && s;
+            /* concatenate the blocks in logical order, dequantising */
+            for (int p = 0; ok && p < L; ++p) {
+                int32_t blk = table[p / block_size];
+                if (blk < 0 || (int64_t)blk >= num_blocks) { ok = 0; break; }
+                const int64_t base = ((int64_t)blk * block_size + p % block_size) * row;
+                for (int64_t e = 0; e < row; ++e) {
+                    K[(int64_t)p * row + e] = oracle_e4m3_decode(key_cache[base + e]) * (double)k_scale;
+                    V[(int64_t)p * row + e] = oracle_e4m3_decode(value_cache[base + e]) * (double)v_scale;
+                }
+            }
+        }
+        if (!ok) {
+            for (int64_t e = 0; e < (int64_t)q_len * num_heads * head_dim; ++e) o_seq[e] = NAN;
+            bad += 1;
+            free(K); free(V); free(s);
+            continue;
+        }
+        for (int j = 0; j < q_len; ++j) {
+            const int last = L - q_len + j;
+            for (int h = 0; h < num_heads; ++h) {
+                const int kvh = h / group;
+                const uint16_t* qrow = query + (((int64_t)i * q_len + j) * num_heads + h) * head_dim;
+                double* o = o_seq + ((int64_t)j * num_heads + h) * head_dim;
+                double qd[1024];
+                for (int k = 0; k < head_dim; ++k) qd[k] = oracle_bits_to_double(qrow[k], dtype);
+                double m = -INFINITY;
+                for (int p = 0; p <= last; ++p) {
+                    const double* kp = K + ((int64_t)p * num_kv_heads + kvh) * head_dim;
+                    double dot = 0.0;
+                    for (int k = 0; k < head_dim; ++k) dot += qd[k] * kp[k];
+                    s[p] = scale * dot;
+                    if (s[p] > m) m = s[p];
+                }
+                double den = 0.0;
+                for (int p = 0; p <= last; ++p) { s[p] = exp(s[p] - m); den += s[p]; }
+                for (int k = 0; k < head_dim; ++k) o[k] = 0.0;
+                for (int p = 0; p <= last; ++p) {
+                    const double* vp = V + ((int64_t)p * num_kv_heads + kvh) * head_dim;
+                    for (int k = 0; k < head_dim; ++k) o[k] += s[p] * vp[k];
+                }
+                for (int k = 0; k < head_dim; ++k) o[k] /= den;
+            }
+        }
+        free(K); free(V); free(s);
+    }
+    return bad;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

@@ -391,6 +391,54 @@ def pin_spec_verify_output_follows_target(orc):
     assert abs(np.mean(acc >= 1) - p_acc) <= 5 * np.sqrt(p_acc * (1 - p_acc) / n)
 
 
+def pin_e4m3_codes(orc):
+    """FP8 E4M3 decode of all 256 codes equals torch's float8_e4m3fn; encode equals torch's
+    round-to-nearest-even cast below the overflow midpoint (464), including exact ties between
+    neighbouring codes, and saturates to +-448 above it."""
+    codes = np.arange(256, dtype=np.uint8)
+    mine = orc.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan) and np.array_equal(mine[~nan], ref[~nan])
+    g = np.random.Generator(np.random.PCG64(19))
+    pos = np.sort(ref[(~nan) & (ref > 0)])
+    ties = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)            # exact in fp32
+    x = np.concatenate([g.standard_normal(200_000).astype(np.float32) * np.float32(40),
+                        g.standard_normal(20_000).astype(np.float32) * np.float32(2 ** -8), ties, -ties])
+    x = x[np.abs(x) < 464]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(orc.e4m3_encode(x), want)
+    assert list(orc.e4m3_encode(np.array([500, -1000, 464.5, 448], np.float32))) == [0x7E, 0xFE, 0x7E, 0x7E]
+
+
+def pin_fp8_attention_is_attention_on_dequantised_cache(orc):
+    """With power-of-two scales every dequantised value is a bf16 number, so FP8 attention must
+    equal, bit for bit, the (SDPA-pinned) 16-bit attention over a bf16 copy of the dequantised
+    cache.  The quantising append equals the library cast of the fp32 quotient."""
+    w = W.make_workload("fp8", [5, 23, 40, 17], num_heads=8, num_kv_heads=2, head_dim=64, q_len=2,
+                        num_blocks=12, seed=20)
+    ks, vs = 0.25, 2.0
+    kc8 = np.zeros(w.key_cache.shape, np.uint8)
+    vc8 = np.zeros(w.value_cache.shape, np.uint8)
+    # history: quantise the pool's valid rows; then the append quantises the new rows
+    k32 = _bits_to_f64_lib(w.key_cache, "bf16").astype(np.float32)
+    v32 = _bits_to_f64_lib(w.value_cache, "bf16").astype(np.float32)
+    kc8[...] = orc.e4m3_encode(np.nan_to_num(k32) / np.float32(ks))
+    vc8[...] = orc.e4m3_encode(np.nan_to_num(v32) / np.float32(vs))
+    assert orc.reshape_and_cache_fp8(w.new_key, w.new_value, kc8, vc8, w.slot_mapping, "bf16", ks, vs) == 0
+    nk32 = _bits_to_f64_lib(w.new_key, "bf16").astype(np.float32)
+    want = torch.from_numpy(nk32 / np.float32(ks)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = kc8.reshape(-1, 2, 64)[w.slot_mapping]
+    assert np.array_equal(got, want)
+    out8, bad = orc.decode_attention_fp8(w.query, kc8, vc8, w.block_tables, w.context_lens, w.scale, "bf16", ks, vs)
+    assert bad == 0
+    deq_k = _bf16_bits((orc.e4m3_decode(kc8) * ks).astype(np.float32))
+    deq_v = _bf16_bits((orc.e4m3_decode(vc8) * vs).astype(np.float32))
+    assert np.array_equal(_bits_to_f64_lib(deq_k, "bf16"), orc.e4m3_decode(kc8) * ks)   # exact in bf16
+    ref = _run(orc, w, key_cache=deq_k, value_cache=deq_v)
+    assert np.array_equal(out8, ref)
+
+
 def _bf16_bits(x: np.ndarray) -> np.ndarray:
     return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
@@ -402,5 +450,6 @@ ALL_PINS = [
     pin_block_permutation, pin_sharing_equals_duplication, pin_gqa_equals_replicated_mha,
     pin_chunk_rows_are_shorter_decodes, pin_append_matches_numpy_assignment,
     pin_append_completes_the_pool, pin_copy_blocks_matches_numpy_assignment, pin_copy_on_write_fork,
-    pin_spec_verify_closed_forms, pin_spec_verify_output_follows_target,
+    pin_spec_verify_closed_forms, pin_spec_verify_output_follows_target, pin_e4m3_codes,
+    pin_fp8_attention_is_attention_on_dequantised_cache,
 ]
