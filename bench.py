@@ -292,6 +292,12 @@ def run_ours(args, rank, world, local):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(tdt)
 
     kc, vc = up(w.key_cache), up(w.value_cache)
+    kv8 = args.kv == "fp8"
+    K_SCALE, V_SCALE = 0.05, 0.03
+    if kv8:   # the same history, quantised to FP8 E4M3 with one scale per cache
+        kc = (kc.float() / K_SCALE).to(torch.float8_e4m3fn).view(torch.uint8)
+        vc = (vc.float() / V_SCALE).to(torch.float8_e4m3fn).view(torch.uint8)
+        torch.cuda.empty_cache()
     nk, nv = up(w.new_key), up(w.new_value)
     q = up(w.query)
     out = torch.empty_like(q)
@@ -304,6 +310,12 @@ def run_ours(args, rank, world, local):
     pa.get_device_error(clear=True)
 
     def step():
+        if kv8:
+            pa.reshape_and_cache_fp8(nk, nv, kc, vc, sm, K_SCALE, V_SCALE, stream=stream)
+            n1 = pa.last_launch_count()
+            pa.decode_attention_fp8kv(out, q, kc, vc, bt, cl, w.scale, w.max_context_len, ws, K_SCALE, V_SCALE,
+                                      stream=stream)
+            return n1 + pa.last_launch_count()
         pa.reshape_and_cache(nk, nv, kc, vc, sm, stream=stream)
         n1 = pa.last_launch_count()
         pa.decode_attention(out, q, kc, vc, bt, cl, w.scale, w.max_context_len, ws, stream=stream)
@@ -313,8 +325,8 @@ def run_ours(args, rank, world, local):
         launches_per_step = step()
     torch.cuda.synchronize(dev)
 
-    attn_bytes = W.attention_bytes(w)
-    step_bytes = attn_bytes + W.append_bytes(w)
+    attn_bytes = W.attention_bytes(w, 1 if kv8 else None)
+    step_bytes = attn_bytes + W.append_bytes(w, 1 if kv8 else None)
     seq_tokens = int(w.context_lens.astype(np.int64).sum())
     flush = None
     if step_bytes < 2 * L2_BYTES:   # small working set: flush L2 between steps
@@ -409,7 +421,7 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": DESCR[cfg], "seq_tokens_per_step": seq_tokens, "bytes_per_step": step_bytes,
-                   "attention_bytes": attn_bytes, "partition_tokens": 512, "math": args.math,
+                   "attention_bytes": attn_bytes, "partition_tokens": 512, "math": args.math, "kv_cache": args.kv,
                    "l2": "flushed between steps" if flush is not None else
                    f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step vs 129 MB L2)",
                    "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
@@ -530,6 +542,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", choices=["decode_step", "copy_blocks", "spec_verify"], default="decode_step",
                     help="decode_step: the timed hot path; copy_blocks / spec_verify: those steps alone")
+    ap.add_argument("--kv", choices=["16bit", "fp8"], default="16bit",
+                    help="KV cache element type: the workload's 16-bit type, or FP8 E4M3 with per-cache scales")
     ap.add_argument("--math", choices=["auto", "fma", "tensor"], default="auto",
                     help="decode consumer arithmetic (auto: CUDA cores for one row per kv head, else tensor cores)")
     args = ap.parse_args()

@@ -248,6 +248,37 @@ int pa_decode_attention_noalloc(void* out, const void* query, const void* key_ca
                                 int64_t num_blocks, int max_context_len, float scale, int dtype,
                                 int partition_size, void* stream);
 
+/*
+ * FP8 KV cache ([P3] section 4.1: quantising the KV cache cuts its bytes; the
+ * pages fix no format).  Caches hold one FP8 E4M3 byte per element (OCP E4M3: bias
+ * 7, 3 mantissa bits, largest finite 448, no infinities), in the same
+ * [num_blocks, 16, num_kv_heads, head_dim] layout, with one fp32 scale per cache
+ * tensor: stored = e4m3(x / scale), read back as e4m3 * scale.
+ *
+ * pa_reshape_and_cache_fp8: as pa_reshape_and_cache, but key/value (16-bit, dtype)
+ * are divided by k_scale / v_scale in fp32 (round to nearest) and stored as E4M3,
+ * rounded to nearest even and saturated to +-448.  key_cache/value_cache are
+ * uint8 [num_blocks, 16, num_kv_heads, head_dim].  Scales must be finite and > 0.
+ *
+ * pa_decode_attention_fp8kv: as pa_decode_attention_ex over FP8 caches (query and
+ * out stay 16-bit, of dtype).  K and V are widened exactly to fp16 in shared
+ * memory; the score and P.V products run on the tensor cores in fp16 with fp32
+ * accumulation (a bf16 query is rounded to fp16 for them), k_scale folds into the
+ * softmax scale and v_scale into the output.  head_dim 128 only; the workspace is
+ * sized as for pa_decode_attention_ex.
+ */
+int pa_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache, void* value_cache,
+                             const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads, int head_dim,
+                             int block_size, int64_t num_blocks, int dtype, float k_scale, float v_scale,
+                             void* stream);
+
+int pa_decode_attention_fp8kv(void* out, const void* query, const void* key_cache, const void* value_cache,
+                              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                              int num_seqs, int q_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                              int64_t num_blocks, int max_context_len, float scale, int dtype, float k_scale,
+                              float v_scale, int partition_size, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* pa_status_string(int status);
 

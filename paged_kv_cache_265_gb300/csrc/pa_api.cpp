@@ -168,6 +168,74 @@ int pa_decode_attention_ex(void* out, const void* query, const void* key_cache, 
     return rc;
 }
 
+int pa_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache, void* value_cache,
+                             const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads, int head_dim,
+                             int block_size, int64_t num_blocks, int dtype, float k_scale, float v_scale,
+                             void* stream) {
+    t_last_launches = 0;
+    if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 1) return PA_ERR_INVALID_ARG;
+    if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
+        return PA_ERR_INVALID_ARG;
+    if (block_size != PA_BLOCK_SIZE || !supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
+        return PA_ERR_INVALID_ARG;
+    int launches = 0;
+    const int st = pa::launch_reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, num_tokens,
+                                                    num_kv_heads * head_dim, num_blocks * block_size, dtype, k_scale,
+                                                    v_scale, static_cast<cudaStream_t>(stream), &launches);
+    t_last_launches = launches;
+    return st;
+}
+
+int pa_decode_attention_fp8kv(void* out, const void* query, const void* key_cache, const void* value_cache,
+                              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                              int num_seqs, int q_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                              int64_t num_blocks, int max_context_len, float scale, int dtype, float k_scale,
+                              float v_scale, int partition_size, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+    t_last_launches = 0;
+    const int st = check_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                                context_lens, num_seqs, q_len, num_heads, num_kv_heads, head_dim, block_size,
+                                num_blocks, max_context_len, scale, dtype, partition_size);
+    if (st != PA_OK || num_seqs == 0) return st;
+    if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
+        return PA_ERR_INVALID_ARG;
+    const int partition = partition_size == 0 ? PA_DEFAULT_PARTITION : partition_size;
+    const size_t need = pa::ws_layout(num_seqs, q_len, num_heads, head_dim, max_context_len, partition).total;
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+    pa::DecodeArgs a;
+    a.out = out;
+    a.query = query;
+    a.key_cache = key_cache;
+    a.value_cache = value_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_seqs = num_seqs;
+    a.q_len = q_len;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.num_blocks = num_blocks;
+    a.max_context_len = max_context_len;
+    a.scale = scale;
+    a.dtype = dtype;
+    a.partition = partition;
+    a.workspace = workspace;
+    a.fp8 = true;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    int launches = 0;
+    const int rc = pa::launch_decode(a, static_cast<cudaStream_t>(stream), &launches);
+    t_last_launches = launches;
+    return rc;
+}
+
 int pa_decode_attention(void* out, const void* query, const void* key_cache, const void* value_cache,
                         const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
                         int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,

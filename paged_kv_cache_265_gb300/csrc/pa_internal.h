@@ -69,6 +69,9 @@ struct DecodeArgs {
     int dtype;
     int partition;
     void* workspace;
+    bool fp8 = false;     // key/value caches hold FP8 E4M3 bytes
+    float k_scale = 1.f;  // their dequantisation scales
+    float v_scale = 1.f;
 };
 
 // Launchers: return a pa_status; `launches` receives the number of kernels enqueued.
@@ -79,6 +82,9 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int* launches);
 int launch_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* target_probs,
                        const float* draft_probs, const int32_t* draft_tokens, const float* u_accept,
                        const float* u_sample, int num_seqs, int k, int vocab, cudaStream_t stream, int* launches);
+int launch_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache, void* value_cache,
+                                 const int64_t* slot_mapping, int64_t num_tokens, int row_elems, int64_t num_slots,
+                                 int dtype, float k_scale, float v_scale, cudaStream_t stream, int* launches);
 int launch_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_mapping, int64_t num_pairs,
                        int block_bytes, int64_t num_blocks, cudaStream_t stream, int* launches);
 int read_device_error(int32_t* flags, int clear, cudaStream_t stream);

@@ -28,6 +28,7 @@
 #include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 #include <utility>
 
 #include "pa_device.cuh"
@@ -85,6 +86,64 @@ __global__ void __launch_bounds__(256) reshape_kernel(const uint4* __restrict__ 
         const uint4* src = which ? value : key;
         uint4* dst = which ? value_cache : key_cache;
         dst[slot * row_vecs + v] = __ldg(src + t * row_vecs + v);
+    }
+}
+
+// Eight 16-bit values (one 16-byte chunk) widened to fp32.
+template <typename T>
+__device__ __forceinline__ void unpack8(const uint4 raw, float (&f)[8]) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (Elem<T>::kDtype == PA_BF16) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        } else {
+            const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            f[2 * i] = v.x;
+            f[2 * i + 1] = v.y;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// KV append into FP8 caches: each 16-bit element divided by the cache's scale in
+// fp32 (round to nearest) and stored as E4M3, rounded to nearest even, saturating.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    unsigned short d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) reshape_fp8_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                                                          uint2* __restrict__ key_cache, uint2* __restrict__ value_cache,
+                                                          const long long* __restrict__ slots, long long num_tokens,
+                                                          int row_vecs, long long num_slots, float k_scale,
+                                                          float v_scale) {
+    griddep_launch_dependents();
+    const long long per_token = 2LL * row_vecs;  // 8 elements per vector
+    const long long total = num_tokens * per_token;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long t = idx / per_token;
+        const int rem = (int)(idx - t * per_token);
+        const int which = rem >= row_vecs;
+        const int v = rem - which * row_vecs;
+        const long long slot = __ldg(slots + t);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (rem == 0) atomicOr(&g_pa_error, PA_DEVERR_SLOT);
+            continue;
+        }
+        float f[8];
+        unpack8<T>(__ldg((which ? value : key) + t * row_vecs + v), f);
+        const float sc = which ? v_scale : k_scale;
+        uint32_t b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) b[i] = f32x2_to_e4m3x2(__fdiv_rn(f[2 * i], sc), __fdiv_rn(f[2 * i + 1], sc));
+        (which ? value_cache : key_cache)[slot * row_vecs + v] = make_uint2(b[0] | b[1] << 16, b[2] | b[3] << 16);
     }
 }
 
@@ -442,7 +501,8 @@ struct alignas(128) DecodeParams {
     int mtiles;        // ceil(rows / 16) tensor-core row tiles
     int block_splits;  // kConsumerWarps / mtiles warps share a tile's blocks
     int slot_rows;     // min(16, rows): rows each warp leaves in the combine buffer
-    float scale_log2;  // scale * log2(e)
+    float scale_log2;  // scale * log2(e) (times the K dequantisation scale for an FP8 cache)
+    float v_scale;     // V dequantisation scale (1 for 16-bit caches)
 };
 
 struct UnitInfo {
@@ -460,9 +520,10 @@ struct SmemLayout {
 constexpr int kFmaWarpFloats = 8 * 16 + 8;
 
 __host__ __device__ inline SmemLayout smem_layout(int head_dim, int stages, int mtiles, int tile_rows, int slot_rows,
-                                                  bool fma = false) {
+                                                  bool fma = false, bool f8 = false) {
     SmemLayout s;
-    s.stage_bytes = 2 * (head_dim / kBoxCols) * kBoxBytes;  // K boxes then V boxes
+    // 16-bit caches: K boxes then V boxes; FP8 caches: the K box then the V box (128 B rows); all swizzled
+    s.stage_bytes = f8 ? 2 * kBlock * head_dim : 2 * (head_dim / kBoxCols) * kBoxBytes;
     s.qpitch = head_dim * 2 + 16;                            // padded query rows
     s.q_half_bytes = mtiles * tile_rows * s.qpitch;
     s.off_q = stages * s.stage_bytes;
@@ -514,23 +575,6 @@ __device__ __forceinline__ bool consumers_any(bool v) {
     return r != 0;
 }
 
-// Eight 16-bit values (one 16-byte chunk) widened to fp32.
-template <typename T>
-__device__ __forceinline__ void unpack8(const uint4 raw, float (&f)[8]) {
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        if constexpr (Elem<T>::kDtype == PA_BF16) {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        } else {
-            const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-            f[2 * i] = v.x;
-            f[2 * i + 1] = v.y;
-        }
-    }
-}
-
 // Sum of 8 per-row partials over the 2^LCH lanes of a lane group, transposed: three
 // halving exchange stages on lane bits LCH-1, LCH-2, LCH-3 leave each lane with the total
 // of row ((lane >> (LCH-3)) & 7); remaining lower bits are summed as a plain all-reduce.
@@ -560,18 +604,35 @@ __device__ __forceinline__ float transpose_reduce8(const float (&part)[8], int l
 }
 
 // Resident CTAs per SM each kernel variant is built for (its register budget).
-__host__ __device__ constexpr int decode_ctas_per_sm(int nt, int rt) {
-    return rt == 0 ? (nt == 1 ? PA_CTAS_PER_SM_NT1 : PA_CTAS_PER_SM_NT2) : (rt <= 2 ? 4 : (rt == 4 ? 3 : 2));
+__host__ __device__ constexpr int decode_ctas_per_sm(int nt, int rt, bool f8 = false) {
+    return f8 ? (nt == 1 ? 4 : 2)
+              : rt == 0 ? (nt == 1 ? PA_CTAS_PER_SM_NT1 : PA_CTAS_PER_SM_NT2) : (rt <= 2 ? 4 : (rt == 4 ? 3 : 2));
+}
+
+// Two FP8 E4M3 values (low byte first) widened exactly to a pair of fp16 values.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    uint32_t d;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(d) : "r"(two));
+    return d;
+}
+
+// A pair of bf16 values (one register) as a pair of fp16 values.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
+    const float lo = __uint_as_float(x << 16), hi = __uint_as_float(x & 0xffff0000u);
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
 }
 
 // NT: query rows per consumer warp / 8 on the tensor-core path (RT == 0).
 // RT > 0 selects the CUDA-core path for up to RT (1, 2, 4 or 8) query rows per kv head.
-template <typename T, int D, int NT, int RT>
-__global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT))
+// F8: the K/V caches hold FP8 E4M3 bytes (tensor-core path, fp16 products).
+template <typename T, int D, int NT, int RT, bool F8>
+__global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
     decode_kernel(const __grid_constant__ DecodeParams p) {
+    using MT = std::conditional_t<F8, __half, T>;  // element type of the tensor-core products
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const SmemLayout lay = smem_layout(D, p.stages, p.mtiles, 8 * NT, p.slot_rows, RT > 0);
+    const SmemLayout lay = smem_layout(D, p.stages, p.mtiles, 8 * NT, p.slot_rows, RT > 0, F8);
     const int qpitch = lay.qpitch;
     constexpr int kRowBytes = D * 2;
     constexpr int kBoxes = D / kBoxCols;  // boxes per K (or V) block
@@ -712,6 +773,12 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT))
                         const uint32_t bar = full0 + 8 * s;
                         if (b_bad) {
                             mbar_arrive(bar);  // nothing to wait for; the consumers compute on stale data
+                        } else if constexpr (F8) {
+                            mbar_arrive_expect_tx(bar, 2 * kBlock * D);
+                            const uint32_t dst = smem_addr(stage_base + s * lay.stage_bytes);
+                            const int y0 = valid - kBlock;  // <= 0; rows before token 0 arrive as zeros
+                            tma_load_4d(dst, &p.tmap_k, 0, kvh, y0, b, bar, pol_stream);
+                            tma_load_4d(dst + kBlock * D, &p.tmap_v, 0, kvh, y0, b, bar, pol_stream);
                         } else {
                             mbar_arrive_expect_tx(bar, 2 * kBoxes * kBoxBytes);
                             const uint32_t dst = smem_addr(stage_base + s * lay.stage_bytes);
@@ -817,6 +884,29 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT))
                         ldsm_x4(smem_addr(qrow + rr * qpitch + cc * 2), qf[nt][2 * k2][0], qf[nt][2 * k2][1],
                                 qf[nt][2 * k2 + 1][0], qf[nt][2 * k2 + 1][1]);
                     }
+                if constexpr (F8) {
+                    // Same permuted contraction order as the K fragments: step kk of lane tig
+                    // takes query elements tig*32 + kk*4 .. +3; products run in fp16.
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const uint8_t* qr = qrow + (nt * 8 + gid) * qpitch + tig * 64;
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            const uint4 x = *reinterpret_cast<const uint4*>(qr + c4 * 16);
+                            const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                uint32_t r0 = w4[2 * h], r1 = w4[2 * h + 1];
+                                if constexpr (Elem<T>::kDtype == PA_BF16) {
+                                    r0 = bf16x2_to_f16x2(r0);
+                                    r1 = bf16x2_to_f16x2(r1);
+                                }
+                                qf[nt][c4 * 2 + h][0] = r0;
+                                qf[nt][c4 * 2 + h][1] = r1;
+                            }
+                        }
+                    }
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qempty0 + 8 * qb);
 
@@ -850,14 +940,40 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT))
                         float sc[NT][4];
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                        if constexpr (F8) {
+                            // FP8 stage, 128 B rows, 128-byte swizzled.  The head-dim order of the
+                            // contraction is permuted (Q's fragments follow it): the lane's four
+                            // k columns of step kk are bytes t*32 + kk*4 .. +3 of its token rows, so
+                            // each register is one adjacent E4M3 pair widened to fp16.
+                            const uint8_t* k8 = stage_base + s * lay.stage_bytes;
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            uint32_t a[4];
-                            const int tr = (lane & 7) + ((lane >> 3) & 1) * 8;
-                            const int cc = kk * 16 + (lane >> 4) * 8;
-                            ldsm_x4(kst + swz(tr, cc), a[0], a[1], a[2], a[3]);
+                            for (int h = 0; h < 2; ++h) {
+                                const uint4 lo = *reinterpret_cast<const uint4*>(
+                                    k8 + gid * 128 + ((((tig * 2 + h) ^ (gid & 7))) << 4));
+                                const uint4 hi = *reinterpret_cast<const uint4*>(
+                                    k8 + (gid + 8) * 128 + ((((tig * 2 + h) ^ ((gid + 8) & 7))) << 4));
+                                const uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w};
+                                const uint32_t wh[4] = {hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) Elem<T>::mma(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+                                for (int q4 = 0; q4 < 4; ++q4) {
+                                    const int kk = h * 4 + q4;
+                                    const uint32_t a[4] = {e4m3x2_to_f16x2(wl[q4] & 0xffff), e4m3x2_to_f16x2(wh[q4] & 0xffff),
+                                                           e4m3x2_to_f16x2(wl[q4] >> 16), e4m3x2_to_f16x2(wh[q4] >> 16)};
+#pragma unroll
+                                    for (int nt = 0; nt < NT; ++nt)
+                                        Elem<MT>::mma(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                uint32_t a[4];
+                                const int tr = (lane & 7) + ((lane >> 3) & 1) * 8;
+                                const int cc = kk * 16 + (lane >> 4) * 8;
+                                ldsm_x4(kst + swz(tr, cc), a[0], a[1], a[2], a[3]);
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt) Elem<MT>::mma(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+                            }
                         }
                         // Scale into log2 units; mask positions past each row's limit (and the zero rows
                         // in front of a short block).
@@ -908,25 +1024,59 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT))
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {
                                 const float x0 = pr[nt][2 * h], x1 = pr[nt][2 * h + 1];
-                                const float h0 = Elem<T>::round_trip(x0), h1 = Elem<T>::round_trip(x1);
-                                pb_hi[nt][h] = movmatrix_trans(Elem<T>::pack(h0, h1));
-                                pb_lo[nt][h] = movmatrix_trans(Elem<T>::pack(x0 - h0, x1 - h1));
+                                const float h0 = Elem<MT>::round_trip(x0), h1 = Elem<MT>::round_trip(x1);
+                                pb_hi[nt][h] = movmatrix_trans(Elem<MT>::pack(h0, h1));
+                                pb_lo[nt][h] = movmatrix_trans(Elem<MT>::pack(x0 - h0, x1 - h1));
                             }
+                        if constexpr (F8) {
+                            // Output columns are permuted inside each 16-column tile: tile dt's rows
+                            // gid and gid+8 are head-dim columns gid*16 + 2dt and +1, so the lane
+                            // needs bytes gid*16 .. +15 of its four token rows 2t, 2t+1, 2t+8, 2t+9;
+                            // a byte permute pairs the two tokens of each column.
+                            const uint8_t* v8 = stage_base + s * lay.stage_bytes + kBlock * D;
+                            uint32_t vw[4][4];
 #pragma unroll
-                        for (int dt = 0; dt < D / 16; ++dt) {
-                            uint32_t a[4];
-                            const int tr = (lane & 7) + (lane >> 4) * 8;
-                            const int cc = dt * 16 + ((lane >> 3) & 1) * 8;
-                            ldsm_x4_trans(vst + swz(tr, cc), a[0], a[1], a[2], a[3]);
+                            for (int rr = 0; rr < 4; ++rr) {
+                                const int r = 2 * tig + (rr & 1) + (rr >> 1) * 8;
+                                const uint4 x = *reinterpret_cast<const uint4*>(v8 + r * 128 + ((gid ^ (r & 7)) << 4));
+                                vw[rr][0] = x.x;
+                                vw[rr][1] = x.y;
+                                vw[rr][2] = x.z;
+                                vw[rr][3] = x.w;
+                            }
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(empty0 + 8 * s);  // stage consumed: everything is in registers
 #pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                Elem<T>::mma(o[dt][nt], a, pb_hi[nt][0], pb_hi[nt][1]);
-                                Elem<T>::mma(o[dt][nt], a, pb_lo[nt][0], pb_lo[nt][1]);
+                            for (int dt = 0; dt < D / 16; ++dt) {
+                                const int w = dt >> 1, b = (dt & 1) * 2;
+                                const uint32_t sel = b | (4 + b) << 4 | (b + 1) << 8 | (5 + b) << 12;
+                                const uint32_t p01 = __byte_perm(vw[0][w], vw[1][w], sel);  // tokens 2t, 2t+1
+                                const uint32_t p89 = __byte_perm(vw[2][w], vw[3][w], sel);  // tokens 2t+8, 2t+9
+                                const uint32_t a[4] = {e4m3x2_to_f16x2(p01 & 0xffff), e4m3x2_to_f16x2(p01 >> 16),
+                                                       e4m3x2_to_f16x2(p89 & 0xffff), e4m3x2_to_f16x2(p89 >> 16)};
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    Elem<MT>::mma(o[dt][nt], a, pb_hi[nt][0], pb_hi[nt][1]);
+                                    Elem<MT>::mma(o[dt][nt], a, pb_lo[nt][0], pb_lo[nt][1]);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int dt = 0; dt < D / 16; ++dt) {
+                                uint32_t a[4];
+                                const int tr = (lane & 7) + (lane >> 4) * 8;
+                                const int cc = dt * 16 + ((lane >> 3) & 1) * 8;
+                                ldsm_x4_trans(vst + swz(tr, cc), a[0], a[1], a[2], a[3]);
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    Elem<MT>::mma(o[dt][nt], a, pb_hi[nt][0], pb_hi[nt][1]);
+                                    Elem<MT>::mma(o[dt][nt], a, pb_lo[nt][0], pb_lo[nt][1]);
+                                }
                             }
                         }
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+                    if (lane == 0 && !(F8 && j < nblk)) mbar_arrive(empty0 + 8 * s);  // FP8: released after its loads
                 }
             }
             k += nblk_pad;
@@ -949,8 +1099,13 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT))
                         if (row < rows_here) {
 #pragma unroll
                             for (int dt = 0; dt < D / 16; ++dt) {
-                                co[row * D + dt * 16 + gid] = o[dt][nt][c];
-                                co[row * D + dt * 16 + gid + 8] = o[dt][nt][c + 2];
+                                if constexpr (F8) {  // permuted columns: gid*16 + 2dt and + 1
+                                    *reinterpret_cast<float2*>(co + row * D + gid * 16 + dt * 2) =
+                                        make_float2(o[dt][nt][c], o[dt][nt][c + 2]);
+                                } else {
+                                    co[row * D + dt * 16 + gid] = o[dt][nt][c];
+                                    co[row * D + dt * 16 + gid + 8] = o[dt][nt][c + 2];
+                                }
                             }
                             if (gid == 0) {
                                 comb_m[warp * 16 + row] = m[nt][c];
@@ -1125,10 +1280,10 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT))
             const int h = ui.kvh * p.group + (r - qi * p.group);
             const long long orow = (long long)(ui.seq * p.q_len + qi) * p.num_heads + h;
             if (nparts == 1) {
-                static_cast<uint16_t*>(p.out)[orow * D + e] = Elem<T>::to_bits(acc / lsum);
+                static_cast<uint16_t*>(p.out)[orow * D + e] = Elem<T>::to_bits(acc * p.v_scale / lsum);
             } else {
                 const long long prow = ((long long)(ui.slot0 + ui.part) * p.q_len + qi) * p.num_heads + h;
-                p.pacc[prow * D + e] = acc;
+                p.pacc[prow * D + e] = acc * p.v_scale;
                 if (e == 0) p.pml[prow] = make_float2(M, lsum);
             }
         }
@@ -1343,6 +1498,22 @@ int make_kv_map(CUtensorMap* map, const void* base, int dtype, int64_t num_block
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_INVALID_ARG;
 }
 
+// An FP8 pool [num_blocks, 16, Hkv, D] bytes: one box = the 16 rows (128 B) of one kv head, 128-byte swizzled.
+int make_kv_map_fp8(CUtensorMap* map, const void* base, int64_t num_blocks, int num_kv_heads, int head_dim) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return PA_ERR_CUDA;
+    const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)kBlock,
+                                (cuuint64_t)num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads * head_dim,
+                                   (cuuint64_t)kBlock * num_kv_heads * head_dim};
+    const cuuint32_t box[4] = {(cuuint32_t)head_dim, 1, (cuuint32_t)kBlock, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_INVALID_ARG;
+}
+
 template <typename T, int D>
 int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches) {
     const WsLayout w = ws_layout(a.num_seqs, a.q_len, a.num_heads, D, a.max_context_len, a.partition);
@@ -1371,8 +1542,14 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     *launches += 1;
 
     DecodeParams p;
-    if (int st = make_kv_map(&p.tmap_k, a.key_cache, a.dtype, a.num_blocks, a.num_kv_heads, D)) return st;
-    if (int st = make_kv_map(&p.tmap_v, a.value_cache, a.dtype, a.num_blocks, a.num_kv_heads, D)) return st;
+    if (a.fp8) {
+        if (D != 128) return PA_ERR_UNSUPPORTED;
+        if (int st = make_kv_map_fp8(&p.tmap_k, a.key_cache, a.num_blocks, a.num_kv_heads, D)) return st;
+        if (int st = make_kv_map_fp8(&p.tmap_v, a.value_cache, a.num_blocks, a.num_kv_heads, D)) return st;
+    } else {
+        if (int st = make_kv_map(&p.tmap_k, a.key_cache, a.dtype, a.num_blocks, a.num_kv_heads, D)) return st;
+        if (int st = make_kv_map(&p.tmap_v, a.value_cache, a.dtype, a.num_blocks, a.num_kv_heads, D)) return st;
+    }
     p.out = a.out;
     p.query = a.query;
     p.block_tables = a.block_tables;
@@ -1389,7 +1566,8 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     p.group = a.num_heads / a.num_kv_heads;
     p.rows = p.group * a.q_len;
     p.partition = a.partition;
-    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.scale_log2 = a.scale * (a.fp8 ? a.k_scale : 1.f) * 1.4426950408889634f;
+    p.v_scale = a.fp8 ? a.v_scale : 1.f;
     // Each consumer warp owns 8 (NT = 1) or 16 (NT = 2) query rows of the kv head; the row
     // tiles per kv head are rounded up to a divisor of the consumer warp count (a third
     // tile becomes a fourth, all-padding one) so that every consumer warp owns exactly one
@@ -1401,6 +1579,7 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     int rt = 0;
     if (g_decode_math == 1 && p.rows <= 8) rt = p.rows <= 1 ? 1 : p.rows <= 2 ? 2 : p.rows <= 4 ? 4 : 8;
     if (g_decode_math == 0 && p.rows == 1) rt = 1;
+    if (a.fp8) rt = 0;  // FP8 caches are read on the tensor-core path
     const int nt = p.rows <= 8 ? 1 : 2;
     const int tile_rows = 8 * nt;
     p.mtiles = (p.rows + tile_rows - 1) / tile_rows;
@@ -1410,25 +1589,30 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     p.slot_rows = std::min(tile_rows, p.rows);
 
     using KernelFn = void (*)(DecodeParams);
-    const KernelFn kfn = rt == 1   ? decode_kernel<T, D, 1, 1>
-                         : rt == 2 ? decode_kernel<T, D, 1, 2>
-                         : rt == 4 ? decode_kernel<T, D, 1, 4>
-                         : rt == 8 ? decode_kernel<T, D, 1, 8>
-                         : nt == 1 ? decode_kernel<T, D, 1, 0>
-                                   : decode_kernel<T, D, 2, 0>;
+    KernelFn kfn;
+    if constexpr (D == 128) {
+        if (a.fp8) kfn = nt == 1 ? decode_kernel<T, D, 1, 0, true> : decode_kernel<T, D, 2, 0, true>;
+    }
+    if (!a.fp8)
+        kfn = rt == 1   ? decode_kernel<T, D, 1, 1, false>
+              : rt == 2 ? decode_kernel<T, D, 1, 2, false>
+              : rt == 4 ? decode_kernel<T, D, 1, 4, false>
+              : rt == 8 ? decode_kernel<T, D, 1, 8, false>
+              : nt == 1 ? decode_kernel<T, D, 1, 0, false>
+                        : decode_kernel<T, D, 2, 0, false>;
     const void* fn = reinterpret_cast<const void*>(kfn);
-    const int ctas_target = decode_ctas_per_sm(nt, rt);
+    const int ctas_target = decode_ctas_per_sm(nt, rt, a.fp8);
     // Deepest ring that still lets ctas_target CTAs share an SM.  Its length must be a
     // multiple of block_splits: then every stage is always consumed by the same warps,
     // which wait its phases strictly in order (a waiter two phases ahead of a barrier
     // would see its parity as already complete).
     int stages = (kMaxStages / p.block_splits) * p.block_splits;
     if (stages < p.block_splits) return PA_ERR_UNSUPPORTED;
-    SmemLayout lay = smem_layout(D, stages, p.mtiles, tile_rows, p.slot_rows, rt > 0);
+    SmemLayout lay = smem_layout(D, stages, p.mtiles, tile_rows, p.slot_rows, rt > 0, a.fp8);
     const int per_sm_budget = 228 * 1024 / ctas_target - 1024;
     while (stages > p.block_splits && lay.total > per_sm_budget) {
         stages -= p.block_splits;
-        lay = smem_layout(D, stages, p.mtiles, tile_rows, p.slot_rows, rt > 0);
+        lay = smem_layout(D, stages, p.mtiles, tile_rows, p.slot_rows, rt > 0, a.fp8);
     }
     if (lay.total > dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
     p.stages = stages;
@@ -1482,6 +1666,30 @@ int launch_reshape_and_cache(const void* key, const void* value, void* key_cache
                                              static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache),
                                              reinterpret_cast<const long long*>(slot_mapping), num_tokens,
                                              row_vecs, num_slots);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    *launches += 1;
+    return PA_OK;
+}
+
+int launch_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache, void* value_cache,
+                                 const int64_t* slot_mapping, int64_t num_tokens, int row_elems, int64_t num_slots,
+                                 int dtype, float k_scale, float v_scale, cudaStream_t stream, int* launches) {
+    DeviceInfo dev;
+    if (int st = device_info(dev)) return st;
+    const int row_vecs = row_elems / 8;
+    const long long total = (long long)num_tokens * 2 * row_vecs;
+    const int grid = (int)std::max(1LL, std::min<long long>((total + 255) / 256, (long long)dev.sms * 8));
+    const auto* k = static_cast<const uint4*>(key);
+    const auto* v = static_cast<const uint4*>(value);
+    auto* kc = static_cast<uint2*>(key_cache);
+    auto* vc = static_cast<uint2*>(value_cache);
+    const auto* sm = reinterpret_cast<const long long*>(slot_mapping);
+    if (dtype == PA_BF16)
+        reshape_fp8_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(k, v, kc, vc, sm, num_tokens, row_vecs, num_slots,
+                                                                    k_scale, v_scale);
+    else
+        reshape_fp8_kernel<__half><<<grid, 256, 0, stream>>>(k, v, kc, vc, sm, num_tokens, row_vecs, num_slots,
+                                                             k_scale, v_scale);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     *launches += 1;
     return PA_OK;

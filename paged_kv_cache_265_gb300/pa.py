@@ -31,6 +31,11 @@ _c_int, _c_i64, _c_sz, _c_f, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 _SIGS = {
     "pa_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_int, _vp]),
     "pa_spec_verify": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp]),
+    "pa_reshape_and_cache_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_int,
+                                          _c_f, _c_f, _vp]),
+    "pa_decode_attention_fp8kv": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int,
+                                           _c_int, _c_int, _c_i64, _c_int, _c_f, _c_int, _c_f, _c_f, _c_int, _vp,
+                                           _c_sz, _vp]),
     "pa_copy_blocks": (_c_int, [_vp, _vp, _vp, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_int, _vp]),
     "pa_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "pa_decode_workspace_size_ex": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
@@ -161,6 +166,47 @@ def spec_verify(target_probs: torch.Tensor, draft_probs: torch.Tensor, draft_tok
                               _dev(u_sample, "u_sample"), n, k, v, _stream(stream))
     _check("pa_spec_verify", st)
     return num_accepted, out_tokens
+
+
+def reshape_and_cache_fp8(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                         value_cache: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float, v_scale: float,
+                         stream=None) -> None:
+    """Quantising append: 16-bit K/V rows [T, Hkv, d] into uint8 (FP8 E4M3) caches [NB, 16, Hkv, d]."""
+    nb, bs, hkv, d = key_cache.shape
+    if key_cache.dtype != torch.uint8 or value_cache.dtype != torch.uint8 or value_cache.shape != key_cache.shape:
+        raise ValueError("FP8 caches must be uint8 tensors of one shape")
+    if key.shape != (slot_mapping.shape[0], hkv, d) or value.shape != key.shape or slot_mapping.dtype != torch.int64:
+        raise ValueError("key/value must be [num_tokens, num_kv_heads, head_dim]; slot_mapping int64")
+    st = lib().pa_reshape_and_cache_fp8(
+        _dev(key, "key"), _dev(value, "value"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(slot_mapping, "slot_mapping"), slot_mapping.shape[0], hkv, d, bs, nb, dtype_code(key), float(k_scale),
+        float(v_scale), _stream(stream))
+    _check("pa_reshape_and_cache_fp8", st)
+
+
+def decode_attention_fp8kv(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                           value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                           scale: float, max_context_len: int, workspace: torch.Tensor, k_scale: float,
+                           v_scale: float, partition_size: int = 0, stream=None) -> torch.Tensor:
+    """Decode attention over uint8 (FP8 E4M3) caches; query/out 16-bit, [N, Hq, d] or [N, q_len, Hq, d]."""
+    if query.dim() == 3:
+        n, hq, d = query.shape
+        q_len = 1
+    else:
+        n, q_len, hq, d = query.shape
+    nb, bs, hkv, d2 = key_cache.shape
+    if key_cache.dtype != torch.uint8 or value_cache.dtype != torch.uint8 or d2 != d:
+        raise ValueError("FP8 caches must be uint8 with the query's head_dim")
+    if out.shape != query.shape or out.dtype != query.dtype:
+        raise ValueError("out must match query")
+    st = lib().pa_decode_attention_fp8kv(
+        _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(block_tables, "block_tables"), block_tables.shape[1], _dev(context_lens, "context_lens"), n, q_len, hq,
+        hkv, d, bs, nb, int(max_context_len), float(scale), dtype_code(query), float(k_scale), float(v_scale),
+        int(partition_size), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check("pa_decode_attention_fp8kv", st)
+    return out
 
 
 def workspace_size(num_seqs: int, q_len: int, num_heads: int, head_dim: int, max_context_len: int,

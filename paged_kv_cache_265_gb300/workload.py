@@ -316,16 +316,21 @@ def block_bytes(block_size: int, num_kv_heads: int, head_size: int, elem_bytes: 
     return 2 * block_size * num_kv_heads * head_size * elem_bytes
 
 
-def attention_bytes(w: Workload) -> int:
+def attention_bytes(w: Workload, kv_elem_bytes: Optional[int] = None) -> int:
     """Algorithmic HBM bytes of one decode-attention pass: each sequence's K and V rows
-    (all L_i positions, every kv head) once, plus Q read and O written once."""
+    (all L_i positions, every kv head) once, plus Q read and O written once.
+    kv_elem_bytes overrides the cache element size (1 for an FP8 cache)."""
     e = ELEM_BYTES[w.dtype]
-    kv = int(w.context_lens.astype(np.int64).sum()) * kv_bytes_per_token(1, w.num_kv_heads, w.head_dim, e)
+    kve = e if kv_elem_bytes is None else kv_elem_bytes
+    kv = int(w.context_lens.astype(np.int64).sum()) * kv_bytes_per_token(1, w.num_kv_heads, w.head_dim, kve)
     qo = 2 * w.num_seqs * w.q_len * w.num_heads * w.head_dim * e
     return kv + qo
 
 
-def append_bytes(w: Workload) -> int:
-    """Algorithmic bytes of the KV append: each new K and V row read once and written once."""
+def append_bytes(w: Workload, kv_elem_bytes: Optional[int] = None) -> int:
+    """Algorithmic bytes of the KV append: each new K and V row read once (16-bit) and written
+    once (kv_elem_bytes, default the input's)."""
     e = ELEM_BYTES[w.dtype]
-    return 2 * w.num_new_tokens * kv_bytes_per_token(1, w.num_kv_heads, w.head_dim, e)
+    kve = e if kv_elem_bytes is None else kv_elem_bytes
+    return w.num_new_tokens * (kv_bytes_per_token(1, w.num_kv_heads, w.head_dim, e) +
+                               kv_bytes_per_token(1, w.num_kv_heads, w.head_dim, kve))

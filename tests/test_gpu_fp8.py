@@ -1,0 +1,86 @@
+"""GPU parity of the FP8 (E4M3) KV cache against the oracle: the quantising append
+bit-exact over the whole pool, attention within the attention tolerance."""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_265_gb300 import pa
+from paged_kv_cache_265_gb300 import workload as W
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import gpu_helpers as G
+    import oracle
+
+K_SCALE, V_SCALE = 0.05, 0.03   # not powers of two: real rescaling on both sides
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from paged_kv_cache_265_gb300 import build
+
+    build.build()
+    pa.get_device_error(clear=True)
+    yield
+    assert pa.get_device_error(clear=True) == 0
+
+
+def fp8_pools(w: W.Workload):
+    """History quantised on the host by the oracle (NaN sentinels stay NaN bytes)."""
+    orc = oracle.load()
+    k = G.bits_to_f64(w.key_cache.ravel(), w.dtype).astype(np.float32)
+    v = G.bits_to_f64(w.value_cache.ravel(), w.dtype).astype(np.float32)
+    kc = orc.e4m3_encode(k / np.float32(K_SCALE)).reshape(w.key_cache.shape)
+    vc = orc.e4m3_encode(v / np.float32(V_SCALE)).reshape(w.value_cache.shape)
+    return kc, vc
+
+
+def run_fp8(w: W.Workload, partition: int = 0):
+    kc, vc = fp8_pools(w)
+    dk, dv = torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
+    pa.reshape_and_cache_fp8(G.to_dev(w.new_key, w.dtype), G.to_dev(w.new_value, w.dtype), dk, dv,
+                             torch.from_numpy(w.slot_mapping).cuda(), K_SCALE, V_SCALE)
+    q = G.to_dev(w.query, w.dtype)
+    out = torch.empty_like(q)
+    ws = pa.alloc_workspace(w.num_seqs, w.q_len, w.num_heads, w.head_dim, w.max_context_len, partition)
+    pa.decode_attention_fp8kv(out, q, dk, dv, torch.from_numpy(w.block_tables).cuda(),
+                              torch.from_numpy(w.context_lens).cuda(), w.scale, w.max_context_len, ws, K_SCALE,
+                              V_SCALE, partition_size=partition)
+    torch.cuda.synchronize()
+    orc = oracle.load()
+    assert orc.reshape_and_cache_fp8(w.new_key, w.new_value, kc, vc, w.slot_mapping, w.dtype, K_SCALE, V_SCALE) == 0
+    assert np.array_equal(dk.cpu().numpy(), kc) and np.array_equal(dv.cpu().numpy(), vc)
+    ref, bad = orc.decode_attention_fp8(w.query, kc, vc, w.block_tables, w.context_lens, w.scale, w.dtype,
+                                        K_SCALE, V_SCALE)
+    assert bad == 0
+    return G.to_bits(out), ref
+
+
+@pytest.mark.parametrize("cfg", [3, 2, 4])
+def test_fp8_named_workloads(cfg):
+    w = W.WORKLOADS[cfg]()
+    got, ref = run_fp8(w)
+    mabs, mrel = G.compare(got, ref, w.dtype, f"{w.name} fp8")
+    print(f"{w.name} fp8: max abs {mabs:.3e}, ulp vs rounded oracle {G.ulps_from_rounded_oracle(got, ref, w.dtype)}")
+
+
+@pytest.mark.parametrize("partition", [16, 1 << 20])
+def test_fp8_partitions_and_edges(partition):
+    w = W.make_workload("fp8edge", [1, 16, 17, 513, 1500], num_heads=16, num_kv_heads=4, head_dim=128,
+                        dtype="fp16", q_len=1, num_blocks=160, seed=41)
+    got, ref = run_fp8(w, partition)
+    G.compare(got, ref, w.dtype, f"fp8 partition {partition}")
+
+
+def test_fp8_head_dim_64_is_unsupported():
+    q = torch.empty((2, 4, 64), dtype=torch.bfloat16, device="cuda")
+    kc = torch.empty((4, 16, 4, 64), dtype=torch.uint8, device="cuda")
+    bt = torch.zeros((2, 4), dtype=torch.int32, device="cuda")
+    cl = torch.ones(2, dtype=torch.int32, device="cuda")
+    ws = pa.alloc_workspace(2, 1, 4, 64, 64)
+    with pytest.raises(pa.PaError) as e:
+        pa.decode_attention_fp8kv(torch.empty_like(q), q, kc, kc, bt, cl, 0.125, 64, ws, 1.0, 1.0)
+    assert e.value.status == 2
