@@ -43,6 +43,7 @@ WORKLOADS = {
     "shared_prefix": 4,
     "long_context": 5,
     "gqa_batch32": 6,
+    "chunked_prefill": 7,
 }
 DESCR = {
     1: "tiny_mha_d64: 4 seqs L={1,17,33,100}, MHA 4 heads, d=64, bf16, block 16, 64-block pool, 4-row append",
@@ -54,6 +55,8 @@ DESCR = {
        "65536-block pool, 256-row append",
     6: "gqa_batch32 (profiling size): 32 seqs L~U[1,4096], GQA 32q/8kv, d=128, bf16, block 16, 10000-block pool, "
        "32-row append",
+    7: "chunked_prefill_256: 16 seqs, history U[1024,4096] + 256-token chunk (256 causal query rows), GQA 32q/8kv, "
+       "d=128, bf16, block 16, 5000-block pool, 4096-row append",
 }
 L2_BYTES = 129 * 1024 * 1024
 
@@ -65,6 +68,15 @@ def peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 tensor TFLOP/s: the measured cuBLAS burst figure (a kernel timed alone)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
 
 
 def kernel_source_hash() -> str:
@@ -415,7 +427,10 @@ def run_ours(args, rank, world, local):
     peak, peak_kind = peaks()
     kern_ms = kern_ms_total / max(1, kern_n)
     achieved = attn_bytes / (kern_ms * 1e-3) / 1e9
-    traffic = ncu_traffic(args.workload)
+    traffic = ncu_traffic(args.workload) if not kv8 and args.math == "auto" else None
+    flops = W.attention_flops(w)
+    tpeak, tpeak_kind = tensor_peak()
+    compute_bound = flops / attn_bytes > tpeak * 1e12 / (peak * 1e9)   # past the ridge point
     line = {
         "metric": METRIC, "value": total_bytes / (step_ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
@@ -426,10 +441,16 @@ def run_ours(args, rank, world, local):
                    f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step vs 129 MB L2)",
                    "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
         "seq_tokens_per_s": total_tokens / (step_ms * 1e-3),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",
-                     "kernel": "decode_kernel (partition pass)", "kernel_ms": kern_ms,
-                     "traffic": traffic},
+        "roofline": ({"bound": "tensor", "achieved": flops / (kern_ms * 1e-3) / 1e12, "peak": tpeak,
+                      "unit": "TFLOP/s", "frac": flops / (kern_ms * 1e-3) / 1e12 / tpeak,
+                      "peak_source": f"{tpeak_kind} dense bf16 cuBLAS burst", "flops_per_launch": flops,
+                      "kernel": "decode_kernel (partition pass)", "kernel_ms": kern_ms, "traffic": traffic,
+                      "hbm_gbs": achieved}
+                     if compute_bound else
+                     {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                      "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",
+                      "kernel": "decode_kernel (partition pass)", "kernel_ms": kern_ms,
+                      "traffic": traffic, "tflops": flops / (kern_ms * 1e-3) / 1e12}),
         "gpu_launches": launches_per_step * args.steps,
         "roofline_steps": kern_n,
         "clocks": clocks.summary(),

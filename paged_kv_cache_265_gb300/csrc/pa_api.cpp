@@ -28,7 +28,7 @@ int check_decode(const void* out, const void* query, const void* key_cache, cons
     if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
     if (partition < 0 || partition % PA_BLOCK_SIZE != 0) return PA_ERR_INVALID_ARG;
     if (block_size != PA_BLOCK_SIZE || !supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
-    if ((num_heads / num_kv_heads) * q_len > 64) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)(num_heads / num_kv_heads) * q_len > 65536) return PA_ERR_UNSUPPORTED;
     if ((int64_t)max_context_len > (int64_t)max_blocks_per_seq * PA_BLOCK_SIZE) return PA_ERR_INVALID_ARG;
     if (num_blocks > (int64_t)INT32_MAX) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;

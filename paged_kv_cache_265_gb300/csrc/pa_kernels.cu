@@ -50,6 +50,15 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 #ifndef PA_MAX_STAGES
 #define PA_MAX_STAGES 8
 #endif
+// Query rows per work unit when a kv head has more of them than one CTA's four
+// warps hold at once; and whether such units prefer 8-row warps (more resident CTAs)
+// over 16-row warps.
+#ifndef PA_ROW_GROUP_ROWS
+#define PA_ROW_GROUP_ROWS 32
+#endif
+#ifndef PA_PREFER_NT1
+#define PA_PREFER_NT1 1
+#endif
 #ifndef PA_CTAS_PER_SM_NT1
 #define PA_CTAS_PER_SM_NT1 4  // kernels whose warps own 8 query rows
 #endif
@@ -495,7 +504,9 @@ struct alignas(128) DecodeParams {
     int num_heads;
     int num_kv_heads;
     int group;         // query heads per kv head
-    int rows;          // group * q_len query rows per work unit
+    int rows;          // query rows per work unit: min(64, group * q_len)
+    int total_rows;    // group * q_len query rows per kv head
+    int row_groups;    // ceil(total_rows / rows): units per (sequence, partition, kv head)
     int partition;     // tokens per partition (multiple of 16)
     int stages;        // ring length, a multiple of block_splits, <= kMaxStages
     int mtiles;        // ceil(rows / 16) tensor-core row tiles
@@ -506,7 +517,7 @@ struct alignas(128) DecodeParams {
 };
 
 struct UnitInfo {
-    int seq, part, len, slot0, kvh, ntok, pad0, pad1;
+    int seq, part, len, slot0, kvh, ntok, row0, nrows;  // rows row0 .. row0+nrows-1 of the kv head
 };
 
 struct SmemLayout {
@@ -676,7 +687,8 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
 
     griddep_launch_dependents();  // the merge kernel may be scheduled as CTAs retire
     griddep_wait();               // the work list (and the appended K/V) must be complete
-    const long long total_units = (long long)p.header[0] * p.num_kv_heads;
+    const int units_per_entry = p.num_kv_heads * p.row_groups;  // row groups of one kv head adjacent
+    const long long total_units = (long long)p.header[0] * units_per_entry;
 
     if (warp == kConsumerWarps) {
         // ===================== producer warp =====================
@@ -695,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
         int4 cur = make_int4(0, 0, 0, 0);
         int bids = 0;
         if (u < total_units) {
-            cur = p.units[u / p.num_kv_heads];
+            cur = p.units[u / units_per_entry];
             const int nb0 = ((min(p.partition, cur.z - cur.y * p.partition)) + kBlock - 1) / kBlock;
             if (lane < nb0)
                 bids = __ldg(p.block_tables + (long long)cur.x * p.max_blocks_per_seq +
@@ -716,7 +728,10 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                 ++ul;
                 break;
             }
-            const int kvh = (int)(u % p.num_kv_heads);
+            const int rem = (int)(u % units_per_entry);
+            const int kvh = rem / p.row_groups;
+            const int row0 = (rem - kvh * p.row_groups) * p.rows;
+            const int nrows = min(p.rows, p.total_rows - row0);
             const int seq = cur.x, part = cur.y, L = cur.z;
             const int tok0 = part * p.partition;
             const int ntok = min(p.partition, L - tok0);
@@ -736,13 +751,14 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                 ui.slot0 = cur.w;
                 ui.kvh = kvh;
                 ui.ntok = ntok;
-                ui.pad0 = ui.pad1 = 0;
+                ui.row0 = row0;
+                ui.nrows = nrows;
                 info[qb] = ui;
-                mbar_arrive_expect_tx(qfull0 + 8 * qb, p.rows * kRowBytes);
+                mbar_arrive_expect_tx(qfull0 + 8 * qb, nrows * kRowBytes);
             }
             __syncwarp();
-            for (int r = lane; r < p.rows; r += 32) {
-                const int qi = r / p.group, hg = r - qi * p.group;
+            for (int r = lane; r < nrows; r += 32) {
+                const int qi = (row0 + r) / p.group, hg = (row0 + r) - qi * p.group;
                 const T* src = static_cast<const T*>(p.query) +
                                ((long long)(seq * p.q_len + qi) * p.num_heads + kvh * p.group + hg) * D;
                 bulk_g2s(smem_addr(qbuf + qb * lay.q_half_bytes + r * qpitch), src, kRowBytes, qfull0 + 8 * qb,
@@ -794,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                     }
                     if (c == 0 && jj == next_at) {
                         un = __shfl_sync(0xffffffffu, un_req, 0);
-                        if (un < total_units) nxt = p.units[un / p.num_kv_heads];
+                        if (un < total_units) nxt = p.units[un / units_per_entry];
                     }
                     if (c == 0 && jj == prefetch_at && un < total_units) {
                         const int nb1 = (min(p.partition, nxt.z - nxt.y * p.partition) + kBlock - 1) / kBlock;
@@ -850,7 +866,6 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
     const int mt = warp / p.block_splits;   // row tile of this warp
     const int bsg = warp % p.block_splits;  // which of the tile's block-split warps
     const int gid = lane >> 2, tig = lane & 3;
-    const int rows_here = min(TR, p.rows - mt * TR);  // <= 0 for an all-padding tile
     uint32_t k = 0;
     int ul = 0;
     for (;; ++ul) {
@@ -859,6 +874,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
         bool ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8 * qb, (ul >> 1) & 1, &g_pa_error, abort_flag));
         const UnitInfo ui = info[qb];
         const bool done = ok && ui.seq < 0;  // end marker: no unit follows
+        const int rows_here = min(TR, ui.nrows - mt * TR);  // <= 0 for an all-padding tile
         if constexpr (RT == 0) {
             uint32_t qf[NT][D / 16][2];      // Q^T as the B operand: Q[row][d 2t..2t+1], Q[row][d 2t+8..2t+9]
             float m[NT][2], l[NT][2];        // running max (log2 units) and sum for rows 2t, 2t+1 of each group
@@ -920,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
-                        const int r = mt * TR + nt * 8 + 2 * tig + c;
+                        const int r = ui.row0 + mt * TR + nt * 8 + 2 * tig + c;
                         lim[nt][c] = ui.len - p.q_len + min(r / p.group, p.q_len - 1) - tok0;
                     }
                 // Units start at a stage counter divisible by block_splits (the producer pads
@@ -1026,7 +1042,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                                 const float x0 = pr[nt][2 * h], x1 = pr[nt][2 * h + 1];
                                 const float h0 = Elem<MT>::round_trip(x0), h1 = Elem<MT>::round_trip(x1);
                                 pb_hi[nt][h] = movmatrix_trans(Elem<MT>::pack(h0, h1));
-                                pb_lo[nt][h] = movmatrix_trans(Elem<MT>::pack(x0 - h0, x1 - h1));
+                                if constexpr (!F8) pb_lo[nt][h] = movmatrix_trans(Elem<MT>::pack(x0 - h0, x1 - h1));
                             }
                         if constexpr (F8) {
                             // Output columns are permuted inside each 16-column tile: tile dt's rows
@@ -1055,10 +1071,8 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                                 const uint32_t a[4] = {e4m3x2_to_f16x2(p01 & 0xffff), e4m3x2_to_f16x2(p01 >> 16),
                                                        e4m3x2_to_f16x2(p89 & 0xffff), e4m3x2_to_f16x2(p89 >> 16)};
 #pragma unroll
-                                for (int nt = 0; nt < NT; ++nt) {
+                                for (int nt = 0; nt < NT; ++nt)  // E4M3 V has 4 significant bits: fp16 P suffices
                                     Elem<MT>::mma(o[dt][nt], a, pb_hi[nt][0], pb_hi[nt][1]);
-                                    Elem<MT>::mma(o[dt][nt], a, pb_lo[nt][0], pb_lo[nt][1]);
-                                }
                             }
                         } else {
 #pragma unroll
@@ -1142,7 +1156,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                 if (lane == 0) mbar_arrive(qempty0 + 8 * qb);
                 nblk = (ui.ntok + kBlock - 1) / kBlock;
                 nblk_pad = ((nblk + p.block_splits - 1) / p.block_splits) * p.block_splits;
-                const int lim_r = ui.len - p.q_len + min(rr / p.group, p.q_len - 1) - ui.part * p.partition;
+                const int lim_r = ui.len - p.q_len + min((ui.row0 + rr) / p.group, p.q_len - 1) - ui.part * p.partition;
                 for (int j = bsg; j < nblk_pad; j += p.block_splits) {
                     const uint32_t kj = k + j;
                     const int s = (int)(kj % stages);
@@ -1262,7 +1276,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
         // Merge the block-split warps of each row tile; write the output or the partial.
         const int nparts = (ui.len + p.partition - 1) / p.partition;
         const int nthreads = kConsumerWarps * 32;
-        for (int idx = threadIdx.x; idx < p.rows * D; idx += nthreads) {
+        for (int idx = threadIdx.x; idx < ui.nrows * D; idx += nthreads) {
             const int r = idx / D, e = idx - r * D;
             const int tile = r / TR, rr = r - tile * TR;
             float M = -INFINITY;
@@ -1276,8 +1290,8 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                     acc += comb_o[(w * p.slot_rows + rr) * D + e] * f;
                 }
             }
-            const int qi = r / p.group;
-            const int h = ui.kvh * p.group + (r - qi * p.group);
+            const int qi = (ui.row0 + r) / p.group;
+            const int h = ui.kvh * p.group + (ui.row0 + r - qi * p.group);
             const long long orow = (long long)(ui.seq * p.q_len + qi) * p.num_heads + h;
             if (nparts == 1) {
                 static_cast<uint16_t*>(p.out)[orow * D + e] = Elem<T>::to_bits(acc * p.v_scale / lsum);
@@ -1564,7 +1578,10 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     p.num_heads = a.num_heads;
     p.num_kv_heads = a.num_kv_heads;
     p.group = a.num_heads / a.num_kv_heads;
-    p.rows = p.group * a.q_len;
+    p.total_rows = p.group * a.q_len;
+    // More than 64 query rows per kv head (a prefill chunk): units take 64-row groups.
+    p.rows = std::min(PA_ROW_GROUP_ROWS, p.total_rows);
+    p.row_groups = (p.total_rows + p.rows - 1) / p.rows;
     p.partition = a.partition;
     p.scale_log2 = a.scale * (a.fp8 ? a.k_scale : 1.f) * 1.4426950408889634f;
     p.v_scale = a.fp8 ? a.v_scale : 1.f;
@@ -1580,7 +1597,7 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     if (g_decode_math == 1 && p.rows <= 8) rt = p.rows <= 1 ? 1 : p.rows <= 2 ? 2 : p.rows <= 4 ? 4 : 8;
     if (g_decode_math == 0 && p.rows == 1) rt = 1;
     if (a.fp8) rt = 0;  // FP8 caches are read on the tensor-core path
-    const int nt = p.rows <= 8 ? 1 : 2;
+    const int nt = (p.rows <= 8 || (PA_PREFER_NT1 && p.rows <= 32)) ? 1 : 2;
     const int tile_rows = 8 * nt;
     p.mtiles = (p.rows + tile_rows - 1) / tile_rows;
     if (p.mtiles == 3) p.mtiles = 4;
@@ -1618,7 +1635,7 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     p.stages = stages;
     int per_sm = 1;
     if (int st = decode_blocks_per_sm(fn, lay.total, per_sm)) return st;
-    const long long max_units = (long long)a.num_seqs * w.pmax * a.num_kv_heads;
+    const long long max_units = (long long)a.num_seqs * w.pmax * a.num_kv_heads * p.row_groups;
     const int grid = (int)std::max(1LL, std::min<long long>((long long)dev.sms * per_sm, max_units));
 
     const bool prof = g_prof.on && g_prof.n < 4096;

@@ -257,6 +257,15 @@ def gqa_batch32(**kw) -> Workload:
                          dtype="bf16", q_len=1, num_blocks=10000, seed=2663, max_blocks_per_seq=256, **kw)
 
 
+def chunked_prefill(**kw) -> Workload:
+    """Chunked prefill over the paged cache: 16 sequences, each with U[1024, 4096] tokens of
+    history and a 256-token prompt chunk (256 query rows, causal inside the chunk, appended
+    first); GQA 32q/8kv, d = 128, bf16, 5000-block pool."""
+    hist = _uniform_lens(2666, 16, 1024, 4096)
+    return make_workload("chunked_prefill_256", hist + 256, num_heads=32, num_kv_heads=8, head_dim=128,
+                         dtype="bf16", q_len=256, num_blocks=5000, seed=2666, max_blocks_per_seq=272, **kw)
+
+
 WORKLOADS = {
     1: tiny_mha,
     2: opt13b_mha,
@@ -264,6 +273,7 @@ WORKLOADS = {
     4: shared_prefix_verify,
     5: long_context_skewed,
     6: gqa_batch32,
+    7: chunked_prefill,
 }
 
 
@@ -325,6 +335,16 @@ def attention_bytes(w: Workload, kv_elem_bytes: Optional[int] = None) -> int:
     kv = int(w.context_lens.astype(np.int64).sum()) * kv_bytes_per_token(1, w.num_kv_heads, w.head_dim, kve)
     qo = 2 * w.num_seqs * w.q_len * w.num_heads * w.head_dim * e
     return kv + qo
+
+
+def attention_flops(w: Workload) -> int:
+    """Algorithmic flops of one attention pass: for every query row and head, 2 d flops for the
+    score and 2 d for the P.V term of each position the row attends (row j of a q-row chunk
+    attends L - q + j + 1 positions)."""
+    lens = w.context_lens.astype(np.int64)
+    q = w.q_len
+    visible = int((q * (lens - q) + q * (q + 1) // 2).sum())
+    return 4 * w.head_dim * w.num_heads * visible
 
 
 def append_bytes(w: Workload, kv_elem_bytes: Optional[int] = None) -> int:

@@ -114,11 +114,12 @@ def pin_sdpa_random_small(orc):
         dict(lens=[5, 23, 40], hq=8, hkv=2, d=64, q=3, dtype="bf16", shared=0),
         dict(lens=[33, 40, 34, 48], hq=4, hkv=1, d=8, q=5, dtype="fp16", shared=2),
         dict(lens=[3, 31, 32, 39], hq=4, hkv=4, d=64, q=3, dtype="fp16", shared=0),
+        dict(lens=[64, 100, 130], hq=4, hkv=2, d=8, q=64, dtype="bf16", shared=0),   # a prefill chunk
     ]
     for c_i, c in enumerate(cases):
         w = W.make_workload(f"pin{c_i}", c["lens"], num_heads=c["hq"], num_kv_heads=c["hkv"],
                             head_dim=c["d"], dtype=c["dtype"], q_len=c["q"], append_len=0,
-                            num_blocks=40, seed=100 + c_i, shared_prefix_blocks=c["shared"],
+                            num_blocks=48, seed=100 + c_i, shared_prefix_blocks=c["shared"],
                             keep_logical=True)
         got = _run(orc, w)
         ref = _sdpa_reference(w)

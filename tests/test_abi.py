@@ -64,7 +64,7 @@ def test_decode_host_validation(lib):
     assert _decode(lib, query=FAKE + 8) == 1            # misaligned
     assert _decode(lib, d=96) == 2                      # head_dim not compiled
     assert _decode(lib, bs=32) == 2                     # block size other than 16
-    assert _decode(lib, hq=64, hkv=1, q_len=2) == 2     # 128 rows per kv head
+    assert _decode(lib, hq=64, hkv=1, q_len=2000, max_ctx=128) == 2   # 128,000 rows per kv head
     assert _decode(lib, ws=None) == 3
     assert _decode(lib, ws_bytes=16) == 3
 

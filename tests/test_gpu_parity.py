@@ -76,6 +76,8 @@ EDGE = [
     ([9, 64, 999], 32, 4, 128, 3, "bf16"),                  # 24 rows: two row tiles
     ([12, 300, 1600], 8, 1, 64, 8, "bf16"),                 # 64 rows: four row tiles
     ([5, 77, 1300], 16, 2, 128, 5, "bf16"),                 # 40 rows: three row tiles (+1 padding tile)
+    ([64, 300, 700, 1500], 32, 8, 128, 64, "bf16"),         # prefill chunk: 256 rows, four 64-row groups
+    ([200, 513, 1100], 8, 8, 128, 200, "fp16"),             # 200 rows: groups of 64, 64, 64, 8
 ]
 
 
@@ -247,4 +249,13 @@ def test_tensor_path_on_single_row_heads(cfg):
         pa.set_decode_math("auto")
     _, _, ref = G.oracle_step(w)
     G.compare(got, ref, w.dtype, f"{w.name} (tensor-core path)")
+    assert G.ulps_from_rounded_oracle(got, ref, w.dtype) <= 1
+
+
+def test_chunked_prefill_workload():
+    """Chunked prefill: 16 sequences, a 256-token chunk each over up to 4096 tokens of history."""
+    w = W.chunked_prefill()
+    got = G.GpuStep(w).run()
+    kc, vc, ref = G.oracle_step(w)
+    G.compare(got, ref, w.dtype, w.name)
     assert G.ulps_from_rounded_oracle(got, ref, w.dtype) <= 1
