@@ -79,10 +79,15 @@ def tensor_peak():
     return 1900.0, "fallback"
 
 
+# Sources that define the decode partition kernel and its launch: a change to any of them
+# invalidates DRAM counters taken earlier.
+DECODE_SOURCES = ("pa_device.cuh", "pa_internal.h", "pa_kernels.cu")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_265_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in DECODE_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())

@@ -261,11 +261,11 @@ int pa_decode_attention_noalloc(void* out, const void* query, const void* key_ca
  * uint8 [num_blocks, 16, num_kv_heads, head_dim].  Scales must be finite and > 0.
  *
  * pa_decode_attention_fp8kv: as pa_decode_attention_ex over FP8 caches (query and
- * out stay 16-bit, of dtype).  K and V are widened exactly to fp16 in shared
- * memory; the score and P.V products run on the tensor cores in fp16 with fp32
- * accumulation (a bf16 query is rounded to fp16 for them), k_scale folds into the
- * softmax scale and v_scale into the output.  head_dim 128 only; the workspace is
- * sized as for pa_decode_attention_ex.
+ * out stay 16-bit, of dtype).  K and V bytes are widened exactly to fp16 in
+ * registers; the score and P.V products run on the tensor cores in fp16 with fp32
+ * accumulation (a bf16 query and the softmax weights P are rounded to fp16 for
+ * them), k_scale folds into the softmax scale and v_scale into the output.
+ * head_dim 128 only; the workspace is sized as for pa_decode_attention_ex.
  */
 int pa_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache, void* value_cache,
                              const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads, int head_dim,
