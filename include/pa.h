@@ -191,6 +191,15 @@ int pa_decode_attention(void* out, const void* query, const void* key_cache, con
  * positions 0 .. L - q_len + j.
  *   out, query [num_seqs, q_len, num_heads, head_dim]
  * Everything else as pa_decode_attention; each context_lens[i] must be >= q_len.
+ *
+ * Prefill chunks ("现代 LLM 推理引擎剖析", section 2.1 Chunked Prefill: a long
+ * prompt runs in chunks, each attending to the cache its earlier chunks
+ * filled) are this same call with q_len = the chunk length.  When a kv head has
+ * at least 128 query rows (num_heads / num_kv_heads * q_len) and the library
+ * chooses the split (partition size 0), the call runs as one tcgen05 kernel:
+ * 128-row query tiles, S and O accumulated in tensor memory, the softmax weights
+ * rounded once to the input type for the P.V product, no split of the context.
+ * The workspace is then not used.
  */
 int pa_decode_attention_multiquery(void* out, const void* query, const void* key_cache,
                                    const void* value_cache, const int32_t* block_tables,
@@ -294,9 +303,14 @@ int pa_get_device_error(int32_t* host_flags, int clear, void* stream);
  *      reductions when each kv head has one query row (MHA, single token);
  *      tensor-core tiles (mma.sync m16n8k16, fp32 accumulation) for grouped
  *      heads and multi-query chunks, where they stream faster;
+ *      with 128 or more query rows per kv head and the default partition, the
+ *      tcgen05 prefill kernel (see pa_decode_attention_multiquery);
  *   1: CUDA-core FMA wherever a kv head has at most 8 query rows;
- *   2: tensor-core tiles everywhere.
- * All give results within fp32 rounding of each other.  Returns
+ *   2: mma.sync tensor-core tiles everywhere;
+ *   3: the tcgen05 prefill kernel for every call over 16-bit caches, whatever
+ *      the row count and partition size (FP8 caches keep their own path).
+ * All agree with the fp64 definition within the output type's rounding plus
+ * fp32 accumulation (the tcgen05 kernel also rounds P once).  Returns
  * PA_ERR_INVALID_ARG for other values.  Not thread safe: set it before
  * launching work.
  */

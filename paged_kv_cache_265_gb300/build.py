@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa.so")
 
-SOURCES = ["pa_kernels.cu", "pa_api.cpp"]
+SOURCES = ["pa_kernels.cu", "pa_prefill.cu", "pa_api.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O3", "-I", os.path.join(ROOT, "include"),
           "--expt-relaxed-constexpr"]

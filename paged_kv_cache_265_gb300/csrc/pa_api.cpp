@@ -161,6 +161,7 @@ int pa_decode_attention_ex(void* out, const void* query, const void* key_cache, 
     a.scale = scale;
     a.dtype = dtype;
     a.partition = partition;
+    a.partition_auto = partition_size == 0;
     a.workspace = workspace;
     int launches = 0;
     const int rc = pa::launch_decode(a, static_cast<cudaStream_t>(stream), &launches);

@@ -2,9 +2,12 @@
 // kernel launchers (pa_kernels.cu).  Not installed; not part of the ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
+
+#include <utility>
 
 namespace pa {
 
@@ -72,6 +75,7 @@ struct DecodeArgs {
     bool fp8 = false;     // key/value caches hold FP8 E4M3 bytes
     float k_scale = 1.f;  // their dequantisation scales
     float v_scale = 1.f;
+    bool partition_auto = false;  // the caller passed partition size 0 (the library chooses)
 };
 
 // Launchers: return a pa_status; `launches` receives the number of kernels enqueued.
@@ -79,6 +83,8 @@ int launch_reshape_and_cache(const void* key, const void* value, void* key_cache
                              const int64_t* slot_mapping, int64_t num_tokens, int row_bytes,
                              int64_t num_slots, cudaStream_t stream, int* launches);
 int launch_decode(const DecodeArgs& a, cudaStream_t stream, int* launches);
+// Chunked-prefill attention on tcgen05 (pa_prefill.cu); launch_decode routes calls to it.
+int launch_prefill_tc(const DecodeArgs& a, cudaStream_t stream, int* launches);
 int launch_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* target_probs,
                        const float* draft_probs, const int32_t* draft_tokens, const float* u_accept,
                        const float* u_sample, int num_seqs, int k, int vocab, cudaStream_t stream, int* launches);
@@ -93,11 +99,41 @@ int read_device_error(int32_t* flags, int clear, cudaStream_t stream);
 // (looked up on the first call per device, then cached).
 int noalloc_workspace(void** ptr);
 
-// Consumer arithmetic of the partition kernel: 0 auto, 1 CUDA-core FMA, 2 tensor cores.
+// Consumer arithmetic: 0 auto, 1 CUDA-core FMA, 2 mma.sync tensor-core tiles, 3 tcgen05 prefill kernel.
 int set_decode_math(int math);
 
 // Benchmark timing hook around the main decode kernel.
 int profile_enable(int on);
 int profile_read(float* total_ms, int* launches);
+// Inside a launcher: records the start event if timing is on (then profile_end after the launch).
+bool profile_begin(cudaStream_t stream);
+void profile_end(cudaStream_t stream);
+
+// Tensor map of a 16-bit pool [num_blocks, 16, Hkv, head_dim]: one box = 64 elements of one
+// kv head for the 16 positions of one block, 128-byte swizzled.
+int kv_tensor_map(CUtensorMap* map, const void* base, int dtype, int64_t num_blocks, int num_kv_heads,
+                  int head_dim);
+// Device address of the library's error word (PA_DEVERR_* bits) on the current device.
+int device_error_word(int** ptr);
+// Raises a kernel's dynamic shared-memory limit to `smem` bytes if it is lower.
+int ensure_dynamic_smem(const void* fn, int smem);
+
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// before its predecessor finishes; it orders itself with griddep_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace pa

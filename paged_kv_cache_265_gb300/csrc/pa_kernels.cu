@@ -59,6 +59,10 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 #ifndef PA_PREFER_NT1
 #define PA_PREFER_NT1 1
 #endif
+// Query rows per kv head from which the auto mode runs a call on the tcgen05 prefill kernel.
+#ifndef PA_TC_MIN_ROWS
+#define PA_TC_MIN_ROWS 128
+#endif
 #ifndef PA_CTAS_PER_SM_NT1
 #define PA_CTAS_PER_SM_NT1 4  // kernels whose warps own 8 query rows
 #endif
@@ -1447,7 +1451,9 @@ int decode_blocks_per_sm(const void* fn, int smem, int& blocks) {
     return PA_OK;
 }
 
-int g_decode_math = 0;  // 0: auto, 1: CUDA-core FMA (up to 8 rows per kv head), 2: tensor-core tiles
+// 0: auto, 1: CUDA-core FMA (up to 8 rows per kv head), 2: mma.sync tensor-core tiles,
+// 3: the tcgen05 prefill kernel for every call over 16-bit caches
+int g_decode_math = 0;
 
 struct Profile {
     bool on = false;
@@ -1456,24 +1462,6 @@ struct Profile {
     cudaEvent_t ev[2 * 4096] = {};
     bool created = false;
 } g_prof;
-
-// Launch with programmatic stream serialisation: the kernel may be scheduled
-// before its predecessor finishes; it orders itself with griddep_wait().
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       Args&&... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
 
 // cuTensorMapEncodeTiled, fetched from the driver at first use (no link-time libcuda dependency).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1670,6 +1658,55 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Pieces shared with the other kernel translation units (pa_internal.h).
+// ---------------------------------------------------------------------------
+int kv_tensor_map(CUtensorMap* map, const void* base, int dtype, int64_t num_blocks, int num_kv_heads,
+                  int head_dim) {
+    return make_kv_map(map, base, dtype, num_blocks, num_kv_heads, head_dim);
+}
+
+int device_error_word(int** ptr) {
+    static int* cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!cached[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pa_error) != cudaSuccess || !p) return PA_ERR_CUDA;
+        cached[dev] = static_cast<int*>(p);
+    }
+    *ptr = cached[dev];
+    return PA_OK;
+}
+
+int ensure_dynamic_smem(const void* fn, int smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    DeviceInfo d;
+    if (int st = device_info(d)) return st;
+    if (smem > d.max_smem_optin) return PA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return PA_ERR_CUDA;
+    // Raised to what this call needs and never lowered.
+    if (fa.maxDynamicSharedSizeBytes < smem &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+bool profile_begin(cudaStream_t stream) {
+    const bool prof = g_prof.on && g_prof.n < 4096;
+    if (prof) cudaEventRecord(g_prof.ev[2 * g_prof.n], stream);
+    return prof;
+}
+
+void profile_end(cudaStream_t stream) {
+    cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], stream);
+    g_prof.n++;
+}
+
 int launch_reshape_and_cache(const void* key, const void* value, void* key_cache, void* value_cache,
                              const int64_t* slot_mapping, int64_t num_tokens, int row_bytes,
                              int64_t num_slots, cudaStream_t stream, int* launches) {
@@ -1747,7 +1784,18 @@ int launch_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* 
     return PA_OK;
 }
 
+// Prefill chunks (many query rows per kv head) run on the tcgen05 kernel: in auto mode
+// when a kv head has at least PA_TC_MIN_ROWS query rows and the caller left the split to
+// the library, and always in tcgen05 mode (16-bit caches).
+bool use_prefill_tc(const DecodeArgs& a) {
+    if (a.fp8) return false;
+    if (g_decode_math == 3) return true;
+    const long long rows = (long long)(a.num_heads / a.num_kv_heads) * a.q_len;
+    return g_decode_math == 0 && a.partition_auto && rows >= PA_TC_MIN_ROWS;
+}
+
 int launch_decode(const DecodeArgs& a, cudaStream_t stream, int* launches) {
+    if (use_prefill_tc(a)) return launch_prefill_tc(a, stream, launches);
     if (a.dtype == PA_BF16) {
         if (a.head_dim == 128) return launch_decode_typed<__nv_bfloat16, 128>(a, stream, launches);
         if (a.head_dim == 64) return launch_decode_typed<__nv_bfloat16, 64>(a, stream, launches);
@@ -1774,7 +1822,7 @@ int read_device_error(int32_t* flags, int clear, cudaStream_t stream) {
 }
 
 int set_decode_math(int math) {
-    if (math < 0 || math > 2) return PA_ERR_INVALID_ARG;
+    if (math < 0 || math > 3) return PA_ERR_INVALID_ARG;
     g_decode_math = math;
     return PA_OK;
 }

@@ -1,0 +1,448 @@
+// pa_prefill.cu -- attention of prefill chunks over the paged KV cache on the
+// fifth-generation tensor cores: tcgen05.mma with its accumulators in tensor
+// memory (TMEM), K/V blocks staged in shared memory by tensor-map TMA.
+//
+// It computes exactly what the multi-query decode path computes: the q_len
+// chunk tokens are the last q_len positions of each sequence, and query row j
+// sees positions 0 .. L - q_len + j ("现代 LLM 推理引擎剖析", section 2.1 Chunked
+// Prefill: a long prompt is run in chunks, each attending to the cache its
+// earlier chunks filled; the attention is the dense causal definition of "LLM
+// 推理优化的系统视角", section 3.1, with the query-head grouping of its section
+// 3.2).  A chunk has g * q_len query rows per kv head, enough to fill 128-row
+// tensor-core tiles, so the context is not split.
+//
+// One CTA = one tile of 128 query rows of one kv head.  Rows are token-major
+// (row r of a kv head is chunk token r / g, query head kvh * g + r % g), so a
+// tile spans 128 / g consecutive chunk tokens whose causal limits are close.
+// For each K/V tile of 128 positions (8 pool blocks):
+//   S = Q K^T    M = 128, N = 16 x blocks, K = D: A = Q, B = K tile, both
+//                K-major and 128-byte swizzled; S (fp32) in TMEM columns 0-127
+//   softmax      warps 0-3, thread i = TMEM lane i = tile row i: one tcgen05.ld
+//                of the row, masking, log2-unit scaling, ex2.approx against a
+//                running max that is raised only when it grows by more than 8
+//                (weights stay <= 2^8; the final division uses the same max,
+//                so only rounding changes); each weight p is split into
+//                p_hi = p rounded to the input type and p_lo = (p - p_hi)
+//                rounded, both stored as A operands (about 16 significant bits
+//                of p reach the product; one 16-bit P alone misses the
+//                attention tolerance when a few positions dominate)
+//   O += P V     M = 128, N = D, K = 16 x blocks, once with P_hi and once with
+//                P_lo: B = V tile (MN-major: d is contiguous in the cache); O
+//                (fp32) in TMEM columns 128 .. 128 + D - 1
+// The S product of tile j + 1 is issued as soon as the softmax warps have
+// copied S_j out of TMEM, so it runs under their exponentials, and P_j V_j runs
+// while they start on tile j + 1.
+//
+// Warps: 0-3 softmax and epilogue, 4 TMA producer (K/V blocks found through the
+// block table, two stages of one K/V tile), 5 TMEM owner and MMA issuer (one
+// thread).  Every wait is bounded (PA_DEVERR_TIMEOUT); a failed wait stops all
+// roles, and the CTA lets its copies and products finish before it frees TMEM.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <type_traits>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kTcRows = 128;             // query rows per CTA tile (MMA M)
+constexpr int kTcPos = 128;              // positions per K/V tile
+constexpr int kTcBlocks = kTcPos / 16;   // pool blocks per K/V tile
+constexpr int kTcStages = 2;             // K/V tiles in flight
+constexpr int kTcThreads = 192;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemS = 0;           // S columns
+constexpr uint32_t kTmemO = 128;         // O columns
+constexpr int kRegion = kTcRows * 128;   // 128 rows x 128 B: one 64-element column block
+constexpr int kBox = 16 * 128;           // one TMA box: 16 positions x 64 elements
+
+struct PrefillTcParams {
+    CUtensorMap tmap_k;  // 64-byte aligned members first
+    CUtensorMap tmap_v;
+    void* out;
+    const void* query;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    int* err;
+    int max_blocks_per_seq;
+    int num_blocks;
+    int q_len;
+    int num_heads;
+    int num_kv_heads;
+    int group;       // query heads per kv head
+    int total_rows;  // group * q_len query rows per kv head
+    int mtiles;      // 128-row tiles per kv head
+    int max_context_len;
+    float scale_log2;
+};
+
+template <int D>
+struct TcLayout {
+    static constexpr int kHalves = D / 64;                 // 64-element column blocks of d
+    static constexpr int kQ = 0;                           // Q tile, K-major
+    static constexpr int kP = kQ + kHalves * kRegion;      // P_hi tile, K-major (2 blocks of 64 positions)
+    static constexpr int kPlo = kP + 2 * kRegion;          // P_lo tile, same layout
+    static constexpr int kStage0 = kPlo + 2 * kRegion;     // stages: K tile then V tile
+    static constexpr int kKBytes = kHalves * kRegion;
+    static constexpr int kStageBytes = 2 * kKBytes;
+    static constexpr int kBars = kStage0 + kTcStages * kStageBytes;
+    // barriers: kvfull[2] +0, kvempty[2] +16, sfull +32, sfree +40, pfull +48,
+    // odone +56, drain +64, qready +72; TMEM base +80; abort flag +84
+    static constexpr int kTotal = kBars + 128;
+    static constexpr int kAlloc = kTotal + 1024;           // slack to align the base to 1024 B
+};
+
+__device__ __forceinline__ float lo16(uint32_t v, std::true_type /*bf16*/) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float hi16(uint32_t v, std::true_type) { return __uint_as_float(v & 0xffff0000u); }
+__device__ __forceinline__ float lo16(uint32_t v, std::false_type /*fp16*/) {
+    return __half2float(__ushort_as_half((unsigned short)(v & 0xffffu)));
+}
+__device__ __forceinline__ float hi16(uint32_t v, std::false_type) {
+    return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
+    using Lay = TcLayout<D>;
+    using IsBf16 = std::integral_constant<bool, std::is_same<T, __nv_bfloat16>::value>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t q_s = sbase + Lay::kQ, p_s = sbase + Lay::kP, plo_s = sbase + Lay::kPlo,
+                   st_s = sbase + Lay::kStage0;
+    const uint32_t bars = sbase + Lay::kBars;
+    const uint32_t kvfull = bars, kvempty = bars + 16, sfull = bars + 32, sfree = bars + 40, pfull = bars + 48,
+                   odone = bars + 56, drain = bars + 64, qready = bars + 72;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Lay::kBars + 80);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kBars + 84);
+    int* err = p.err;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Tiles of one (sequence, kv head) are adjacent and share its K/V in L2; the
+    // last rows (the longest causal ranges) go first.
+    const int idx = blockIdx.x;
+    const int mt = p.mtiles - 1 - idx % p.mtiles;
+    const int kvh = (idx / p.mtiles) % p.num_kv_heads;
+    const int seq = idx / (p.mtiles * p.num_kv_heads);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(kvfull + 8 * s, 1);
+            mbar_init(kvempty + 8 * s, 1);
+        }
+        mbar_init(sfull, 1);
+        mbar_init(sfree, kTcRows);
+        mbar_init(pfull, kTcRows);
+        mbar_init(odone, 1);
+        mbar_init(drain, 1);
+        mbar_init(qready, kTcRows);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        tc::alloc(bars + 80, kTmemCols);
+        tc::relinquish_alloc_permit();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    griddep_launch_dependents();
+    griddep_wait();  // the appended K/V rows and the query come from earlier kernels
+
+    const int L = p.context_lens[seq];
+    const bool valid = L >= p.q_len && L <= p.max_context_len && L <= p.max_blocks_per_seq * 16;
+    if (!valid && threadIdx.x == 0) atomicOr(err, PA_DEVERR_CONTEXT);  // rows left untouched
+    const int row0 = mt * kTcRows;
+    const int t_first = row0 / p.group;
+    const int t_last = min((row0 + kTcRows - 1) / p.group, p.q_len - 1);
+    const int nblk = valid ? (L - p.q_len + t_last) / 16 + 1 : 0;  // blocks this tile sees
+    const int ntiles = (nblk + kTcBlocks - 1) / kTcBlocks;
+    const int lastblk = (L - 1) / 16;           // the sequence's last block ...
+    const int sh = 16 * (lastblk + 1) - L;      // ... is short by sh rows, fetched as leading zeros
+
+    if (valid && warp == 4) {
+        // ===================== TMA producer =====================
+        const int* bt = p.block_tables + (long long)seq * p.max_blocks_per_seq;
+        int armed[kTcStages] = {0, 0};
+        for (int j = 0; j < ntiles; ++j) {
+            const int s = j & 1;
+            if (j >= kTcStages) {
+                bool w = true;
+                if (lane == 0) w = mbar_wait(kvempty + 8 * s, ((j >> 1) - 1) & 1, err, abort_flag);
+                if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
+            }
+            const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
+            int bid = 0;
+            bool good = false;
+            if (lane < nb) {
+                bid = __ldg(bt + kTcBlocks * j + lane);
+                good = bid >= 0 && bid < p.num_blocks;
+                if (!good) atomicOr(err, PA_DEVERR_BLOCK_ID);  // skipped: the tile computes on stale data
+            }
+            const unsigned gm = __ballot_sync(0xffffffffu, good);
+            const uint32_t bar = kvfull + 8 * s;
+            if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(gm) * 2u * Lay::kHalves * kBox);
+            __syncwarp();
+            if (good) {
+                const int y0 = (kTcBlocks * j + lane == lastblk) ? -sh : 0;  // rows before 0 arrive as zeros
+                const uint32_t kdst = st_s + s * Lay::kStageBytes + lane * kBox;
+#pragma unroll
+                for (int h = 0; h < Lay::kHalves; ++h) {
+                    tc::tma_load_4d(kdst + h * kRegion, &p.tmap_k, h * 64, kvh, y0, bid, bar);
+                    tc::tma_load_4d(kdst + Lay::kKBytes + h * kRegion, &p.tmap_v, h * 64, kvh, y0, bid, bar);
+                }
+            }
+            ++armed[s];
+        }
+        // No copy may still be landing when the CTA exits.
+        if (lane == 0)
+            for (int s = 0; s < kTcStages; ++s)
+                if (armed[s] > 0) mbar_wait(kvfull + 8 * s, (armed[s] - 1) & 1, err, nullptr);
+        __syncwarp();
+    } else if (valid && warp == 5) {
+        // ===================== MMA issuer =====================
+        if (lane == 0) {
+            constexpr bool kBf16 = IsBf16::value;
+            const uint32_t id_o = tc::idesc_f16(kBf16, true, kTcRows, D);
+            bool ok = mbar_wait(qready, 0, err, abort_flag);
+            for (int j = 0; ok && j <= ntiles; ++j) {
+                if (j < ntiles) {
+                    const int s = j & 1;
+                    ok = mbar_wait(kvfull + 8 * s, (j >> 1) & 1, err, abort_flag) &&
+                         (j == 0 || mbar_wait(sfree, (j - 1) & 1, err, abort_flag));
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
+                    const uint32_t id_s = tc::idesc_f16(kBf16, false, kTcRows, 16 * nb);
+                    const uint32_t kst = st_s + s * Lay::kStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kRegion + (kk & 3) * 32;
+                        tc::mma_f16_ss(tmem + kTmemS, tc::smem_desc_sw128(q_s + off, 16, 1024),
+                                       tc::smem_desc_sw128(kst + off, 16, 1024), id_s, kk > 0);
+                    }
+                    tc::commit(sfull);
+                }
+                if (j > 0) {
+                    const int i = j - 1, s = i & 1;
+                    ok = mbar_wait(pfull, i & 1, err, abort_flag);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    const int nb = min(kTcBlocks, nblk - kTcBlocks * i);
+                    const uint32_t vst = st_s + s * Lay::kStageBytes + Lay::kKBytes;
+                    for (int kk = 0; kk < nb; ++kk) {
+                        const uint32_t aoff = (kk >> 2) * kRegion + (kk & 3) * 32;
+                        const uint64_t vdesc = tc::smem_desc_sw128(vst + kk * 2 * 1024, kRegion, 1024);
+                        tc::mma_f16_ss(tmem + kTmemO, tc::smem_desc_sw128(p_s + aoff, 16, 1024), vdesc, id_o,
+                                       (i > 0 || kk > 0) ? 1u : 0u);
+                        tc::mma_f16_ss(tmem + kTmemO, tc::smem_desc_sw128(plo_s + aoff, 16, 1024), vdesc, id_o, 1u);
+                    }
+                    tc::commit(kvempty + 8 * s);
+                    tc::commit(odone);
+                }
+            }
+            // No product may be in flight when TMEM is freed.
+            tc::commit(drain);
+            mbar_wait(drain, 0, err, nullptr);
+        }
+        __syncwarp();
+    } else if (valid) {
+        // ===================== softmax and epilogue (warps 0-3) =====================
+        const int r = threadIdx.x;  // tile row = TMEM lane
+        const int gr = row0 + r;
+        const bool real = gr < p.total_rows;
+        const int t = real ? gr / p.group : p.q_len - 1;
+        const int hq = kvh * p.group + (real ? gr - t * p.group : 0);
+        const int lim = L - p.q_len + t;               // last position this row sees
+        const int lim_min = L - p.q_len + t_first;     // smallest limit in the tile
+        const uint32_t lane_tmem = tmem + ((uint32_t)(warp * 32) << 16);
+        const long long row_off = (((long long)seq * p.q_len + t) * p.num_heads + hq) * D;
+
+        // Q row into the K-major swizzled tile (rows past the chunk are zeros).
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.query) + row_off);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                const uint4 v = real ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                tc::st_shared_v4(q_s + (c >> 3) * kRegion + r * 128 + (((c & 7) ^ (r & 7)) << 4), v);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(qready);
+        }
+
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            if (!__all_sync(0xffffffffu, mbar_wait(sfull, j & 1, err, abort_flag))) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            uint32_t sv[128];
+            tc::ld_x128(lane_tmem + kTmemS, sv);
+            tc::fence_before_sync();
+            mbar_arrive(sfree);
+
+            const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
+            const int pos0 = kTcPos * j;
+            // Column c holds position pos0 + c, except in the sequence's short last block
+            // (columns lastc .. lastc + 15), whose first sh columns are zero rows and whose
+            // column c holds position pos0 + c - sh.
+            const bool short_here = sh > 0 && lastblk < kTcBlocks * j + nb;
+            const bool edge = nb < kTcBlocks || short_here || pos0 + kTcPos - 1 > lim_min;
+            float tmax = -INFINITY;
+            if (edge) {
+                // Visible columns: [0, hi1] and [lo2, hi2].
+                const int lastc = short_here ? 16 * (lastblk - kTcBlocks * j) : 16 * nb;
+                const int hi1 = min(min(lim - pos0, 16 * nb - 1), lastc - 1);
+                const int lo2 = short_here ? lastc + sh : 128;
+                const int hi2 = min(lim - pos0 + sh, 16 * nb - 1);
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const bool vis = c <= hi1 || (c >= lo2 && c <= hi2);
+                    const float x = vis ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
+                    sv[c] = __float_as_uint(x);
+                    tmax = fmaxf(tmax, x);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const float x = __uint_as_float(sv[c]) * p.scale_log2;
+                    sv[c] = __float_as_uint(x);
+                    tmax = fmaxf(tmax, x);
+                }
+            }
+            float alpha = 1.f;
+            const bool bump = tmax > m_run + 8.f;
+            if (bump) {
+                alpha = ex2(m_run - tmax);
+                m_run = tmax;
+            }
+            const float msub = m_run == -INFINITY ? 0.f : m_run;
+            float sum = 0.f;
+            uint32_t pk[64], pl[64];  // P_hi and P_lo, two weights per register
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float p0 = ex2(__uint_as_float(sv[2 * c]) - msub);
+                const float p1 = ex2(__uint_as_float(sv[2 * c + 1]) - msub);
+                pk[c] = Elem<T>::pack(p0, p1);
+                pl[c] = Elem<T>::pack(p0 - lo16(pk[c], IsBf16()), p1 - hi16(pk[c], IsBf16()));
+                sum += p0 + p1;
+            }
+            // P_{j-1} V_{j-1} must be done before P and O are touched.
+            if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(odone, (j - 1) & 1, err, abort_flag))) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                if (c < 2 * nb) {
+                    const uint32_t off = (c >> 3) * kRegion + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+                    tc::st_shared_v4(p_s + off, make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+                    tc::st_shared_v4(plo_s + off, make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]));
+                }
+            if (j > 0 && __any_sync(0xffffffffu, bump)) {
+#pragma unroll
+                for (int h = 0; h < D / 64; ++h) {
+                    uint32_t o[64];
+                    tc::ld_x64(lane_tmem + kTmemO + 64 * h, o);
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                    tc::st_x64(lane_tmem + kTmemO + 64 * h, o);
+                }
+                tc::wait_st();
+            }
+            l_run = l_run * alpha + sum;
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            mbar_arrive(pfull);
+        }
+
+        // Epilogue: O / l, rounded once, to out[seq, t, hq, :].
+        if (ok && __all_sync(0xffffffffu, mbar_wait(odone, (ntiles - 1) & 1, err, abort_flag))) {
+            tc::fence_after_sync();
+            const float inv = 1.f / l_run;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row_off);
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) {
+                uint32_t o[64];
+                tc::ld_x64(lane_tmem + kTmemO + 64 * h, o);
+                if (real) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint4 v;
+                        v.x = Elem<T>::pack(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
+                        v.y = Elem<T>::pack(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
+                        v.z = Elem<T>::pack(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
+                        v.w = Elem<T>::pack(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
+                        dst[h * 8 + c] = v;
+                    }
+                }
+            }
+        }
+    }
+
+    // Teardown: every TMEM access and product is complete; free TMEM.
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 5) {
+        tc::fence_after_sync();
+        tc::dealloc(tmem, kTmemCols);
+    }
+}
+
+template <typename T, int D>
+int launch_prefill_tc_typed(const DecodeArgs& a, cudaStream_t stream, int* launches) {
+    PrefillTcParams p;
+    if (int st = kv_tensor_map(&p.tmap_k, a.key_cache, a.dtype, a.num_blocks, a.num_kv_heads, D)) return st;
+    if (int st = kv_tensor_map(&p.tmap_v, a.value_cache, a.dtype, a.num_blocks, a.num_kv_heads, D)) return st;
+    p.out = a.out;
+    p.query = a.query;
+    p.block_tables = a.block_tables;
+    p.context_lens = a.context_lens;
+    if (int st = device_error_word(&p.err)) return st;
+    p.max_blocks_per_seq = a.max_blocks_per_seq;
+    p.num_blocks = (int)a.num_blocks;
+    p.q_len = a.q_len;
+    p.num_heads = a.num_heads;
+    p.num_kv_heads = a.num_kv_heads;
+    p.group = a.num_heads / a.num_kv_heads;
+    p.total_rows = p.group * a.q_len;
+    p.mtiles = (p.total_rows + kTcRows - 1) / kTcRows;
+    p.max_context_len = a.max_context_len;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    const long long grid = (long long)a.num_seqs * a.num_kv_heads * p.mtiles;
+    if (grid > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    auto kfn = prefill_tc_kernel<T, D>;
+    const int smem = TcLayout<D>::kAlloc;
+    if (int st = ensure_dynamic_smem(reinterpret_cast<const void*>(kfn), smem)) return st;
+    const bool prof = profile_begin(stream);
+    if (launch_pdl(kfn, dim3((unsigned)grid), dim3(kTcThreads), (size_t)smem, stream, p) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (prof) profile_end(stream);
+    *launches += 1;
+    return PA_OK;
+}
+
+}  // namespace
+
+int launch_prefill_tc(const DecodeArgs& a, cudaStream_t stream, int* launches) {
+    if (a.fp8) return PA_ERR_UNSUPPORTED;
+    if (a.dtype == PA_BF16) {
+        if (a.head_dim == 128) return launch_prefill_tc_typed<__nv_bfloat16, 128>(a, stream, launches);
+        if (a.head_dim == 64) return launch_prefill_tc_typed<__nv_bfloat16, 64>(a, stream, launches);
+    } else {
+        if (a.head_dim == 128) return launch_prefill_tc_typed<__half, 128>(a, stream, launches);
+        if (a.head_dim == 64) return launch_prefill_tc_typed<__half, 64>(a, stream, launches);
+    }
+    return PA_ERR_UNSUPPORTED;
+}
+
+}  // namespace pa

@@ -294,10 +294,12 @@ def get_device_error(clear: bool = True, stream=None) -> int:
 
 
 def set_decode_math(math: str) -> None:
-    """'auto' (default): CUDA-core FMA for one query row per kv head, tensor-core tiles otherwise;
-    'fma': CUDA-core FMA up to 8 query rows per kv head; 'tensor': tensor-core tiles everywhere.
-    Process-wide."""
-    _check("pa_set_decode_math", lib().pa_set_decode_math({"auto": 0, "fma": 1, "tensor": 2}[math]))
+    """'auto' (default): CUDA-core FMA for one query row per kv head, mma.sync tensor-core tiles
+    for grouped heads and short chunks, the tcgen05 prefill kernel from 128 query rows per kv head;
+    'fma': CUDA-core FMA up to 8 query rows per kv head; 'tensor': mma.sync tiles everywhere;
+    'tcgen05': the tcgen05 prefill kernel for every 16-bit call.  Process-wide."""
+    _check("pa_set_decode_math",
+           lib().pa_set_decode_math({"auto": 0, "fma": 1, "tensor": 2, "tcgen05": 3}[math]))
 
 
 def profile_enable(on: bool = True) -> None:

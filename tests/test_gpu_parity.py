@@ -137,7 +137,7 @@ def test_shared_prefix_equals_private_copies():
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("math", ["tensor", "fma"])
+@pytest.mark.parametrize("math", ["tensor", "fma", "tcgen05"])
 def test_gqa_equals_replicated_mha(math):
     """GQA (4 query heads per kv head) equals MHA over kv heads repeated 4 times, bit for bit,
     with either consumer arithmetic (each row's sums do not depend on the other rows)."""
@@ -207,6 +207,11 @@ def test_launch_counts():
     step16 = G.GpuStep(w, partition_size=16)
     step16.attend()
     assert pa.last_launch_count() == 3
+    # a prefill chunk with >= 128 query rows per kv head: one tcgen05 kernel
+    chunk = W.make_workload("chunk", [200, 300], num_heads=8, num_kv_heads=2, head_dim=128, q_len=32,
+                            num_blocks=40, seed=31)
+    G.GpuStep(chunk).attend()
+    assert pa.last_launch_count() == 1
 
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 5])
@@ -252,10 +257,15 @@ def test_tensor_path_on_single_row_heads(cfg):
     assert G.ulps_from_rounded_oracle(got, ref, w.dtype) <= 1
 
 
-def test_chunked_prefill_workload():
-    """Chunked prefill: 16 sequences, a 256-token chunk each over up to 4096 tokens of history."""
+def test_chunked_prefill_workload_mma_sync():
+    """Chunked prefill on the mma.sync row-group path: 16 sequences, a 256-token chunk each over up
+    to 4096 tokens of history."""
     w = W.chunked_prefill()
-    got = G.GpuStep(w).run()
+    pa.set_decode_math("tensor")
+    try:
+        got = G.GpuStep(w).run()
+    finally:
+        pa.set_decode_math("auto")
     kc, vc, ref = G.oracle_step(w)
     G.compare(got, ref, w.dtype, w.name)
     assert G.ulps_from_rounded_oracle(got, ref, w.dtype) <= 1
