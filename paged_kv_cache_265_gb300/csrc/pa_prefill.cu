@@ -1,6 +1,7 @@
 // pa_prefill.cu -- attention of prefill chunks over the paged KV cache on the
-// fifth-generation tensor cores: tcgen05.mma with its accumulators in tensor
-// memory (TMEM), K/V blocks staged in shared memory by tensor-map TMA.
+// fifth-generation tensor cores: tcgen05.mma with its accumulators and the
+// softmax weights in tensor memory (TMEM), K/V blocks staged in shared memory by
+// tensor-map TMA.
 //
 // It computes exactly what the multi-query decode path computes: the q_len
 // chunk tokens are the last q_len positions of each sequence, and query row j
@@ -14,27 +15,28 @@
 // One CTA = one tile of 128 query rows of one kv head.  Rows are token-major
 // (row r of a kv head is chunk token r / g, query head kvh * g + r % g), so a
 // tile spans 128 / g consecutive chunk tokens whose causal limits are close.
-// For each K/V tile of 128 positions (8 pool blocks):
-//   S = Q K^T    M = 128, N = 16 x blocks, K = D: A = Q, B = K tile, both
-//                K-major and 128-byte swizzled; S (fp32) in TMEM columns 0-127
-//   softmax      warps 0-3, thread i = TMEM lane i = tile row i: one tcgen05.ld
-//                of the row, masking, log2-unit scaling, ex2.approx against a
-//                running max that is raised only when it grows by more than 8
-//                (weights stay <= 2^8; the final division uses the same max,
-//                so only rounding changes); each weight p is split into
-//                p_hi = p rounded to the input type and p_lo = (p - p_hi)
-//                rounded, both stored as A operands (about 16 significant bits
-//                of p reach the product; one 16-bit P alone misses the
-//                attention tolerance when a few positions dominate)
-//   O += P V     M = 128, N = D, K = 16 x blocks, once with P_hi and once with
-//                P_lo: B = V tile (MN-major: d is contiguous in the cache); O
-//                (fp32) in TMEM columns 128 .. 128 + D - 1
-// The S product of tile j + 1 is issued as soon as the softmax warps have
-// copied S_j out of TMEM, so it runs under their exponentials, and P_j V_j runs
-// while they start on tile j + 1.
+// For each K/V tile j of 128 positions (8 pool blocks):
+//   S_j = Q K^T   M = 128, N = 16 x blocks, K = D, A = Q and B = K tile from
+//                 shared memory (K-major, 128-byte swizzled); S_j (fp32) into
+//                 TMEM buffer j % 2 (columns 0-127 or 128-255)
+//   softmax       warps 0-3, thread i = TMEM lane i = tile row i: one tcgen05.ld
+//                 of the row, masking, ex2.approx of the log2-scaled scores
+//                 against a running max that is raised only when it grows by
+//                 more than 8 (weights stay <= 2^8; the final division uses the
+//                 same max, so only rounding changes).  Each weight p is split
+//                 into p_hi = p rounded to the input type and p_lo = (p - p_hi)
+//                 rounded (about 16 significant bits reach the product; one
+//                 16-bit P alone misses the attention tolerance when a few
+//                 positions dominate); both are stored back into the S buffer
+//                 (columns 0-63 and 64-127 of it, two weights per column)
+//   O += P V      M = 128, N = D, K = 16 x blocks, A = P_hi then P_lo straight
+//                 from TMEM, B = V tile (MN-major: d is contiguous in the
+//                 cache); O (fp32) in TMEM columns 256 .. 256 + D - 1
+// With two S buffers, S_{j+1} runs on the tensor cores while the softmax warps
+// work on S_j, and P_j V_j while they start on S_{j+1}.
 //
 // Warps: 0-3 softmax and epilogue, 4 TMA producer (K/V blocks found through the
-// block table, two stages of one K/V tile), 5 TMEM owner and MMA issuer (one
+// block table, three stages of one K/V tile), 5 TMEM owner and MMA issuer (one
 // thread).  Every wait is bounded (PA_DEVERR_TIMEOUT); a failed wait stops all
 // roles, and the CTA lets its copies and products finish before it frees TMEM.
 #include <cuda.h>
@@ -52,11 +54,11 @@ namespace {
 constexpr int kTcRows = 128;             // query rows per CTA tile (MMA M)
 constexpr int kTcPos = 128;              // positions per K/V tile
 constexpr int kTcBlocks = kTcPos / 16;   // pool blocks per K/V tile
-constexpr int kTcStages = 2;             // K/V tiles in flight
+constexpr int kTcStages = 3;             // K/V tiles in flight
 constexpr int kTcThreads = 192;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kTmemS = 0;           // S columns
-constexpr uint32_t kTmemO = 128;         // O columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0;           // S / P buffers: columns 0-127 and 128-255
+constexpr uint32_t kTmemO = 256;         // O columns
 constexpr int kRegion = kTcRows * 128;   // 128 rows x 128 B: one 64-element column block
 constexpr int kBox = 16 * 128;           // one TMA box: 16 positions x 64 elements
 
@@ -84,14 +86,12 @@ template <int D>
 struct TcLayout {
     static constexpr int kHalves = D / 64;                 // 64-element column blocks of d
     static constexpr int kQ = 0;                           // Q tile, K-major
-    static constexpr int kP = kQ + kHalves * kRegion;      // P_hi tile, K-major (2 blocks of 64 positions)
-    static constexpr int kPlo = kP + 2 * kRegion;          // P_lo tile, same layout
-    static constexpr int kStage0 = kPlo + 2 * kRegion;     // stages: K tile then V tile
+    static constexpr int kStage0 = kQ + kHalves * kRegion; // stages: K tile then V tile
     static constexpr int kKBytes = kHalves * kRegion;
     static constexpr int kStageBytes = 2 * kKBytes;
     static constexpr int kBars = kStage0 + kTcStages * kStageBytes;
-    // barriers: kvfull[2] +0, kvempty[2] +16, sfull +32, sfree +40, pfull +48,
-    // odone +56, drain +64, qready +72; TMEM base +80; abort flag +84
+    // barriers (8 B each): kvfull[3] +0, kvempty[3] +24, sfull[2] +48, pfull +64, odone +72,
+    // drain +80, qready +88; TMEM base +96; abort flag +100
     static constexpr int kTotal = kBars + 128;
     static constexpr int kAlloc = kTotal + 1024;           // slack to align the base to 1024 B
 };
@@ -105,6 +105,19 @@ __device__ __forceinline__ float hi16(uint32_t v, std::false_type) {
     return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]: the A operand (M = 128 rows in TMEM lanes, two
+// 16-bit K elements per column, the even one in the low half) read from tensor memory.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        :
+        : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
     using Lay = TcLayout<D>;
@@ -112,13 +125,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t q_s = sbase + Lay::kQ, p_s = sbase + Lay::kP, plo_s = sbase + Lay::kPlo,
-                   st_s = sbase + Lay::kStage0;
+    const uint32_t q_s = sbase + Lay::kQ, st_s = sbase + Lay::kStage0;
     const uint32_t bars = sbase + Lay::kBars;
-    const uint32_t kvfull = bars, kvempty = bars + 16, sfull = bars + 32, sfree = bars + 40, pfull = bars + 48,
-                   odone = bars + 56, drain = bars + 64, qready = bars + 72;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Lay::kBars + 80);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kBars + 84);
+    const uint32_t kvfull = bars, kvempty = bars + 24, sfull = bars + 48, pfull = bars + 64, odone = bars + 72,
+                   drain = bars + 80, qready = bars + 88;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Lay::kBars + 96);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kBars + 100);
     int* err = p.err;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -135,7 +147,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             mbar_init(kvempty + 8 * s, 1);
         }
         mbar_init(sfull, 1);
-        mbar_init(sfree, kTcRows);
+        mbar_init(sfull + 8, 1);
         mbar_init(pfull, kTcRows);
         mbar_init(odone, 1);
         mbar_init(drain, 1);
@@ -144,7 +156,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         fence_barrier_init();
     }
     if (warp == 5) {
-        tc::alloc(bars + 80, kTmemCols);
+        tc::alloc(bars + 96, kTmemCols);
         tc::relinquish_alloc_permit();
     }
     tc::fence_before_sync();
@@ -169,12 +181,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     if (valid && warp == 4) {
         // ===================== TMA producer =====================
         const int* bt = p.block_tables + (long long)seq * p.max_blocks_per_seq;
-        int armed[kTcStages] = {0, 0};
+        int armed[kTcStages] = {0, 0, 0};
         for (int j = 0; j < ntiles; ++j) {
-            const int s = j & 1;
+            const int s = j % kTcStages;
             if (j >= kTcStages) {
                 bool w = true;
-                if (lane == 0) w = mbar_wait(kvempty + 8 * s, ((j >> 1) - 1) & 1, err, abort_flag);
+                if (lane == 0) w = mbar_wait(kvempty + 8 * s, ((j / kTcStages) - 1) & 1, err, abort_flag);
                 if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
             }
             const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
@@ -207,41 +219,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         __syncwarp();
     } else if (valid && warp == 5) {
         // ===================== MMA issuer =====================
+        // Order: S_j, then P_{j-1} V_{j-1}.  S_j overwrites the buffer P_{j-2} was read
+        // from, so it waits for P_{j-2} V_{j-2} to complete.
         if (lane == 0) {
             constexpr bool kBf16 = IsBf16::value;
             const uint32_t id_o = tc::idesc_f16(kBf16, true, kTcRows, D);
             bool ok = mbar_wait(qready, 0, err, abort_flag);
             for (int j = 0; ok && j <= ntiles; ++j) {
                 if (j < ntiles) {
-                    const int s = j & 1;
-                    ok = mbar_wait(kvfull + 8 * s, (j >> 1) & 1, err, abort_flag) &&
-                         (j == 0 || mbar_wait(sfree, (j - 1) & 1, err, abort_flag));
+                    const int s = j % kTcStages;
+                    ok = mbar_wait(kvfull + 8 * s, (j / kTcStages) & 1, err, abort_flag) &&
+                         (j < 2 || mbar_wait(odone, (j - 2) & 1, err, abort_flag));
                     if (!ok) break;
                     tc::fence_after_sync();
                     const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
                     const uint32_t id_s = tc::idesc_f16(kBf16, false, kTcRows, 16 * nb);
                     const uint32_t kst = st_s + s * Lay::kStageBytes;
+                    const uint32_t d_s = tmem + kTmemS + (uint32_t)(j & 1) * 128;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * kRegion + (kk & 3) * 32;
-                        tc::mma_f16_ss(tmem + kTmemS, tc::smem_desc_sw128(q_s + off, 16, 1024),
+                        tc::mma_f16_ss(d_s, tc::smem_desc_sw128(q_s + off, 16, 1024),
                                        tc::smem_desc_sw128(kst + off, 16, 1024), id_s, kk > 0);
                     }
-                    tc::commit(sfull);
+                    tc::commit(sfull + 8 * (j & 1));
                 }
                 if (j > 0) {
-                    const int i = j - 1, s = i & 1;
+                    const int i = j - 1, s = i % kTcStages;
                     ok = mbar_wait(pfull, i & 1, err, abort_flag);
                     if (!ok) break;
                     tc::fence_after_sync();
                     const int nb = min(kTcBlocks, nblk - kTcBlocks * i);
                     const uint32_t vst = st_s + s * Lay::kStageBytes + Lay::kKBytes;
+                    const uint32_t p_t = tmem + kTmemS + (uint32_t)(i & 1) * 128;  // P_hi; P_lo at +64
                     for (int kk = 0; kk < nb; ++kk) {
-                        const uint32_t aoff = (kk >> 2) * kRegion + (kk & 3) * 32;
                         const uint64_t vdesc = tc::smem_desc_sw128(vst + kk * 2 * 1024, kRegion, 1024);
-                        tc::mma_f16_ss(tmem + kTmemO, tc::smem_desc_sw128(p_s + aoff, 16, 1024), vdesc, id_o,
-                                       (i > 0 || kk > 0) ? 1u : 0u);
-                        tc::mma_f16_ss(tmem + kTmemO, tc::smem_desc_sw128(plo_s + aoff, 16, 1024), vdesc, id_o, 1u);
+                        mma_f16_ts(tmem + kTmemO, p_t + kk * 8, vdesc, id_o, (i > 0 || kk > 0) ? 1u : 0u);
+                        mma_f16_ts(tmem + kTmemO, p_t + 64 + kk * 8, vdesc, id_o, 1u);
                     }
                     tc::commit(kvempty + 8 * s);
                     tc::commit(odone);
@@ -263,6 +277,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         const int lim_min = L - p.q_len + t_first;     // smallest limit in the tile
         const uint32_t lane_tmem = tmem + ((uint32_t)(warp * 32) << 16);
         const long long row_off = (((long long)seq * p.q_len + t) * p.num_heads + hq) * D;
+        const float c2 = p.scale_log2;
 
         // Q row into the K-major swizzled tile (rows past the chunk are zeros).
         {
@@ -279,15 +294,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            if (!__all_sync(0xffffffffu, mbar_wait(sfull, j & 1, err, abort_flag))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(sfull + 8 * (j & 1), (j >> 1) & 1, err, abort_flag))) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
+            const uint32_t buf = lane_tmem + kTmemS + (uint32_t)(j & 1) * 128;
             uint32_t sv[128];
-            tc::ld_x128(lane_tmem + kTmemS, sv);
-            tc::fence_before_sync();
-            mbar_arrive(sfree);
+            tc::ld_x128(buf, sv);
 
             const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
             const int pos0 = kTcPos * j;
@@ -296,7 +310,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             // column c holds position pos0 + c - sh.
             const bool short_here = sh > 0 && lastblk < kTcBlocks * j + nb;
             const bool edge = nb < kTcBlocks || short_here || pos0 + kTcPos - 1 > lim_min;
-            float tmax = -INFINITY;
+            // Scores go to log2 units as s * c2 - m in one FFMA per weight, on every path, so a
+            // row's result does not depend on which other rows share its tile.  With a positive
+            // scale the max is taken on the raw scores (masked columns become -inf); a
+            // non-positive scale pre-multiplies every column instead.
+            const bool raw = c2 > 0.f;
+            const float cs = raw ? c2 : 1.f;
+            float mx[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
             if (edge) {
                 // Visible columns: [0, hi1] and [lo2, hi2].
                 const int lastc = short_here ? 16 * (lastblk - kTcBlocks * j) : 16 * nb;
@@ -306,18 +328,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
                     const bool vis = c <= hi1 || (c >= lo2 && c <= hi2);
-                    const float x = vis ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
+                    const float v = __uint_as_float(sv[c]);
+                    const float x = vis ? (raw ? v : v * c2) : -INFINITY;
                     sv[c] = __float_as_uint(x);
-                    tmax = fmaxf(tmax, x);
+                    mx[c & 7] = fmaxf(mx[c & 7], x);
+                }
+            } else if (!raw) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const float x = __uint_as_float(sv[c]) * c2;
+                    sv[c] = __float_as_uint(x);
+                    mx[c & 7] = fmaxf(mx[c & 7], x);
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const float x = __uint_as_float(sv[c]) * p.scale_log2;
-                    sv[c] = __float_as_uint(x);
-                    tmax = fmaxf(tmax, x);
-                }
+                for (int c = 0; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sv[c]));
             }
+            float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            if (raw) tmax *= c2;
             float alpha = 1.f;
             const bool bump = tmax > m_run + 8.f;
             if (bump) {
@@ -325,29 +354,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
                 m_run = tmax;
             }
             const float msub = m_run == -INFINITY ? 0.f : m_run;
-            float sum = 0.f;
-            uint32_t pk[64], pl[64];  // P_hi and P_lo, two weights per register
+            float sm[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) sm[u] = 0.f;
+            uint32_t ph[64], pl[64];  // P_hi and P_lo, two weights per register
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                const float p0 = ex2(__uint_as_float(sv[2 * c]) - msub);
-                const float p1 = ex2(__uint_as_float(sv[2 * c + 1]) - msub);
-                pk[c] = Elem<T>::pack(p0, p1);
-                pl[c] = Elem<T>::pack(p0 - lo16(pk[c], IsBf16()), p1 - hi16(pk[c], IsBf16()));
-                sum += p0 + p1;
+                const float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), cs, -msub));
+                const float p1 = ex2(fmaf(__uint_as_float(sv[2 * c + 1]), cs, -msub));
+                ph[c] = Elem<T>::pack(p0, p1);
+                pl[c] = Elem<T>::pack(p0 - lo16(ph[c], IsBf16()), p1 - hi16(ph[c], IsBf16()));
+                sm[c & 7] += p0 + p1;
             }
-            // P_{j-1} V_{j-1} must be done before P and O are touched.
+            const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+            tc::st_x64(buf, ph);
+            tc::st_x64(buf + 64, pl);
+            // P_{j-1} V_{j-1} must be done before O is rescaled.
             if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(odone, (j - 1) & 1, err, abort_flag))) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-                if (c < 2 * nb) {
-                    const uint32_t off = (c >> 3) * kRegion + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-                    tc::st_shared_v4(p_s + off, make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
-                    tc::st_shared_v4(plo_s + off, make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]));
-                }
             if (j > 0 && __any_sync(0xffffffffu, bump)) {
 #pragma unroll
                 for (int h = 0; h < D / 64; ++h) {
@@ -357,10 +384,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
                     for (int c = 0; c < 64; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
                     tc::st_x64(lane_tmem + kTmemO + 64 * h, o);
                 }
-                tc::wait_st();
             }
+            tc::wait_st();
             l_run = l_run * alpha + sum;
-            fence_proxy_async_smem();
             tc::fence_before_sync();
             mbar_arrive(pfull);
         }
