@@ -16,9 +16,13 @@
 // (row r of a kv head is chunk token r / g, query head kvh * g + r % g), so a
 // tile spans 128 / g consecutive chunk tokens whose causal limits are close.
 // For each K/V tile j of 128 positions (8 pool blocks):
-//   S_j = Q K^T   M = 128, N = 16 x blocks, K = D, A = Q and B = K tile from
-//                 shared memory (K-major, 128-byte swizzled); S_j (fp32) into
-//                 TMEM buffer j % 2 (columns 0-127 or 128-255)
+//   S_j = Q K^T   M = 128, N = 16 x blocks, K = D: A = Q, held in TMEM for the
+//                 whole CTA (columns 384 .. 384 + D/2 - 1, two elements per
+//                 column), B = K tile from shared memory (K-major, 128-byte
+//                 swizzled); S_j (fp32) into TMEM buffer j % 2 (columns 0-127 or
+//                 128-255).  With both operands in shared memory a 128 x 128
+//                 product is limited by the shared-memory operand reads; with A
+//                 in TMEM it runs at the tensor rate
 //   softmax       warps 0-3, thread i = TMEM lane i = tile row i: one tcgen05.ld
 //                 of the row, masking, ex2.approx of the log2-scaled scores
 //                 against a running max that is raised only when it grows by
@@ -59,6 +63,7 @@ constexpr int kTcThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;           // S / P buffers: columns 0-127 and 128-255
 constexpr uint32_t kTmemO = 256;         // O columns
+constexpr uint32_t kTmemQ = 384;         // Q: two 16-bit elements per column
 constexpr int kRegion = kTcRows * 128;   // 128 rows x 128 B: one 64-element column block
 constexpr int kBox = 16 * 128;           // one TMA box: 16 positions x 64 elements
 
@@ -85,8 +90,7 @@ struct PrefillTcParams {
 template <int D>
 struct TcLayout {
     static constexpr int kHalves = D / 64;                 // 64-element column blocks of d
-    static constexpr int kQ = 0;                           // Q tile, K-major
-    static constexpr int kStage0 = kQ + kHalves * kRegion; // stages: K tile then V tile
+    static constexpr int kStage0 = 0;                      // stages: K tile then V tile
     static constexpr int kKBytes = kHalves * kRegion;
     static constexpr int kStageBytes = 2 * kKBytes;
     static constexpr int kBars = kStage0 + kTcStages * kStageBytes;
@@ -103,6 +107,14 @@ __device__ __forceinline__ float lo16(uint32_t v, std::false_type /*fp16*/) {
 }
 __device__ __forceinline__ float hi16(uint32_t v, std::false_type) {
     return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
+}
+
+// Bits of the columns in [lo, hi] that fall in the 32-column word starting at `base`.
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base) {
+    const int a = max(lo - base, 0), b = min(hi - base, 31);
+    if (b < a) return 0u;
+    const uint32_t upto_b = b == 31 ? 0xffffffffu : ((1u << (b + 1)) - 1u);
+    return upto_b & ~((1u << a) - 1u);
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]: the A operand (M = 128 rows in TMEM lanes, two
@@ -125,7 +137,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t q_s = sbase + Lay::kQ, st_s = sbase + Lay::kStage0;
+    const uint32_t st_s = sbase + Lay::kStage0;
     const uint32_t bars = sbase + Lay::kBars;
     const uint32_t kvfull = bars, kvempty = bars + 24, sfull = bars + 48, pfull = bars + 64, odone = bars + 72,
                    drain = bars + 80, qready = bars + 88;
@@ -182,21 +194,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         // ===================== TMA producer =====================
         const int* bt = p.block_tables + (long long)seq * p.max_blocks_per_seq;
         int armed[kTcStages] = {0, 0, 0};
+        // Block ids arrive 32 at a time (four tiles): lane l holds the id of block 32c + l
+        // of chunk c, and chunk c + 1 is requested when chunk c starts, so no tile waits on
+        // a block-table load.
+        int ids = lane < nblk ? __ldg(bt + lane) : 0;
+        int ids_next = 32 + lane < nblk ? __ldg(bt + 32 + lane) : 0;
         for (int j = 0; j < ntiles; ++j) {
             const int s = j % kTcStages;
+            const int jj = j & 3;
+            if (jj == 0 && j > 0) {
+                ids = ids_next;
+                const int nxt = 32 * ((j >> 2) + 1) + lane;
+                ids_next = nxt < nblk ? __ldg(bt + nxt) : 0;
+            }
             if (j >= kTcStages) {
                 bool w = true;
                 if (lane == 0) w = mbar_wait(kvempty + 8 * s, ((j / kTcStages) - 1) & 1, err, abort_flag);
                 if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
             }
             const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
-            int bid = 0;
-            bool good = false;
-            if (lane < nb) {
-                bid = __ldg(bt + kTcBlocks * j + lane);
-                good = bid >= 0 && bid < p.num_blocks;
-                if (!good) atomicOr(err, PA_DEVERR_BLOCK_ID);  // skipped: the tile computes on stale data
-            }
+            const int bid = __shfl_sync(0xffffffffu, ids, (8 * jj + lane) & 31);
+            const bool good = lane < nb && bid >= 0 && bid < p.num_blocks;
+            if (lane < nb && !good) atomicOr(err, PA_DEVERR_BLOCK_ID);  // skipped: the tile computes on stale data
             const unsigned gm = __ballot_sync(0xffffffffu, good);
             const uint32_t bar = kvfull + 8 * s;
             if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(gm) * 2u * Lay::kHalves * kBox);
@@ -239,8 +258,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * kRegion + (kk & 3) * 32;
-                        tc::mma_f16_ss(d_s, tc::smem_desc_sw128(q_s + off, 16, 1024),
-                                       tc::smem_desc_sw128(kst + off, 16, 1024), id_s, kk > 0);
+                        mma_f16_ts(d_s, tmem + kTmemQ + kk * 8, tc::smem_desc_sw128(kst + off, 16, 1024), id_s,
+                                   kk > 0);
                     }
                     tc::commit(sfull + 8 * (j & 1));
                 }
@@ -279,15 +298,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         const long long row_off = (((long long)seq * p.q_len + t) * p.num_heads + hq) * D;
         const float c2 = p.scale_log2;
 
-        // Q row into the K-major swizzled tile (rows past the chunk are zeros).
+        // Q row into TMEM lane r (rows past the chunk are zeros): 32-bit column c holds
+        // elements 2c (low half) and 2c + 1, which is how the row lies in memory.
         {
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.query) + row_off);
+            uint32_t qv[64];
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
                 const uint4 v = real ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-                tc::st_shared_v4(q_s + (c >> 3) * kRegion + r * 128 + (((c & 7) ^ (r & 7)) << 4), v);
+                qv[4 * c] = v.x;
+                qv[4 * c + 1] = v.y;
+                qv[4 * c + 2] = v.z;
+                qv[4 * c + 3] = v.w;
             }
-            fence_proxy_async_smem();
+            if constexpr (D == 128) {
+                tc::st_x64(lane_tmem + kTmemQ, qv);
+            } else {
+                uint32_t q32[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) q32[c] = qv[c];
+                tc::st_x32(lane_tmem + kTmemQ, q32);
+            }
+            tc::wait_st();
+            tc::fence_before_sync();
             mbar_arrive(qready);
         }
 
@@ -320,14 +353,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 #pragma unroll
             for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
             if (edge) {
-                // Visible columns: [0, hi1] and [lo2, hi2].
+                // Visible columns: [0, hi1] and [lo2, hi2], as a 128-bit mask.
                 const int lastc = short_here ? 16 * (lastblk - kTcBlocks * j) : 16 * nb;
                 const int hi1 = min(min(lim - pos0, 16 * nb - 1), lastc - 1);
                 const int lo2 = short_here ? lastc + sh : 128;
                 const int hi2 = min(lim - pos0 + sh, 16 * nb - 1);
+                uint32_t vm[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) vm[k] = range_bits(0, hi1, 32 * k) | range_bits(lo2, hi2, 32 * k);
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
-                    const bool vis = c <= hi1 || (c >= lo2 && c <= hi2);
+                    const bool vis = (vm[c >> 5] >> (c & 31)) & 1u;
                     const float v = __uint_as_float(sv[c]);
                     const float x = vis ? (raw ? v : v * c2) : -INFINITY;
                     sv[c] = __float_as_uint(x);
