@@ -117,16 +117,17 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base) {
     return upto_b & ~((1u << a) - 1u);
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]: the A operand (M = 128 rows in TMEM lanes, two
-// 16-bit K elements per column, the even one in the low half) read from tensor memory.
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem] (kAccumulate: add to D, else overwrite it), issued by one
+// thread: the A operand (M = 128 rows in TMEM lanes, two 16-bit K elements per column, the
+// even one in the low half) is read from tensor memory.
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
         :
-        : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "n"(kAccumulate ? 1 : 0)
         : "memory");
 }
 
@@ -240,9 +241,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         // ===================== MMA issuer =====================
         // Order: S_j, then P_{j-1} V_{j-1}.  S_j overwrites the buffer P_{j-2} was read
         // from, so it waits for P_{j-2} V_{j-2} to complete.
+        // The tensor cores take 64 cycles per 128 x 128 x 16 product, so the issuing thread does
+        // little else: descriptors are formed once per stage and each product adds a constant.
         if (lane == 0) {
             constexpr bool kBf16 = IsBf16::value;
-            const uint32_t id_o = tc::idesc_f16(kBf16, true, kTcRows, D);
+            constexpr uint32_t id_o = tc::idesc_f16(kBf16, true, kTcRows, D);
+            // Stage s adds s * kStageBytes / 16 to the start-address field of stage 0's
+            // descriptors and a product's K slice its byte offset / 16; addresses stay below
+            // 256 KB, so the 14-bit field never carries into the next one.
+            const uint64_t kdesc0 = tc::smem_desc_sw128(st_s, 16, 1024);
+            const uint64_t vdesc0 = tc::smem_desc_sw128(st_s + Lay::kKBytes, kRegion, 1024);
             bool ok = mbar_wait(qready, 0, err, abort_flag);
             for (int j = 0; ok && j <= ntiles; ++j) {
                 if (j < ntiles) {
@@ -253,14 +261,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
                     tc::fence_after_sync();
                     const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
                     const uint32_t id_s = tc::idesc_f16(kBf16, false, kTcRows, 16 * nb);
-                    const uint32_t kst = st_s + s * Lay::kStageBytes;
+                    const uint64_t kd = kdesc0 + (uint64_t)((s * Lay::kStageBytes) >> 4);
                     const uint32_t d_s = tmem + kTmemS + (uint32_t)(j & 1) * 128;
+                    mma_ts<false>(d_s, tmem + kTmemQ, kd, id_s);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kRegion + (kk & 3) * 32;
-                        mma_f16_ts(d_s, tmem + kTmemQ + kk * 8, tc::smem_desc_sw128(kst + off, 16, 1024), id_s,
-                                   kk > 0);
-                    }
+                    for (int kk = 1; kk < D / 16; ++kk)
+                        mma_ts<true>(d_s, tmem + kTmemQ + kk * 8, kd + (((kk >> 2) * kRegion + (kk & 3) * 32) >> 4),
+                                     id_s);
                     tc::commit(sfull + 8 * (j & 1));
                 }
                 if (j > 0) {
@@ -269,12 +276,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
                     if (!ok) break;
                     tc::fence_after_sync();
                     const int nb = min(kTcBlocks, nblk - kTcBlocks * i);
-                    const uint32_t vst = st_s + s * Lay::kStageBytes + Lay::kKBytes;
+                    const uint64_t vd = vdesc0 + (uint64_t)((s * Lay::kStageBytes) >> 4);
                     const uint32_t p_t = tmem + kTmemS + (uint32_t)(i & 1) * 128;  // P_hi; P_lo at +64
-                    for (int kk = 0; kk < nb; ++kk) {
-                        const uint64_t vdesc = tc::smem_desc_sw128(vst + kk * 2 * 1024, kRegion, 1024);
-                        mma_f16_ts(tmem + kTmemO, p_t + kk * 8, vdesc, id_o, (i > 0 || kk > 0) ? 1u : 0u);
-                        mma_f16_ts(tmem + kTmemO, p_t + 64 + kk * 8, vdesc, id_o, 1u);
+                    if (i == 0)
+                        mma_ts<false>(tmem + kTmemO, p_t, vd, id_o);
+                    else
+                        mma_ts<true>(tmem + kTmemO, p_t, vd, id_o);
+                    mma_ts<true>(tmem + kTmemO, p_t + 64, vd, id_o);
+#pragma unroll
+                    for (int kk = 1; kk < kTcBlocks; ++kk) {
+                        if (kk < nb) {  // one 16-position block per K step; 2048 B = 128 x 16 apart
+                            mma_ts<true>(tmem + kTmemO, p_t + kk * 8, vd + kk * 128, id_o);
+                            mma_ts<true>(tmem + kTmemO, p_t + 64 + kk * 8, vd + kk * 128, id_o);
+                        }
                     }
                     tc::commit(kvempty + 8 * s);
                     tc::commit(odone);
