@@ -23,24 +23,27 @@
 //                 128-255).  With both operands in shared memory a 128 x 128
 //                 product is limited by the shared-memory operand reads; with A
 //                 in TMEM it runs at the tensor rate
-//   softmax       warps 0-3, thread i = TMEM lane i = tile row i: one tcgen05.ld
-//                 of the row, masking, ex2.approx of the log2-scaled scores
+//   softmax       warps 0-7: warps w and w + 4 share TMEM lanes 32 (w % 4) ..,
+//                 so each tile row (lane) has two threads, one per 64-column
+//                 half.  A thread reads the other half only for the row max,
+//                 then masks, exponentiates (ex2.approx of the log2-scaled scores
 //                 against a running max that is raised only when it grows by
-//                 more than 8 (weights stay <= 2^8; the final division uses the
-//                 same max, so only rounding changes).  Each weight p is split
-//                 into p_hi = p rounded to the input type and p_lo = (p - p_hi)
-//                 rounded (about 16 significant bits reach the product; one
-//                 16-bit P alone misses the attention tolerance when a few
-//                 positions dominate); both are stored back into the S buffer
-//                 (columns 0-63 and 64-127 of it, two weights per column)
+//                 more than 8: weights stay <= 2^8 and the final division uses
+//                 the same max, so only rounding changes) and writes back its own
+//                 half.  Each weight p is split into p_hi = p rounded to the input
+//                 type and p_lo = (p - p_hi) rounded (about 16 significant bits
+//                 reach the product; one 16-bit P alone misses the attention
+//                 tolerance when a few positions dominate); for positions 64 h ..
+//                 64 h + 63 they go back over the same S columns, P_hi in the
+//                 first 32 and P_lo in the next 32 (two weights per column)
 //   O += P V      M = 128, N = D, K = 16 x blocks, A = P_hi then P_lo straight
 //                 from TMEM, B = V tile (MN-major: d is contiguous in the
 //                 cache); O (fp32) in TMEM columns 256 .. 256 + D - 1
 // With two S buffers, S_{j+1} runs on the tensor cores while the softmax warps
 // work on S_j, and P_j V_j while they start on S_{j+1}.
 //
-// Warps: 0-3 softmax and epilogue, 4 TMA producer (K/V blocks found through the
-// block table, three stages of one K/V tile), 5 TMEM owner and MMA issuer (one
+// Warps: 0-7 softmax and epilogue, 8 TMA producer (K/V blocks found through the
+// block table, three stages of one K/V tile), 9 TMEM owner and MMA issuer (one
 // thread).  Every wait is bounded (PA_DEVERR_TIMEOUT); a failed wait stops all
 // roles, and the CTA lets its copies and products finish before it frees TMEM.
 #include <cuda.h>
@@ -59,7 +62,7 @@ constexpr int kTcRows = 128;             // query rows per CTA tile (MMA M)
 constexpr int kTcPos = 128;              // positions per K/V tile
 constexpr int kTcBlocks = kTcPos / 16;   // pool blocks per K/V tile
 constexpr int kTcStages = 3;             // K/V tiles in flight
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;           // S / P buffers: columns 0-127 and 128-255
 constexpr uint32_t kTmemO = 256;         // O columns
@@ -95,8 +98,9 @@ struct TcLayout {
     static constexpr int kStageBytes = 2 * kKBytes;
     static constexpr int kBars = kStage0 + kTcStages * kStageBytes;
     // barriers (8 B each): kvfull[3] +0, kvempty[3] +24, sfull[2] +48, pfull +64, odone +72,
-    // drain +80, qready +88; TMEM base +96; abort flag +100
-    static constexpr int kTotal = kBars + 128;
+    // drain +80, qready +88, lready +96; TMEM base +104; abort flag +108; the two half-row
+    // sums of every row at +128 (float [2][128])
+    static constexpr int kTotal = kBars + 128 + 1024;
     static constexpr int kAlloc = kTotal + 1024;           // slack to align the base to 1024 B
 };
 
@@ -141,9 +145,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     const uint32_t st_s = sbase + Lay::kStage0;
     const uint32_t bars = sbase + Lay::kBars;
     const uint32_t kvfull = bars, kvempty = bars + 24, sfull = bars + 48, pfull = bars + 64, odone = bars + 72,
-                   drain = bars + 80, qready = bars + 88;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Lay::kBars + 96);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kBars + 100);
+                   drain = bars + 80, qready = bars + 88, lready = bars + 96;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Lay::kBars + 104);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kBars + 108);
+    float* lsum = reinterpret_cast<float*>(smem + Lay::kBars + 128);
     int* err = p.err;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,15 +166,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         }
         mbar_init(sfull, 1);
         mbar_init(sfull + 8, 1);
-        mbar_init(pfull, kTcRows);
+        mbar_init(pfull, 2 * kTcRows);
         mbar_init(odone, 1);
         mbar_init(drain, 1);
-        mbar_init(qready, kTcRows);
+        mbar_init(qready, 2 * kTcRows);
+        mbar_init(lready, 2 * kTcRows);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
-        tc::alloc(bars + 96, kTmemCols);
+    if (warp == 9) {
+        tc::alloc(bars + 104, kTmemCols);
         tc::relinquish_alloc_permit();
     }
     tc::fence_before_sync();
@@ -191,7 +197,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     const int lastblk = (L - 1) / 16;           // the sequence's last block ...
     const int sh = 16 * (lastblk + 1) - L;      // ... is short by sh rows, fetched as leading zeros
 
-    if (valid && warp == 4) {
+    if (valid && warp == 8) {
         // ===================== TMA producer =====================
         const int* bt = p.block_tables + (long long)seq * p.max_blocks_per_seq;
         int armed[kTcStages] = {0, 0, 0};
@@ -237,7 +243,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             for (int s = 0; s < kTcStages; ++s)
                 if (armed[s] > 0) mbar_wait(kvfull + 8 * s, (armed[s] - 1) & 1, err, nullptr);
         __syncwarp();
-    } else if (valid && warp == 5) {
+    } else if (valid && warp == 9) {
         // ===================== MMA issuer =====================
         // Order: S_j, then P_{j-1} V_{j-1}.  S_j overwrites the buffer P_{j-2} was read
         // from, so it waits for P_{j-2} V_{j-2} to complete.
@@ -277,17 +283,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
                     tc::fence_after_sync();
                     const int nb = min(kTcBlocks, nblk - kTcBlocks * i);
                     const uint64_t vd = vdesc0 + (uint64_t)((s * Lay::kStageBytes) >> 4);
-                    const uint32_t p_t = tmem + kTmemS + (uint32_t)(i & 1) * 128;  // P_hi; P_lo at +64
+                    // K step kk = positions 16 kk .. 16 kk + 15: P_hi at column 64 (kk / 4) +
+                    // 8 (kk % 4) of the buffer, P_lo 32 columns on; V rows 2048 B = 128 x 16 apart
+                    const uint32_t p_t = tmem + kTmemS + (uint32_t)(i & 1) * 128;
                     if (i == 0)
                         mma_ts<false>(tmem + kTmemO, p_t, vd, id_o);
                     else
                         mma_ts<true>(tmem + kTmemO, p_t, vd, id_o);
-                    mma_ts<true>(tmem + kTmemO, p_t + 64, vd, id_o);
+                    mma_ts<true>(tmem + kTmemO, p_t + 32, vd, id_o);
 #pragma unroll
                     for (int kk = 1; kk < kTcBlocks; ++kk) {
-                        if (kk < nb) {  // one 16-position block per K step; 2048 B = 128 x 16 apart
-                            mma_ts<true>(tmem + kTmemO, p_t + kk * 8, vd + kk * 128, id_o);
-                            mma_ts<true>(tmem + kTmemO, p_t + 64 + kk * 8, vd + kk * 128, id_o);
+                        if (kk < nb) {
+                            const uint32_t pa = p_t + 64 * (kk >> 2) + 8 * (kk & 3);
+                            mma_ts<true>(tmem + kTmemO, pa, vd + kk * 128, id_o);
+                            mma_ts<true>(tmem + kTmemO, pa + 32, vd + kk * 128, id_o);
                         }
                     }
                     tc::commit(kvempty + 8 * s);
@@ -300,25 +309,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         }
         __syncwarp();
     } else if (valid) {
-        // ===================== softmax and epilogue (warps 0-3) =====================
-        const int r = threadIdx.x;  // tile row = TMEM lane
+        // ===================== softmax and epilogue (warps 0-7) =====================
+        const int hf = warp >> 2;                   // column half of the row this thread owns
+        const int r = threadIdx.x & (kTcRows - 1);  // tile row = TMEM lane
         const int gr = row0 + r;
         const bool real = gr < p.total_rows;
         const int t = real ? gr / p.group : p.q_len - 1;
         const int hq = kvh * p.group + (real ? gr - t * p.group : 0);
         const int lim = L - p.q_len + t;               // last position this row sees
         const int lim_min = L - p.q_len + t_first;     // smallest limit in the tile
-        const uint32_t lane_tmem = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t lane_tmem = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t o_half = lane_tmem + kTmemO + (D / 2) * hf;  // this thread's half of O
         const long long row_off = (((long long)seq * p.q_len + t) * p.num_heads + hq) * D;
         const float c2 = p.scale_log2;
 
-        // Q row into TMEM lane r (rows past the chunk are zeros): 32-bit column c holds
-        // elements 2c (low half) and 2c + 1, which is how the row lies in memory.
+        // This thread's half of the Q row into TMEM lane r (rows past the chunk are zeros):
+        // 32-bit column c holds elements 2c (low half) and 2c + 1, as the row lies in memory.
         {
-            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.query) + row_off);
-            uint32_t qv[64];
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.query) + row_off) + hf * (D / 16);
+            uint32_t qv[32];
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
+            for (int c = 0; c < D / 16; ++c) {
                 const uint4 v = real ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
                 qv[4 * c] = v.x;
                 qv[4 * c + 1] = v.y;
@@ -326,12 +337,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
                 qv[4 * c + 3] = v.w;
             }
             if constexpr (D == 128) {
-                tc::st_x64(lane_tmem + kTmemQ, qv);
+                tc::st_x32(lane_tmem + kTmemQ + 32 * hf, qv);
             } else {
-                uint32_t q32[32];
+                uint32_t q16[16];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) q32[c] = qv[c];
-                tc::st_x32(lane_tmem + kTmemQ, q32);
+                for (int c = 0; c < 16; ++c) q16[c] = qv[c];
+                tc::st_x16(lane_tmem + kTmemQ + 16 * hf, q16);
             }
             tc::wait_st();
             tc::fence_before_sync();
@@ -347,9 +358,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             }
             tc::fence_after_sync();
             const uint32_t buf = lane_tmem + kTmemS + (uint32_t)(j & 1) * 128;
-            uint32_t sv[128];
-            tc::ld_x128(buf, sv);
-
             const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
             const int pos0 = kTcPos * j;
             // Column c holds position pos0 + c, except in the sequence's short last block
@@ -363,40 +371,54 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             // non-positive scale pre-multiplies every column instead.
             const bool raw = c2 > 0.f;
             const float cs = raw ? c2 : 1.f;
-            float mx[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
-            if (edge) {
-                // Visible columns: [0, hi1] and [lo2, hi2], as a 128-bit mask.
+            const bool transform = edge || !raw;
+            uint32_t vm[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+            if (edge) {  // visible columns: [0, hi1] and [lo2, hi2], as a 128-bit mask
                 const int lastc = short_here ? 16 * (lastblk - kTcBlocks * j) : 16 * nb;
                 const int hi1 = min(min(lim - pos0, 16 * nb - 1), lastc - 1);
                 const int lo2 = short_here ? lastc + sh : 128;
                 const int hi2 = min(lim - pos0 + sh, 16 * nb - 1);
-                uint32_t vm[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) vm[k] = range_bits(0, hi1, 32 * k) | range_bits(lo2, hi2, 32 * k);
+            }
+            float mx[8];
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const bool vis = (vm[c >> 5] >> (c & 31)) & 1u;
-                    const float v = __uint_as_float(sv[c]);
-                    const float x = vis ? (raw ? v : v * c2) : -INFINITY;
-                    sv[c] = __float_as_uint(x);
-                    mx[c & 7] = fmaxf(mx[c & 7], x);
+            for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+            {  // the other half of the row, for the row max only
+                const int oh = hf ^ 1;
+                uint32_t ov[64];
+                tc::ld_x64(buf + 64 * oh, ov);
+                if (transform) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const uint32_t w = vm[2 * oh + (c >> 5)];
+                        const float v = __uint_as_float(ov[c]);
+                        mx[c & 7] = fmaxf(mx[c & 7], ((w >> (c & 31)) & 1u) ? (raw ? v : v * c2) : -INFINITY);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(ov[c]));
                 }
-            } else if (!raw) {
+            }
+            uint32_t sv[64];
+            tc::ld_x64(buf + 64 * hf, sv);
+            if (transform) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const float x = __uint_as_float(sv[c]) * c2;
+                for (int c = 0; c < 64; ++c) {
+                    const uint32_t w = vm[2 * hf + (c >> 5)];
+                    const float v = __uint_as_float(sv[c]);
+                    const float x = ((w >> (c & 31)) & 1u) ? (raw ? v : v * c2) : -INFINITY;
                     sv[c] = __float_as_uint(x);
                     mx[c & 7] = fmaxf(mx[c & 7], x);
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sv[c]));
+                for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sv[c]));
             }
             float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             if (raw) tmax *= c2;
+            // Both threads of a row see the same maxima, so they take the same decisions.
             float alpha = 1.f;
             const bool bump = tmax > m_run + 8.f;
             if (bump) {
@@ -407,9 +429,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             float sm[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) sm[u] = 0.f;
-            uint32_t ph[64], pl[64];  // P_hi and P_lo, two weights per register
+            uint32_t ph[32], pl[32];  // P_hi and P_lo of positions 64 hf .., two weights per register
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
+            for (int c = 0; c < 32; ++c) {
                 const float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), cs, -msub));
                 const float p1 = ex2(fmaf(__uint_as_float(sv[2 * c + 1]), cs, -msub));
                 ph[c] = Elem<T>::pack(p0, p1);
@@ -417,8 +439,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
                 sm[c & 7] += p0 + p1;
             }
             const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
-            tc::st_x64(buf, ph);
-            tc::st_x64(buf + 64, pl);
+            tc::st_x32(buf + 64 * hf, ph);
+            tc::st_x32(buf + 64 * hf + 32, pl);
             // P_{j-1} V_{j-1} must be done before O is rescaled.
             if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(odone, (j - 1) & 1, err, abort_flag))) {
                 ok = false;
@@ -428,11 +450,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             if (j > 0 && __any_sync(0xffffffffu, bump)) {
 #pragma unroll
                 for (int h = 0; h < D / 64; ++h) {
-                    uint32_t o[64];
-                    tc::ld_x64(lane_tmem + kTmemO + 64 * h, o);
+                    uint32_t o[32];
+                    tc::ld_x32(o_half + 32 * h, o);
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                    tc::st_x64(lane_tmem + kTmemO + 64 * h, o);
+                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                    tc::st_x32(o_half + 32 * h, o);
                 }
             }
             tc::wait_st();
@@ -441,24 +463,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             mbar_arrive(pfull);
         }
 
-        // Epilogue: O / l, rounded once, to out[seq, t, hq, :].
+        // Epilogue: the row's two half sums, then O / l, rounded once, to out[seq, t, hq, :]
+        // (this thread's half of the columns).
         if (ok && __all_sync(0xffffffffu, mbar_wait(odone, (ntiles - 1) & 1, err, abort_flag))) {
-            tc::fence_after_sync();
-            const float inv = 1.f / l_run;
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row_off);
+            lsum[hf * kTcRows + r] = l_run;
+            mbar_arrive(lready);
+            if (__all_sync(0xffffffffu, mbar_wait(lready, 0, err, abort_flag))) {
+                tc::fence_after_sync();
+                const float inv = 1.f / (lsum[r] + lsum[kTcRows + r]);
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row_off) + hf * (D / 16);
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
-                uint32_t o[64];
-                tc::ld_x64(lane_tmem + kTmemO + 64 * h, o);
-                if (real) {
+                for (int h = 0; h < D / 64; ++h) {
+                    uint32_t o[32];
+                    tc::ld_x32(o_half + 32 * h, o);
+                    if (real) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint4 v;
-                        v.x = Elem<T>::pack(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
-                        v.y = Elem<T>::pack(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
-                        v.z = Elem<T>::pack(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
-                        v.w = Elem<T>::pack(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
-                        dst[h * 8 + c] = v;
+                        for (int c = 0; c < 4; ++c) {
+                            uint4 v;
+                            v.x = Elem<T>::pack(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
+                            v.y = Elem<T>::pack(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
+                            v.z = Elem<T>::pack(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
+                            v.w = Elem<T>::pack(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
+                            dst[h * 4 + c] = v;
+                        }
                     }
                 }
             }
@@ -468,7 +495,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     // Teardown: every TMEM access and product is complete; free TMEM.
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc::fence_after_sync();
         tc::dealloc(tmem, kTmemCols);
     }
