@@ -478,7 +478,12 @@ def run_ours(args, rank, world, local):
     peak, peak_kind = peaks()
     kern_ms = kern_ms_total / max(1, kern_n)
     achieved = attn_bytes / (kern_ms * 1e-3) / 1e9
-    traffic = ncu_traffic(args.workload) if not kv8 and args.math == "auto" else None
+    # The library runs a call with >= 128 query rows per kv head (and the default split) on the
+    # tcgen05 prefill kernel, everything else on the split-K decode kernel.
+    tc_path = not kv8 and (args.math == "tcgen05" or
+                           (args.math == "auto" and (w.num_heads // w.num_kv_heads) * w.q_len >= 128))
+    kernel_name = "prefill_tc_kernel (tcgen05, no split)" if tc_path else "decode_kernel (partition pass)"
+    traffic = ncu_traffic(args.workload) if not kv8 and not tc_path and args.math == "auto" else None
     flops = W.attention_flops(w)
     tpeak, tpeak_kind = tensor_peak()
     compute_bound = flops / attn_bytes > tpeak * 1e12 / (peak * 1e9)   # past the ridge point
@@ -487,7 +492,8 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": DESCR[cfg], "seq_tokens_per_step": seq_tokens, "bytes_per_step": step_bytes,
-                   "attention_bytes": attn_bytes, "partition_tokens": 512, "math": args.math, "kv_cache": args.kv,
+                   "attention_bytes": attn_bytes, "partition_tokens": None if tc_path else 512, "math": args.math,
+                   "kv_cache": args.kv,
                    "l2": "flushed between steps" if flush is not None else
                    f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step vs 129 MB L2)",
                    "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
@@ -495,12 +501,12 @@ def run_ours(args, rank, world, local):
         "roofline": ({"bound": "tensor", "achieved": flops / (kern_ms * 1e-3) / 1e12, "peak": tpeak,
                       "unit": "TFLOP/s", "frac": flops / (kern_ms * 1e-3) / 1e12 / tpeak,
                       "peak_source": f"{tpeak_kind} dense bf16 cuBLAS burst", "flops_per_launch": flops,
-                      "kernel": "decode_kernel (partition pass)", "kernel_ms": kern_ms, "traffic": traffic,
+                      "kernel": kernel_name, "kernel_ms": kern_ms, "traffic": traffic,
                       "hbm_gbs": achieved}
                      if compute_bound else
                      {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                       "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",
-                      "kernel": "decode_kernel (partition pass)", "kernel_ms": kern_ms,
+                      "kernel": kernel_name, "kernel_ms": kern_ms,
                       "traffic": traffic, "tflops": flops / (kern_ms * 1e-3) / 1e12}),
         "gpu_launches": launches_per_step * args.steps,
         "roofline_steps": kern_n,
@@ -616,8 +622,9 @@ def main():
                     help="decode_step: the timed hot path; copy_blocks / spec_verify: those steps alone")
     ap.add_argument("--kv", choices=["16bit", "fp8"], default="16bit",
                     help="KV cache element type: the workload's 16-bit type, or FP8 E4M3 with per-cache scales")
-    ap.add_argument("--math", choices=["auto", "fma", "tensor"], default="auto",
-                    help="decode consumer arithmetic (auto: CUDA cores for one row per kv head, else tensor cores)")
+    ap.add_argument("--math", choices=["auto", "fma", "tensor", "tcgen05"], default="auto",
+                    help="attention arithmetic (auto: CUDA cores for one row per kv head, mma.sync tiles for "
+                         "grouped heads and short chunks, the tcgen05 kernel from 128 rows per kv head)")
     args = ap.parse_args()
     rank, world, local = dist_setup(args)
     try:
