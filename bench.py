@@ -374,6 +374,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(dev)
 
     attn_bytes = W.attention_bytes(w, 1 if kv8 else None)
+    unique_bytes = W.unique_attention_bytes(w, 1 if kv8 else None)  # shared blocks counted once
     step_bytes = attn_bytes + W.append_bytes(w, 1 if kv8 else None)
     seq_tokens = int(w.context_lens.astype(np.int64).sum())
     flush = None
@@ -421,6 +422,21 @@ def run_ours(args, rank, world, local):
     pa.profile_enable(False)
     kern_ms_total, kern_n = pa.profile_read()
     err = pa.get_device_error(clear=True)
+
+    # --- the append alone (the KV-append kernel), timed over the same number of calls
+    ap_n = max(1, min(args.steps, 500))
+    ap_s, ap_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    ap_s.record(stream)
+    for _ in range(ap_n):
+        if kv8:
+            pa.reshape_and_cache_fp8(nk, nv, kc, vc, sm, K_SCALE, V_SCALE, stream=stream)
+        else:
+            pa.reshape_and_cache(nk, nv, kc, vc, sm, stream=stream)
+    ap_e.record(stream)
+    torch.cuda.synchronize(dev)
+    append_ms = ap_s.elapsed_time(ap_e) / ap_n
+    append_bytes = W.append_bytes(w, 1 if kv8 else None)
 
     # --- end to end through the public API: host inputs in, host output back, every step
     # (query, new K/V rows, slot mapping, block tables and context lengths in one pinned buffer).
@@ -498,6 +514,10 @@ def run_ours(args, rank, world, local):
                    f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step vs 129 MB L2)",
                    "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
         "seq_tokens_per_s": total_tokens / (step_ms * 1e-3),
+        "query_tokens_per_s": sum_over_ranks(w.num_seqs * w.q_len, world, dev) / (step_ms * 1e-3),
+        "unique_attention_bytes": unique_bytes,
+        "append": {"us_per_call": append_ms * 1e3, "bytes": append_bytes,
+                   "gbs": append_bytes / (append_ms * 1e-3) / 1e9},
         "roofline": ({"bound": "tensor", "achieved": flops / (kern_ms * 1e-3) / 1e12, "peak": tpeak,
                       "unit": "TFLOP/s", "frac": flops / (kern_ms * 1e-3) / 1e12 / tpeak,
                       "peak_source": f"{tpeak_kind} dense bf16 cuBLAS burst", "flops_per_launch": flops,

@@ -337,6 +337,23 @@ def attention_bytes(w: Workload, kv_elem_bytes: Optional[int] = None) -> int:
     return kv + qo
 
 
+def unique_attention_bytes(w: Workload, kv_elem_bytes: Optional[int] = None) -> int:
+    """HBM bytes of one attention pass if every physical block were read once: blocks that
+    several sequences map (a shared prefix) count once, with the most rows any sequence uses
+    from them, plus Q read and O written.  Equals attention_bytes when nothing is shared."""
+    e = ELEM_BYTES[w.dtype]
+    kve = e if kv_elem_bytes is None else kv_elem_bytes
+    rows = {}
+    for i in range(w.num_seqs):
+        L = int(w.context_lens[i])
+        for b in range((L + w.block_size - 1) // w.block_size):
+            pb = int(w.block_tables[i, b])
+            rows[pb] = max(rows.get(pb, 0), min(w.block_size, L - w.block_size * b))
+    kv = sum(rows.values()) * kv_bytes_per_token(1, w.num_kv_heads, w.head_dim, kve)
+    qo = 2 * w.num_seqs * w.q_len * w.num_heads * w.head_dim * e
+    return kv + qo
+
+
 def attention_flops(w: Workload) -> int:
     """Algorithmic flops of one attention pass: for every query row and head, 2 d flops for the
     score and 2 d for the P.V term of each position the row attends (row j of a q-row chunk

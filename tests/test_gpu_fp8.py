@@ -84,3 +84,11 @@ def test_fp8_head_dim_64_is_unsupported():
     with pytest.raises(pa.PaError) as e:
         pa.decode_attention_fp8kv(torch.empty_like(q), q, kc, kc, bt, cl, 0.125, 64, ws, 1.0, 1.0)
     assert e.value.status == 2
+
+
+def test_fp8_chunk_row_groups():
+    """A 64-token chunk over FP8 caches: 256 query rows per kv head run as eight 32-row groups."""
+    w = W.make_workload("fp8chunk", [64, 300, 1100], num_heads=16, num_kv_heads=4, head_dim=128, dtype="bf16",
+                        q_len=64, num_blocks=110, seed=42)
+    got, ref = run_fp8(w)
+    G.compare(got, ref, w.dtype, "fp8 chunk")

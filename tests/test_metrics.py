@@ -45,3 +45,15 @@ def test_workloads_are_seeded_and_shaped():
     assert len(set(used.tolist())) == used.size and used.max() < 64
     # unused slots hold the NaN sentinel
     assert a.key_cache[a.block_tables[0, 0], 1, 0, 0] == W.NAN_BITS["bf16"]
+
+
+def test_unique_bytes_count_shared_blocks_once():
+    """Shared prefix: the 64 common blocks count once in the unique bytes; without sharing the
+    unique and logical bytes agree."""
+    w = W.shared_prefix_verify()
+    logical, unique = W.attention_bytes(w), W.unique_attention_bytes(w)
+    per_token = W.kv_bytes_per_token(1, w.num_kv_heads, w.head_dim, 2)
+    shared_rows = w.shared_prefix_blocks * w.block_size
+    assert logical - unique == (w.num_seqs - 1) * shared_rows * per_token
+    t = W.tiny_mha()
+    assert W.unique_attention_bytes(t) == W.attention_bytes(t)
