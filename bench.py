@@ -371,6 +371,7 @@ def run_ours(args, rank, world, local):
 
     for _ in range(max(3, args.warmup)):
         launches_per_step = step()
+    partition_used = pa.last_partition_size()
     torch.cuda.synchronize(dev)
 
     attn_bytes = W.attention_bytes(w, 1 if kv8 else None)
@@ -508,7 +509,7 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": DESCR[cfg], "seq_tokens_per_step": seq_tokens, "bytes_per_step": step_bytes,
-                   "attention_bytes": attn_bytes, "partition_tokens": None if tc_path else 512, "math": args.math,
+                   "attention_bytes": attn_bytes, "partition_tokens": partition_used or None, "math": args.math,
                    "kv_cache": args.kv,
                    "l2": "flushed between steps" if flush is not None else
                    f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step vs 129 MB L2)",

@@ -173,8 +173,9 @@ size_t pa_decode_workspace_size_ex(int num_seqs, int q_len, int num_heads, int h
  *   context_lens [num_seqs] int32, read; each in [1, max_context_len]
  *   max_context_len  an upper bound of every context_lens[i] (sizes the workspace)
  *   workspace    device scratch of at least pa_decode_workspace_size() bytes
- * Sequences longer than one partition are split into PA_DEFAULT_PARTITION-token
- * partitions whose fp32 partial results are merged by their log-sum-exp.
+ * Sequences longer than one partition are split into partitions (512-2048 tokens,
+ * chosen by the library; see pa_decode_attention_ex) whose fp32 partial results are
+ * merged by their log-sum-exp.
  * Sequences with invalid lengths leave their output rows unwritten and set
  * PA_DEVERR_CONTEXT.
  */
@@ -211,10 +212,14 @@ int pa_decode_attention_multiquery(void* out, const void* query, const void* key
 
 /*
  * General form of the two calls above with an explicit split-K partition size
- * (tokens, a positive multiple of 16; 0 = PA_DEFAULT_PARTITION).  A partition
- * size >= max_context_len computes every sequence in one piece (no merge).
- * The workspace must be sized with pa_decode_workspace_size_ex() for the same
- * partition size.  Results agree with the default within fp32 rounding.
+ * (tokens, a positive multiple of 16).  0 lets the library choose: 512, 1024 or
+ * 2048 tokens, the largest that still leaves about three work units per resident
+ * CTA when each sequence is taken as max_context_len / 2 long (fewer partials to
+ * merge, the hand-out still balanced); pa_last_partition_size() reports it.  A
+ * partition size >= max_context_len computes every sequence in one piece (no
+ * merge).  The workspace must be sized with pa_decode_workspace_size_ex() for the
+ * same partition size (0: PA_DEFAULT_PARTITION, which covers every choice).
+ * Results agree across partition sizes within fp32 rounding.
  */
 int pa_decode_attention_ex(void* out, const void* query, const void* key_cache, const void* value_cache,
                            const int32_t* block_tables, int max_blocks_per_seq,
@@ -325,6 +330,12 @@ int pa_set_decode_math(int math);
  */
 int pa_profile_enable(int on);
 int pa_profile_read(float* total_ms, int* launches);
+
+/*
+ * Split-K partition (tokens) the last decode call on this thread used: the caller's size,
+ * the library's choice when it passed 0, or 0 when the tcgen05 kernel ran without splitting.
+ */
+int pa_last_partition_size(void);
 
 /* Number of kernel launches the last decode call on this thread enqueued. */
 int pa_last_launch_count(void);

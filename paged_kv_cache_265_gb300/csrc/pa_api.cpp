@@ -11,6 +11,7 @@
 namespace {
 
 thread_local int t_last_launches = 0;
+thread_local int t_last_partition = 0;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -58,6 +59,8 @@ const char* pa_status_string(int status) {
 }
 
 int pa_last_launch_count(void) { return t_last_launches; }
+
+int pa_last_partition_size(void) { return t_last_partition; }
 
 int pa_reshape_and_cache(const void* key, const void* value, void* key_cache, void* value_cache,
                          const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads, int head_dim,
@@ -163,9 +166,10 @@ int pa_decode_attention_ex(void* out, const void* query, const void* key_cache, 
     a.partition = partition;
     a.partition_auto = partition_size == 0;
     a.workspace = workspace;
-    int launches = 0;
-    const int rc = pa::launch_decode(a, static_cast<cudaStream_t>(stream), &launches);
+    int launches = 0, part = 0;
+    const int rc = pa::launch_decode(a, static_cast<cudaStream_t>(stream), &launches, &part);
     t_last_launches = launches;
+    t_last_partition = part;
     return rc;
 }
 
@@ -231,9 +235,10 @@ int pa_decode_attention_fp8kv(void* out, const void* query, const void* key_cach
     a.fp8 = true;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
-    int launches = 0;
-    const int rc = pa::launch_decode(a, static_cast<cudaStream_t>(stream), &launches);
+    int launches = 0, part = 0;
+    const int rc = pa::launch_decode(a, static_cast<cudaStream_t>(stream), &launches, &part);
     t_last_launches = launches;
+    t_last_partition = part;
     return rc;
 }
 

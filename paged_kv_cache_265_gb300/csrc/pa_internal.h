@@ -82,7 +82,8 @@ struct DecodeArgs {
 int launch_reshape_and_cache(const void* key, const void* value, void* key_cache, void* value_cache,
                              const int64_t* slot_mapping, int64_t num_tokens, int row_bytes,
                              int64_t num_slots, cudaStream_t stream, int* launches);
-int launch_decode(const DecodeArgs& a, cudaStream_t stream, int* launches);
+// `partition_used` receives the split-K partition in tokens (0: the tcgen05 kernel, no split).
+int launch_decode(const DecodeArgs& a, cudaStream_t stream, int* launches, int* partition_used);
 // Chunked-prefill attention on tcgen05 (pa_prefill.cu); launch_decode routes calls to it.
 int launch_prefill_tc(const DecodeArgs& a, cudaStream_t stream, int* launches);
 int launch_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* target_probs,

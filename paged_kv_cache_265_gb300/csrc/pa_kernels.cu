@@ -1523,6 +1523,45 @@ int make_kv_map_fp8(CUtensorMap* map, const void* base, int64_t num_blocks, int 
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_INVALID_ARG;
 }
 
+// Consumer arithmetic of the decode kernel for `rows` query rows per work unit: rt > 0 picks the
+// CUDA-core path for up to rt rows, else tensor-core tiles with warps of 8 * nt rows.
+// Measured on GB300 (partition kernel, CUDA events): with one query row per kv head both paths
+// stream at the same rate (MHA workload 6.33 vs 6.35 TB/s), so that case stays on CUDA-core FMA;
+// with grouped heads the tensor-core tiles win (4 rows: 5.99 vs 3.79 TB/s, 8 rows: 5.88 vs
+// 1.91 TB/s).
+void decode_variant(int rows, bool fp8, int& rt, int& nt) {
+    rt = 0;
+    if (g_decode_math == 1 && rows <= 8) rt = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+    if (g_decode_math == 0 && rows == 1) rt = 1;
+    if (fp8) rt = 0;  // FP8 caches are read on the tensor-core path
+    nt = (rows <= 8 || (PA_PREFER_NT1 && rows <= 32)) ? 1 : 2;
+}
+
+// Split-K partition when the caller leaves it to the library: the largest of 512, 1024 and 2048
+// tokens that still gives about three work units per resident CTA, counting each sequence as
+// max_context_len / 2 positions long.  Larger partitions leave fewer fp32 partials to merge;
+// the largest-first hand-out keeps the tail short while units are plentiful.  Measured on GB300
+// (call time): GQA batch of 128, 512 / 1024 / 2048 tokens: 181.7 / 177.6 / - us; long context
+// (16 sequences of 16-32K + 240 short): 408.6 / 376.5 / 357.3 us (4096: 397.9); OPT-13B-shaped
+// MHA: 156.2 / 158.7 / 182.4 us; 32 GQA sequences: 68.1 / 68.3 / 92.2 us.
+int auto_partition(const DecodeArgs& a, int sms) {
+    if (a.fp8) return PA_DEFAULT_PARTITION;
+    const int group = a.num_heads / a.num_kv_heads;
+    const long long total_rows = (long long)group * a.q_len;
+    const int rows = (int)std::min<long long>(PA_ROW_GROUP_ROWS, total_rows);
+    const long long row_groups = (total_rows + rows - 1) / rows;
+    int rt, nt;
+    decode_variant(rows, a.fp8, rt, nt);
+    const long long slots = (long long)sms * decode_ctas_per_sm(nt, rt, a.fp8);
+    const long long half = std::max(1, a.max_context_len / 2);
+    int best = PA_DEFAULT_PARTITION;
+    for (int part = 2 * PA_DEFAULT_PARTITION; part <= 4 * PA_DEFAULT_PARTITION; part *= 2) {
+        const long long units = (long long)a.num_seqs * a.num_kv_heads * row_groups * ((half + part - 1) / part);
+        if (units >= 3 * slots) best = part;
+    }
+    return best;
+}
+
 template <typename T, int D>
 int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches) {
     const WsLayout w = ws_layout(a.num_seqs, a.q_len, a.num_heads, D, a.max_context_len, a.partition);
@@ -1584,15 +1623,8 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     // tiles per kv head are rounded up to a divisor of the consumer warp count (a third
     // tile becomes a fourth, all-padding one) so that every consumer warp owns exactly one
     // (row tile, block split) pair.
-    // Consumer arithmetic.  Measured on GB300 (partition kernel, CUDA events): with one query
-    // row per kv head both paths stream at the same rate (MHA workload 6.33 vs 6.35 TB/s), so
-    // that case stays on CUDA-core FMA; with grouped heads the tensor-core tiles win
-    // (4 rows: 5.99 vs 3.79 TB/s, 8 rows: 5.88 vs 1.91 TB/s).
-    int rt = 0;
-    if (g_decode_math == 1 && p.rows <= 8) rt = p.rows <= 1 ? 1 : p.rows <= 2 ? 2 : p.rows <= 4 ? 4 : 8;
-    if (g_decode_math == 0 && p.rows == 1) rt = 1;
-    if (a.fp8) rt = 0;  // FP8 caches are read on the tensor-core path
-    const int nt = (p.rows <= 8 || (PA_PREFER_NT1 && p.rows <= 32)) ? 1 : 2;
+    int rt, nt;
+    decode_variant(p.rows, a.fp8, rt, nt);
     const int tile_rows = 8 * nt;
     p.mtiles = (p.rows + tile_rows - 1) / tile_rows;
     if (p.mtiles == 3) p.mtiles = 4;
@@ -1801,8 +1833,16 @@ bool use_prefill_tc(const DecodeArgs& a) {
     return g_decode_math == 0 && a.partition_auto && rows >= PA_TC_MIN_ROWS;
 }
 
-int launch_decode(const DecodeArgs& a, cudaStream_t stream, int* launches) {
-    if (use_prefill_tc(a)) return launch_prefill_tc(a, stream, launches);
+int launch_decode(const DecodeArgs& args, cudaStream_t stream, int* launches, int* partition_used) {
+    *partition_used = 0;
+    if (use_prefill_tc(args)) return launch_prefill_tc(args, stream, launches);  // no split
+    DecodeArgs a = args;
+    if (a.partition_auto) {
+        DeviceInfo dev;
+        if (int st = device_info(dev)) return st;
+        a.partition = auto_partition(a, dev.sms);  // >= the default, so the workspace suffices
+    }
+    *partition_used = a.partition;
     if (a.dtype == PA_BF16) {
         if (a.head_dim == 128) return launch_decode_typed<__nv_bfloat16, 128>(a, stream, launches);
         if (a.head_dim == 64) return launch_decode_typed<__nv_bfloat16, 64>(a, stream, launches);

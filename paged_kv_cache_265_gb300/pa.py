@@ -54,6 +54,7 @@ _SIGS = {
     "pa_profile_enable": (_c_int, [_c_int]),
     "pa_profile_read": (_c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
     "pa_last_launch_count": (_c_int, []),
+    "pa_last_partition_size": (_c_int, []),
     "pa_version": (_c_int, []),
 }
 
@@ -300,6 +301,12 @@ def set_decode_math(math: str) -> None:
     'tcgen05': the tcgen05 prefill kernel for every 16-bit call.  Process-wide."""
     _check("pa_set_decode_math",
            lib().pa_set_decode_math({"auto": 0, "fma": 1, "tensor": 2, "tcgen05": 3}[math]))
+
+
+def last_partition_size() -> int:
+    """Split-K partition (tokens) of this thread's last decode call; 0 if it ran the tcgen05
+    kernel without splitting."""
+    return int(lib().pa_last_partition_size())
 
 
 def profile_enable(on: bool = True) -> None:

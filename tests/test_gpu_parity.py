@@ -212,6 +212,22 @@ def test_launch_counts():
                             num_blocks=40, seed=31)
     G.GpuStep(chunk).attend()
     assert pa.last_launch_count() == 1
+    assert pa.last_partition_size() == 0          # no split on the tcgen05 kernel
+
+
+def test_partition_choice():
+    """A forced partition is used as given; partition 0 lets the library pick 512, 1024 or 2048
+    tokens (more units per resident CTA -> larger partitions); every choice reaches the oracle."""
+    w = named(3)                                  # 128 sequences up to 4096 positions
+    step = G.GpuStep(w, partition_size=256)
+    step.attend()
+    assert pa.last_partition_size() == 256
+    auto = G.GpuStep(w)
+    got = auto.run()
+    assert pa.last_partition_size() in (512, 1024, 2048)
+    _, _, ref = G.oracle_step(w)
+    G.compare(got, ref, w.dtype, f"{w.name} auto partition {pa.last_partition_size()}")
+    assert G.ulps_from_rounded_oracle(got, ref, w.dtype) <= 1
 
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 5])
