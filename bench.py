@@ -146,6 +146,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.out = None
+        self.first = ""
 
     def __enter__(self):
         try:
@@ -154,7 +155,16 @@ class ClockSampler:
                  "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
-        time.sleep(0.3)
+        self.first = ""
+        if self.proc is not None:
+            # Start the timed region only once nvidia-smi delivers samples: its start-up competes
+            # for the CPU that launches the (short) steps.
+            import select
+
+            ready, _, _ = select.select([self.proc.stdout], [], [], 5.0)
+            if ready:
+                self.first = self.proc.stdout.readline()
+        time.sleep(0.1)
         return self
 
     def __exit__(self, *exc):
@@ -168,6 +178,7 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
 
     def summary(self):
+        self.out = (self.first or "") + (self.out or "")
         if not self.out:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 8]
@@ -382,29 +393,36 @@ def run_ours(args, rank, world, local):
     if step_bytes < 2 * L2_BYTES:   # small working set: flush L2 between steps
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
 
-    # --- device-resident timed region (the hot path exactly as a caller runs it)
+    # --- device-resident timed region (the hot path exactly as a caller runs it).  Each L2 flush
+    # is bracketed by its own event pair and its time taken out (a flush costs differently when
+    # it runs between steps than when flushes run back to back).
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    flush_ms = 0.0
+
+    def flushed():
+        """Runs the L2 flush; returns its (start, stop) events when timed."""
+        if flush is None:
+            return None
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        flush.zero_()
+        b.record(stream)
+        return a, b
+
+    flush_events = []
     with ClockSampler(local) as clocks:
         barrier(world)
         torch.cuda.synchronize(dev)
         start.record(stream)
         for _ in range(args.steps):
-            if flush is not None:
-                flush.zero_()
+            ev = flushed()
+            if ev:
+                flush_events.append(ev)
             step()
         stop.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
     total_ms = start.elapsed_time(stop)
-    if flush is not None:
-        fs, fe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        fs.record(stream)
-        for _ in range(args.steps):
-            flush.zero_()
-        fe.record(stream)
-        torch.cuda.synchronize(dev)
-        flush_ms = fs.elapsed_time(fe)
+    flush_ms = sum(a.elapsed_time(b) for a, b in flush_events)
     step_ms_local = max(1e-9, (total_ms - flush_ms) / args.steps)
     step_ms = max_over_ranks(step_ms_local, world, dev)
 
@@ -416,8 +434,7 @@ def run_ours(args, rank, world, local):
     pa.profile_enable(True)
     pa.profile_read()
     for _ in range(prof_steps):
-        if flush is not None:
-            flush.zero_()
+        flushed()
         step()
     torch.cuda.synchronize(dev)
     pa.profile_enable(False)
@@ -466,8 +483,9 @@ def run_ours(args, rank, world, local):
                     stagings[b ^ 1].upload()
                     ev_up[b ^ 1].record(copy_stream)
             stream.wait_event(ev_up[b])
-            if flush is not None:
-                flush.zero_()
+            ev = flushed()
+            if ev:
+                e2e_flush.append(ev)
             step(stagings[b].views, outs[b])
             ev_done[b].record(stream)
             with torch.cuda.stream(copy_stream):
@@ -475,8 +493,10 @@ def run_ours(args, rank, world, local):
                 h_out.copy_(outs[b], non_blocking=True)
         stream.wait_stream(copy_stream)
 
+    e2e_flush = []
     e2e_run(3)
     torch.cuda.synchronize(dev)
+    e2e_flush.clear()
     es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -485,8 +505,8 @@ def run_ours(args, rank, world, local):
     e2e_run(e2e_steps)
     ee.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks((es.elapsed_time(ee) - flush_ms * e2e_steps / max(1, args.steps)) / e2e_steps,
-                            world, dev)
+    e2e_flush_ms = sum(a.elapsed_time(b) for a, b in e2e_flush)
+    e2e_ms = max_over_ranks((es.elapsed_time(ee) - e2e_flush_ms) / e2e_steps, world, dev)
 
     total_bytes = sum_over_ranks(step_bytes, world, dev)
     total_tokens = sum_over_ranks(seq_tokens, world, dev)
