@@ -264,8 +264,31 @@ def oracle_time(w: W.Workload, seq_idx: np.ndarray, threads: int, pools=None):
     return dt, nbytes, int(sub.context_lens.astype(np.int64).sum())
 
 
-def cpu_baseline(w: W.Workload, budget_s: float = 12.0):
-    """The oracle as it stands on all host cores, on a bounded sample of the workload."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    import subprocess
+
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
+def cpu_baseline(w: W.Workload, budget_s: float = 12.0, single_s: float = 3.0):
+    """The oracle as it stands on all host cores, on a bounded sample of the workload; plus the
+    same oracle on one core over a smaller sample."""
     import oracle
 
     threads = oracle.load().max_threads()
@@ -285,9 +308,20 @@ def cpu_baseline(w: W.Workload, budget_s: float = 12.0):
         tot_t += dt
         tot_b += nbytes
         tot_tok += toks
+    # one core: whole sequences in batch order (cycling) until single_s seconds are spent
+    k1, t1, b1, tok1 = 0, 0.0, 0, 0
+    while t1 < single_s:
+        i = k1 % n
+        dt, nbytes, toks = oracle_time(w, np.arange(i, i + 1), 1, pools)
+        k1 += 1
+        t1 += dt
+        b1 += nbytes
+        tok1 += toks
     return {"value": tot_b / tot_t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "seq_tokens_per_s": tot_tok / tot_t,
-            "sample": f"first {k} of {n} sequences (append + attention), {reps} repetitions, {tot_t:.1f} s"}
+            "seq_tokens_per_s": tot_tok / tot_t, "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+            "sample": f"first {k} of {n} sequences (append + attention), {reps} repetitions, {tot_t:.1f} s",
+            "single_core": {"value": b1 / t1 / 1e9, "unit": "GB/s", "seq_tokens_per_s": tok1 / t1,
+                            "sample": f"{k1} sequence runs in batch order, {t1:.1f} s"}}
 
 
 def run_reference(args, rank, world):
