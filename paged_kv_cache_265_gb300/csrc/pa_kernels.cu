@@ -413,9 +413,12 @@ __device__ int block_exclusive_scan(int v, int* scratch32, int& total) {
     return before + x - v;
 }
 
-__device__ __forceinline__ int seq_parts(const PlanParams& p, int i) {
+// Partitions of sequence i (0 past the batch or for an invalid length, which is flagged);
+// its context length goes to L.
+__device__ __forceinline__ int seq_parts(const PlanParams& p, int i, int& L) {
+    L = 0;
     if (i >= p.num_seqs) return 0;
-    const int L = p.context_lens[i];
+    L = p.context_lens[i];
     const bool ok = L >= 1 && L >= p.q_len && L <= p.max_context_len &&
                     (L + kBlock - 1) / kBlock <= p.max_blocks_per_seq;
     if (!ok) {
@@ -439,41 +442,61 @@ __device__ __forceinline__ int part_bucket(const PlanParams& p, int L, int part)
 __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
     griddep_launch_dependents();  // the partition pass may start its set-up now ...
     griddep_wait();               // ... but the lengths may come from the kernel before this one
+    static_assert(kPlanBuckets == 64, "the bucket scan below gives each lane of one warp two buckets");
     __shared__ int scratch[32];
     __shared__ int hist[kPlanBuckets];
     if (threadIdx.x < kPlanBuckets) hist[threadIdx.x] = 0;
     __syncthreads();
-    int carry = 0;
+    // Each thread keeps its first sequence (all of them, up to 1024 sequences) in registers
+    // for the second pass.
+    int carry = 0, L0 = 0, np0 = 0, slot0 = 0;
     for (int base = 0; base < p.num_seqs; base += 1024) {
         const int i = base + threadIdx.x;
-        const int np = seq_parts(p, i);
+        int L;
+        const int np = seq_parts(p, i, L);
         int tot;
         const int slot = carry + block_exclusive_scan(np, scratch, tot);
         if (i < p.num_seqs) {
             p.part_start[i] = slot;
-            const int L = p.context_lens[i];
             for (int c = 0; c < np; ++c) atomicAdd(&hist[part_bucket(p, L, c)], 1);
+        }
+        if (base == 0) {
+            L0 = L;
+            np0 = np;
+            slot0 = slot;
         }
         carry += tot;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;  // bucket starts, largest bucket first
-        for (int b = kPlanBuckets - 1; b >= 0; --b) {
-            const int n = hist[b];
-            hist[b] = run;
-            run += n;
+    if (threadIdx.x < 32) {
+        // Bucket starts, largest bucket first: an exclusive scan over the buckets in descending
+        // order, lane l taking buckets 63 - 2l and 62 - 2l.
+        const int lane = threadIdx.x;
+        const int b0 = kPlanBuckets - 1 - 2 * lane, b1 = b0 - 1;
+        const int n0 = hist[b0], n1 = hist[b1];
+        int x = n0 + n1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
         }
-        p.part_start[p.num_seqs] = carry;
-        p.header[0] = carry;
-        p.header[1] = 0;
+        const int start = x - (n0 + n1);
+        hist[b0] = start;
+        hist[b1] = start + n0;
+        if (lane == 0) {
+            p.part_start[p.num_seqs] = carry;
+            p.header[0] = carry;
+            p.header[1] = 0;
+        }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) {
-        const int np = seq_parts(p, i);
+        int L = L0, np = np0, slot = slot0;
+        if (i >= 1024) {
+            np = seq_parts(p, i, L);
+            slot = p.part_start[i];
+        }
         if (np == 0) continue;
-        const int L = p.context_lens[i];
-        const int slot = p.part_start[i];
         for (int c = 0; c < np; ++c) {
             const int pos = atomicAdd(&hist[part_bucket(p, L, c)], 1);
             p.units[pos] = make_int4(i, c, L, slot);
@@ -1348,16 +1371,21 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
     const int seq = (int)(row / per_seq);
     const int rem = (int)(row - (long long)seq * per_seq);
     const int L = p.context_lens[seq];
+    const long long slot0 = p.part_start[seq];  // loaded with L, not after it
     if (L < 1 || L < p.q_len || L > p.max_context_len) return;
     const int nparts = (L + p.partition - 1) / p.partition;
     if (nparts <= 1) return;
-    const long long slot0 = p.part_start[seq];
-    float M = -INFINITY;
-    for (int i = lane; i < nparts; i += 32) M = fmaxf(M, p.pml[(slot0 + i) * per_seq + rem].x);
+    // Lane l keeps the (max, sum) pairs of partitions l and l + 32; any further ones are re-read.
+    const float2 ml0 = lane < nparts ? p.pml[(slot0 + lane) * per_seq + rem] : make_float2(-INFINITY, 0.f);
+    const float2 ml1 = lane + 32 < nparts ? p.pml[(slot0 + lane + 32) * per_seq + rem] : make_float2(-INFINITY, 0.f);
+    float M = fmaxf(ml0.x, ml1.x);
+    for (int i = lane + 64; i < nparts; i += 32) M = fmaxf(M, p.pml[(slot0 + i) * per_seq + rem].x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float lsum = 0.f;
-    for (int i = lane; i < nparts; i += 32) {
+    if (lane < nparts) lsum += ml0.y * ex2(ml0.x - M);
+    if (lane + 32 < nparts) lsum += ml1.y * ex2(ml1.x - M);
+    for (int i = lane + 64; i < nparts; i += 32) {
         const float2 ml = p.pml[(slot0 + i) * per_seq + rem];
         lsum += ml.y * ex2(ml.x - M);
     }
@@ -1369,7 +1397,9 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
     for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
     for (int base = 0; base < nparts; base += 32) {
         const int mine = base + lane;
-        const float f_mine = mine < nparts ? ex2(p.pml[(slot0 + mine) * per_seq + rem].x - M) * inv : 0.f;
+        const float m_mine = base == 0 ? ml0.x : base == 32 ? ml1.x
+                                                             : (mine < nparts ? p.pml[(slot0 + mine) * per_seq + rem].x : 0.f);
+        const float f_mine = mine < nparts ? ex2(m_mine - M) * inv : 0.f;
         const int cnt = min(32, nparts - base);
 #pragma unroll 8
         for (int j = 0; j < cnt; ++j) {
