@@ -235,6 +235,8 @@ constexpr int kSpecMaxChunks = 64;            // vocabulary up to 262,144
 struct DrawSmem {
     unsigned long long red[kSpecThreads / 32][kSpecMaxChunks];
     unsigned long long chunk_prefix[kSpecMaxChunks + 1];
+    unsigned long long thresh;                    // the draw's threshold (a slot of its own: with 64
+                                                  // chunks every prefix slot is in use)
     unsigned long long scan[kSpecThreads / 32];
     int tok;
     int chunk;
@@ -279,7 +281,7 @@ __device__ int block_draw(const float* a, const float* b, int vocab, float u, Dr
         if (total) {
             const unsigned long long u24 = fixed_from_float(u, 24);
             const unsigned long long thresh = (__umul64hi(u24, total) << 40) | ((u24 * total) >> 24);
-            sm.chunk_prefix[kSpecMaxChunks] = thresh;
+            sm.thresh = thresh;
             for (int j = 0; j < chunks; ++j)
                 if (sm.chunk_prefix[j + 1] > thresh) {
                     sm.chunk = j;
@@ -290,7 +292,7 @@ __device__ int block_draw(const float* a, const float* b, int vocab, float u, Dr
     __syncthreads();
     const int j = sm.chunk;
     if (j >= 0) {
-        const unsigned long long thresh = sm.chunk_prefix[kSpecMaxChunks];
+        const unsigned long long thresh = sm.thresh;
         unsigned long long base = sm.chunk_prefix[j];
         for (int c = 0; c < 4; ++c) {
             const int v = j * kSpecChunk + c * kSpecThreads + t;

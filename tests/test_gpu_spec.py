@@ -61,3 +61,13 @@ def test_spec_verify_bad_draft_token_is_flagged():
     torch.cuda.synchronize()
     assert pa.get_device_error(clear=True) & pa.PA_DEVERR_TOKEN
     assert acc[2].item() <= 1
+
+
+def test_spec_verify_largest_vocabulary_last_chunk():
+    """The largest vocabulary (64 chunks of 4096 entries, split over the cluster's CTAs) with
+    uniforms that put every draw in the last chunk."""
+    x = W.spec_verify_inputs(num_seqs=8, k=2, vocab=262144, seed=9)
+    x.u_sample[:] = np.float32(0.999999)
+    acc, out, ra, ro = run_both(x)
+    assert np.array_equal(acc, ra) and np.array_equal(out, ro)
+    assert np.all(out[np.arange(8), acc] >= 262144 - 4096)
