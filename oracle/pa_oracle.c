@@ -238,7 +238,12 @@ int oracle_reshape_and_cache(const uint16_t* key, const uint16_t* value,
         int64_t slot = slot_mapping[t];
         if (slot < 0) continue;                              /* padding token: nothing to write */
         if (slot >= num_blocks * block_size) { ++bad; continue; }
+#if PLANT == 14
+        int64_t blk = slot % block_size, off = slot / block_size;   /* planted: block and offset swapped */
+        if (blk >= num_blocks || off >= block_size) { ++bad; continue; }
+#else
         int64_t blk = slot / block_size, off = slot % block_size;
+#endif
         uint16_t* kd = key_cache + (blk * block_size + off) * row;
         uint16_t* vd = value_cache + (blk * block_size + off) * row;
         memcpy(kd, key + t * row, sizeof(uint16_t) * row);
@@ -265,6 +270,9 @@ int oracle_copy_blocks(uint16_t* key_cache, uint16_t* value_cache, const int64_t
     for (int64_t i = 0; i < num_pairs; ++i) {
         int64_t src = block_mapping[2 * i], dst = block_mapping[2 * i + 1];
         if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) { ++bad; continue; }
+#if PLANT == 12
+        int64_t tmp = src; src = dst; dst = tmp;                   /* planted: copied the wrong way */
+#endif
         memmove(key_cache + dst * blk, key_cache + src * blk, sizeof(uint16_t) * blk);
         memmove(value_cache + dst * blk, value_cache + src * blk, sizeof(uint16_t) * blk);
     }
@@ -388,7 +396,11 @@ uint8_t oracle_e4m3_encode(float v)
     int E;
     frexp(a, &E);                                             /* a = f * 2^E, f in [0.5, 1) */
     int e = E - 1;                                            /* a in [2^e, 2^(e+1)) */
+#if PLANT == 11
+    double r = floor((a / ldexp(1.0, e) - 1.0) * 8.0);         /* planted: truncation, not round-to-even */
+#else
     double r = round_half_even((a / ldexp(1.0, e) - 1.0) * 8.0);
+#endif
     if (r == 8.0) { e += 1; r = 0.0; }
     return sign | (uint8_t)((e + 7) << 3) | (uint8_t)r;
 }
@@ -399,7 +411,11 @@ double oracle_e4m3_decode(uint8_t b)
     double v;
     if (field == 15 && mant == 7) return NAN;
     if (field == 0) v = ldexp((double)mant, -9);
+#if PLANT == 10
+    else v = ldexp(1.0 + mant / 8.0, field - 8);               /* planted: exponent bias 8 */
+#else
     else v = ldexp(1.0 + mant / 8.0, field - 7);
+#endif
     return sign ? -v : v;
 }
 
@@ -472,8 +488,13 @@ int oracle_decode_attention_fp8(double* out, const uint16_t* query, const uint8_
                 if (blk < 0 || (int64_t)blk >= num_blocks) { ok = 0; break; }
                 const int64_t base = ((int64_t)blk * block_size + p % block_size) * row;
                 for (int64_t e = 0; e < row; ++e) {
+#if PLANT == 13
+                    K[(int64_t)p * row + e] = oracle_e4m3_decode(key_cache[base + e]) * (double)v_scale;  /* planted */
+                    V[(int64_t)p * row + e] = oracle_e4m3_decode(value_cache[base + e]) * (double)k_scale;
+#else
                     K[(int64_t)p * row + e] = oracle_e4m3_decode(key_cache[base + e]) * (double)k_scale;
                     V[(int64_t)p * row + e] = oracle_e4m3_decode(value_cache[base + e]) * (double)v_scale;
+#endif
                 }
             }
         }
