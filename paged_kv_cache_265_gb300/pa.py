@@ -8,6 +8,7 @@ back to anything else.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -97,6 +98,24 @@ def _stream(stream) -> int:
     return int(stream.cuda_stream)
 
 
+@contextlib.contextmanager
+def _device_of(*tensors, stream=None):
+    """Run a library call with the CUDA device of its tensors current: the library launches on
+    the current device, so every tensor (and an explicit stream) must be on that one device."""
+    devs = set()
+    for t in tensors:
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError("arguments must be CUDA tensors")
+        devs.add(t.device)
+    if len(devs) != 1:
+        raise ValueError(f"all tensors must be on one CUDA device (got {sorted(str(d) for d in devs)})")
+    dev = devs.pop()
+    if stream is not None and getattr(stream, "device", dev) != dev:
+        raise ValueError(f"the stream is on {stream.device}, the tensors on {dev}")
+    with torch.cuda.device(dev):
+        yield
+
+
 def _dev(t: torch.Tensor, name: str) -> int:
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
@@ -121,10 +140,11 @@ def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.T
         raise ValueError("slot_mapping must be int64")
     if key.dtype != key_cache.dtype or value.dtype != key_cache.dtype or value_cache.dtype != key_cache.dtype:
         raise ValueError("key, value and the caches must share one dtype")
-    st = lib().pa_reshape_and_cache(
-        _dev(key, "key"), _dev(value, "value"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
-        _dev(slot_mapping, "slot_mapping"), slot_mapping.shape[0], hkv, d, bs, nb, dtype_code(key_cache),
-        _stream(stream))
+    with _device_of(key, value, key_cache, value_cache, slot_mapping, stream=stream):
+        st = lib().pa_reshape_and_cache(
+            _dev(key, "key"), _dev(value, "value"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+            _dev(slot_mapping, "slot_mapping"), slot_mapping.shape[0], hkv, d, bs, nb, dtype_code(key_cache),
+            _stream(stream))
     _check("pa_reshape_and_cache", st)
 
 
@@ -137,9 +157,10 @@ def copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, block_mappin
         raise ValueError("key_cache and value_cache must match")
     if block_mapping.dtype != torch.int64 or block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
         raise ValueError("block_mapping must be int64 [num_pairs, 2]")
-    st = lib().pa_copy_blocks(_dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
-                              _dev(block_mapping, "block_mapping"), block_mapping.shape[0], hkv, d, bs, nb,
-                              dtype_code(key_cache), _stream(stream))
+    with _device_of(key_cache, value_cache, block_mapping, stream=stream):
+        st = lib().pa_copy_blocks(_dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+                                  _dev(block_mapping, "block_mapping"), block_mapping.shape[0], hkv, d, bs, nb,
+                                  dtype_code(key_cache), _stream(stream))
     _check("pa_copy_blocks", st)
 
 
@@ -161,10 +182,11 @@ def spec_verify(target_probs: torch.Tensor, draft_probs: torch.Tensor, draft_tok
         num_accepted = torch.empty(n, dtype=torch.int32, device=target_probs.device)
     if out_tokens is None:
         out_tokens = torch.empty((n, k1), dtype=torch.int32, device=target_probs.device)
-    st = lib().pa_spec_verify(_dev(num_accepted, "num_accepted"), _dev(out_tokens, "out_tokens"),
-                              _dev(target_probs, "target_probs"), _dev(draft_probs, "draft_probs"),
-                              _dev(draft_tokens, "draft_tokens"), _dev(u_accept, "u_accept"),
-                              _dev(u_sample, "u_sample"), n, k, v, _stream(stream))
+    with _device_of(num_accepted, out_tokens, target_probs, draft_probs, draft_tokens, u_accept, u_sample, stream=stream):
+        st = lib().pa_spec_verify(_dev(num_accepted, "num_accepted"), _dev(out_tokens, "out_tokens"),
+                                  _dev(target_probs, "target_probs"), _dev(draft_probs, "draft_probs"),
+                                  _dev(draft_tokens, "draft_tokens"), _dev(u_accept, "u_accept"),
+                                  _dev(u_sample, "u_sample"), n, k, v, _stream(stream))
     _check("pa_spec_verify", st)
     return num_accepted, out_tokens
 
@@ -178,10 +200,11 @@ def reshape_and_cache_fp8(key: torch.Tensor, value: torch.Tensor, key_cache: tor
         raise ValueError("FP8 caches must be uint8 tensors of one shape")
     if key.shape != (slot_mapping.shape[0], hkv, d) or value.shape != key.shape or slot_mapping.dtype != torch.int64:
         raise ValueError("key/value must be [num_tokens, num_kv_heads, head_dim]; slot_mapping int64")
-    st = lib().pa_reshape_and_cache_fp8(
-        _dev(key, "key"), _dev(value, "value"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
-        _dev(slot_mapping, "slot_mapping"), slot_mapping.shape[0], hkv, d, bs, nb, dtype_code(key), float(k_scale),
-        float(v_scale), _stream(stream))
+    with _device_of(key, value, key_cache, value_cache, slot_mapping, stream=stream):
+        st = lib().pa_reshape_and_cache_fp8(
+            _dev(key, "key"), _dev(value, "value"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+            _dev(slot_mapping, "slot_mapping"), slot_mapping.shape[0], hkv, d, bs, nb, dtype_code(key), float(k_scale),
+            float(v_scale), _stream(stream))
     _check("pa_reshape_and_cache_fp8", st)
 
 
@@ -200,12 +223,13 @@ def decode_attention_fp8kv(out: torch.Tensor, query: torch.Tensor, key_cache: to
         raise ValueError("FP8 caches must be uint8 with the query's head_dim")
     if out.shape != query.shape or out.dtype != query.dtype:
         raise ValueError("out must match query")
-    st = lib().pa_decode_attention_fp8kv(
-        _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
-        _dev(block_tables, "block_tables"), block_tables.shape[1], _dev(context_lens, "context_lens"), n, q_len, hq,
-        hkv, d, bs, nb, int(max_context_len), float(scale), dtype_code(query), float(k_scale), float(v_scale),
-        int(partition_size), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-        _stream(stream))
+    with _device_of(out, query, key_cache, value_cache, block_tables, context_lens, workspace, stream=stream):
+        st = lib().pa_decode_attention_fp8kv(
+            _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+            _dev(block_tables, "block_tables"), block_tables.shape[1], _dev(context_lens, "context_lens"), n, q_len, hq,
+            hkv, d, bs, nb, int(max_context_len), float(scale), dtype_code(query), float(k_scale), float(v_scale),
+            int(partition_size), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+            _stream(stream))
     _check("pa_decode_attention_fp8kv", st)
     return out
 
@@ -245,11 +269,12 @@ def decode_attention(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Te
         raise ValueError("block_tables and context_lens must be int32")
     if block_tables.dim() != 2 or block_tables.shape[0] != n or context_lens.shape != (n,):
         raise ValueError("block_tables must be [N, max_blocks] and context_lens [N]")
-    st = lib().pa_decode_attention_ex(
-        _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
-        _dev(block_tables, "block_tables"), block_tables.shape[1], _dev(context_lens, "context_lens"), n, q_len,
-        hq, hkv, d, bs, nb, int(max_context_len), float(scale), dtype_code(query), int(partition_size),
-        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream))
+    with _device_of(out, query, key_cache, value_cache, block_tables, context_lens, workspace, stream=stream):
+        st = lib().pa_decode_attention_ex(
+            _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+            _dev(block_tables, "block_tables"), block_tables.shape[1], _dev(context_lens, "context_lens"), n, q_len,
+            hq, hkv, d, bs, nb, int(max_context_len), float(scale), dtype_code(query), int(partition_size),
+            _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream))
     _check("pa_decode_attention_ex", st)
     return out
 
@@ -279,11 +304,12 @@ def decode_attention_noalloc(out: torch.Tensor, query: torch.Tensor, key_cache: 
         raise ValueError("block_tables and context_lens must be int32")
     if block_tables.dim() != 2 or block_tables.shape[0] != n or context_lens.shape != (n,):
         raise ValueError("block_tables must be [N, max_blocks] and context_lens [N]")
-    st = lib().pa_decode_attention_noalloc(
-        _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
-        _dev(block_tables, "block_tables"), block_tables.shape[1], _dev(context_lens, "context_lens"), n, q_len,
-        hq, hkv, d, bs, nb, int(max_context_len), float(scale), dtype_code(query), int(partition_size),
-        _stream(stream))
+    with _device_of(out, query, key_cache, value_cache, block_tables, context_lens, stream=stream):
+        st = lib().pa_decode_attention_noalloc(
+            _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+            _dev(block_tables, "block_tables"), block_tables.shape[1], _dev(context_lens, "context_lens"), n, q_len,
+            hq, hkv, d, bs, nb, int(max_context_len), float(scale), dtype_code(query), int(partition_size),
+            _stream(stream))
     _check("pa_decode_attention_noalloc", st)
     return out
 
