@@ -17,6 +17,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool supported_head_dim(int d) { return d == 64 || d == 128; }
 
+// Head counts above this are refused: row and block byte counts stay far inside int.
+constexpr int kMaxHeads = 1 << 16;
+
 int check_decode(const void* out, const void* query, const void* key_cache, const void* value_cache,
                  const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
                  int num_seqs, int q_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
@@ -29,6 +32,7 @@ int check_decode(const void* out, const void* query, const void* key_cache, cons
     if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
     if (partition < 0 || partition % PA_BLOCK_SIZE != 0) return PA_ERR_INVALID_ARG;
     if (block_size != PA_BLOCK_SIZE || !supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
+    if (num_heads > kMaxHeads) return PA_ERR_UNSUPPORTED;
     if ((int64_t)(num_heads / num_kv_heads) * q_len > 65536) return PA_ERR_UNSUPPORTED;
     if ((int64_t)max_context_len > (int64_t)max_blocks_per_seq * PA_BLOCK_SIZE) return PA_ERR_INVALID_ARG;
     if (num_blocks > (int64_t)INT32_MAX) return PA_ERR_INVALID_ARG;
@@ -68,7 +72,8 @@ int pa_reshape_and_cache(const void* key, const void* value, void* key_cache, vo
     t_last_launches = 0;
     if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 1) return PA_ERR_INVALID_ARG;
     if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_INVALID_ARG;
-    if (block_size != PA_BLOCK_SIZE || !supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
+    if (block_size != PA_BLOCK_SIZE || !supported_head_dim(head_dim) || num_kv_heads > kMaxHeads)
+        return PA_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PA_OK;
     if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
     if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache) ||
@@ -88,7 +93,8 @@ int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_mapp
     t_last_launches = 0;
     if (num_pairs < 0 || num_kv_heads < 1 || num_blocks < 1) return PA_ERR_INVALID_ARG;
     if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_INVALID_ARG;
-    if (block_size != PA_BLOCK_SIZE || !supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
+    if (block_size != PA_BLOCK_SIZE || !supported_head_dim(head_dim) || num_kv_heads > kMaxHeads)
+        return PA_ERR_UNSUPPORTED;
     if (num_pairs == 0) return PA_OK;
     if (!key_cache || !value_cache || !block_mapping) return PA_ERR_INVALID_ARG;
     if (!aligned16(key_cache) || !aligned16(value_cache) || (reinterpret_cast<uintptr_t>(block_mapping) & 7u) != 0)
@@ -182,7 +188,8 @@ int pa_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache
     if (dtype != PA_BF16 && dtype != PA_FP16) return PA_ERR_INVALID_ARG;
     if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
         return PA_ERR_INVALID_ARG;
-    if (block_size != PA_BLOCK_SIZE || !supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
+    if (block_size != PA_BLOCK_SIZE || !supported_head_dim(head_dim) || num_kv_heads > kMaxHeads)
+        return PA_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PA_OK;
     if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
     if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache) ||

@@ -65,6 +65,7 @@ def test_decode_host_validation(lib):
     assert _decode(lib, d=96) == 2                      # head_dim not compiled
     assert _decode(lib, bs=32) == 2                     # block size other than 16
     assert _decode(lib, hq=64, hkv=1, q_len=2000, max_ctx=128) == 2   # 128,000 rows per kv head
+    assert _decode(lib, hq=1 << 20, hkv=1 << 20) == 2                 # absurd head count
     assert _decode(lib, ws=None) == 3
     assert _decode(lib, ws_bytes=16) == 3
 
@@ -90,3 +91,5 @@ def test_reshape_host_validation(lib):
     assert f(None, FAKE, FAKE, FAKE, FAKE, 4, 4, 64, 16, 64, 0, None) == 1
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE + 4, 4, 4, 64, 16, 64, 0, None) == 1  # slot_mapping alignment
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 4, 64, 16, 64, 0, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 1 << 20, 128, 16, 64, 0, None) == 2   # absurd head count
+    assert lib.pa_copy_blocks(FAKE, FAKE, FAKE, 1, 1 << 20, 128, 16, 64, 0, None) == 2
