@@ -67,7 +67,7 @@ typedef enum { PA_BF16 = 0, PA_FP16 = 1 } pa_dtype;
 typedef enum {
     PA_OK = 0,
     PA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, inconsistent sizes */
-    PA_ERR_UNSUPPORTED = 2,   /* head_dim, block_size or group x q_len outside what is compiled */
+    PA_ERR_UNSUPPORTED = 2,   /* head_dim, block_size, group x q_len or a head count (> 65536) outside what is compiled */
     PA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than pa_decode_workspace_size() */
     PA_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
 } pa_status;
