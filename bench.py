@@ -95,8 +95,9 @@ def kernel_source_hash() -> str:
 
 
 def ncu_traffic(workload: str):
-    """DRAM bytes per launch of the partition kernel from the committed ncu summary, if the
-    summary was taken on the current kernel sources; else None."""
+    """DRAM bytes per call of the partition kernel and of the merge kernel (a dict with keys
+    "partition" and "merge") from the committed ncu summary, if it was taken on the current
+    kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", "decode_kernel_traffic.json")
     if not os.path.exists(path):
         return None
@@ -105,7 +106,7 @@ def ncu_traffic(workload: str):
     e = d.get(workload)
     if not e or e.get("source_hash") != kernel_source_hash():
         return None
-    return e.get("dram_bytes_per_launch_full")
+    return {"partition": e.get("dram_bytes_per_launch_full"), "merge": e.get("merge_dram_bytes_per_launch")}
 
 
 class Staging:
@@ -460,19 +461,25 @@ def run_ours(args, rank, world, local):
     step_ms_local = max(1e-9, (total_ms - flush_ms) / args.steps)
     step_ms = max_over_ranks(step_ms_local, world, dev)
 
-    # --- partition-kernel time for the roofline: the same steps again, with the library's
-    # CUDA-event pair recorded around every partition-kernel launch on the launch stream.
+    # --- kernel times for the roofline: the same steps again, with the library's CUDA events
+    # recorded on the launch stream around the plan, partition and merge kernels of every call.
     # (Events between launches suspend the programmatic overlap of launch set-up, which is
     # why the step itself is timed without them.)
-    prof_steps = min(args.steps, 4096)
-    pa.profile_enable(True)
-    pa.profile_read()
-    for _ in range(prof_steps):
-        flushed()
-        step()
-    torch.cuda.synchronize(dev)
+    # Pass 1 times the partition and merge kernels as one span (their programmatic overlap kept):
+    # the roofline figure.  Pass 2 times the plan, partition and merge kernels apart.
+    prof_steps = min(args.steps, 2048)
+    spans = []
+    for mode in (2, 1):
+        pa.profile_enable(mode)
+        pa.profile_read_parts()
+        for _ in range(prof_steps):
+            flushed()
+            step()
+        torch.cuda.synchronize(dev)
+        spans.append(pa.profile_read_parts())
     pa.profile_enable(False)
-    kern_ms_total, kern_n = pa.profile_read()
+    _, attn_ms_total, _, attn_n = spans[0]
+    plan_ms_total, kern_ms_total, merge_ms_total, kern_n = spans[1]
     err = pa.get_device_error(clear=True)
 
     # --- the append alone (the KV-append kernel), timed over the same number of calls
@@ -547,14 +554,20 @@ def run_ours(args, rank, world, local):
     if rank != 0:
         return
     peak, peak_kind = peaks()
-    kern_ms = kern_ms_total / max(1, kern_n)
-    achieved = attn_bytes / (kern_ms * 1e-3) / 1e9
+    kern_ms = kern_ms_total / max(1, kern_n)          # K2: the partition pass (or the tcgen05 kernel)
+    merge_ms = merge_ms_total / max(1, kern_n)        # K3: the log-sum-exp merge (0 without one), timed apart
+    plan_ms = plan_ms_total / max(1, kern_n)
+    attn_ms = attn_ms_total / max(1, attn_n)          # K2 + K3 as one span, the attention proper
+    achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
+    achieved_k2 = attn_bytes / (kern_ms * 1e-3) / 1e9
     # The library runs a call with >= 128 query rows per kv head (and the default split) on the
     # tcgen05 prefill kernel, everything else on the split-K decode kernel.
     tc_path = not kv8 and (args.math == "tcgen05" or
                            (args.math == "auto" and (w.num_heads // w.num_kv_heads) * w.q_len >= 128))
-    kernel_name = "prefill_tc_kernel (tcgen05, no split)" if tc_path else "decode_kernel (partition pass)"
-    traffic = ncu_traffic(args.workload) if not kv8 and not tc_path and args.math == "auto" else None
+    kernel_name = ("prefill_tc_kernel (tcgen05, no split)" if tc_path else
+                   "decode_kernel + merge_kernel (split-K partition pass and log-sum-exp merge)")
+    t = ncu_traffic(args.workload) if not kv8 and not tc_path and args.math == "auto" else None
+    traffic = t["partition"] + t["merge"] if t and t["partition"] and t["merge"] is not None else None
     flops = W.attention_flops(w)
     tpeak, tpeak_kind = tensor_peak()
     compute_bound = flops / attn_bytes > tpeak * 1e12 / (peak * 1e9)   # past the ridge point
@@ -573,18 +586,21 @@ def run_ours(args, rank, world, local):
         "unique_attention_bytes": unique_bytes,
         "append": {"us_per_call": append_ms * 1e3, "bytes": append_bytes,
                    "gbs": append_bytes / (append_ms * 1e-3) / 1e9},
-        "roofline": ({"bound": "tensor", "achieved": flops / (kern_ms * 1e-3) / 1e12, "peak": tpeak,
-                      "unit": "TFLOP/s", "frac": flops / (kern_ms * 1e-3) / 1e12 / tpeak,
+        "roofline": ({"bound": "tensor", "achieved": flops / (attn_ms * 1e-3) / 1e12, "peak": tpeak,
+                      "unit": "TFLOP/s", "frac": flops / (attn_ms * 1e-3) / 1e12 / tpeak,
                       "peak_source": f"{tpeak_kind} dense bf16 cuBLAS burst", "flops_per_launch": flops,
-                      "kernel": kernel_name, "kernel_ms": kern_ms, "traffic": traffic,
+                      "kernel": kernel_name, "kernel_ms": attn_ms, "traffic": traffic,
                       "hbm_gbs": achieved}
                      if compute_bound else
                      {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                       "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth",
-                      "kernel": kernel_name, "kernel_ms": kern_ms,
-                      "traffic": traffic, "tflops": flops / (kern_ms * 1e-3) / 1e12}),
+                      "kernel": kernel_name, "kernel_ms": attn_ms,
+                      "traffic": traffic, "tflops": flops / (attn_ms * 1e-3) / 1e12,
+                      "partition_kernel": {"ms": kern_ms, "achieved": achieved_k2, "frac": achieved_k2 / peak,
+                                           "traffic": t["partition"] if t else None},
+                      "merge_kernel_ms_apart": merge_ms, "plan_kernel_ms_apart": plan_ms}),
         "gpu_launches": launches_per_step * args.steps,
-        "roofline_steps": kern_n,
+        "roofline_steps": attn_n,
         "clocks": clocks.summary(),
         "device_error_flags": err,
         "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,

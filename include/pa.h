@@ -31,8 +31,9 @@
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers, owned by the caller, C-contiguous,
  *     16-byte aligned.  The library never allocates device memory, never frees
- *     caller memory and never synchronises the stream (pa_get_device_error and
- *     pa_profile_read are the documented exceptions: they wait for the stream).
+ *     caller memory and never synchronises the stream (pa_get_device_error,
+ *     pa_profile_read and pa_profile_read_parts are the documented
+ *     exceptions: they wait for the stream or the recorded events).
  *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = the
  *     legacy default stream) of the current device.
  *   - 16-bit element types: PA_BF16 (bfloat16) or PA_FP16 (IEEE binary16).
@@ -45,7 +46,7 @@
  *   - context_lens[i] counts every position of sequence i INCLUDING the q_len
  *     positions being decoded (their K/V must already be appended).
  *   - Supported: head_dim 64 or 128; block_size 16;
- *     (num_heads / num_kv_heads) * q_len <= 64.
+ *     (num_heads / num_kv_heads) * q_len <= 65536.
  *   - Host-side argument errors return a status and enqueue nothing.  Device
  *     contents (block ids, lengths, slots) are checked inside the kernels: a
  *     bad value sets a bit in the library's device error word (see
@@ -234,19 +235,26 @@ int pa_decode_attention_ex(void* out, const void* query, const void* key_cache, 
  *
  * Some callers cannot hand the library a workspace: a host program that reaches
  * the GPU only through this C ABI and has no device allocator of its own, or a
- * serving process whose allocator has reserved all device memory up front (the
- * pages' gpu_memory_utilization budget) and allows no further cudaMalloc, whose
- * implicit device-wide synchronisation would also stall a decode loop.  This
- * variant computes exactly what pa_decode_attention_ex computes, with the same
- * arguments minus the workspace, and takes its split-K scratch from a fixed
- * array inside the library:
+ * serving process whose allocator reserved nearly all device memory at start-up
+ * for its KV pool and permits no further cudaMalloc (which would also
+ * synchronise the whole device in the middle of a decode loop).  This variant
+ * computes exactly what pa_decode_attention_ex computes, with the same arguments
+ * minus the workspace, and takes its split-K scratch from a fixed array inside
+ * the library:
  *   - the array holds PA_NOALLOC_WORKSPACE_BYTES (32 MiB) on every GPU that
  *     loads the library, until the process exits;
- *   - a call whose pa_decode_workspace_size_ex() exceeds that returns
- *     PA_ERR_WORKSPACE and enqueues nothing (use pa_decode_attention_ex then);
+ *   - a call that splits (every call the tcgen05 kernel does not run, see
+ *     pa_decode_attention_multiquery) and whose pa_decode_workspace_size_ex()
+ *     exceeds that returns PA_ERR_WORKSPACE and enqueues nothing (use
+ *     pa_decode_attention_ex then); a call the tcgen05 kernel runs uses no
+ *     scratch and has no such limit;
  *   - the first call on each device looks up the array's device address (a
- *     runtime symbol query, no allocation) with that device current; make that
- *     first call before any stream capture;
+ *     runtime symbol query, no allocation) with that device current, and keeps
+ *     it; make that first call before any stream capture.  The address belongs
+ *     to the device's primary context: after cudaDeviceReset (or anything else
+ *     that destroys that context) the process must not call this library on
+ *     that device again, as its cached addresses (this array, the error word)
+ *     and kernel attributes then refer to the old context;
  *   - every call on a device shares the one array, which keeps the last call's
  *     contents (each call rewrites all of it that it reads, so nothing needs
  *     clearing); calls that overlap on the GPU, on different streams or from
@@ -323,13 +331,34 @@ int pa_set_decode_math(int math);
 
 /*
  * Timing hook for benchmarks.  pa_profile_enable(1) makes every following
- * decode call record a CUDA event pair around its main (partition) kernel on
- * the call's stream (up to 4096 pairs); pa_profile_read() waits for the
- * recorded events, returns the summed milliseconds and the launch count, and
- * clears the record.  pa_profile_enable(0) stops recording.
+ * decode call record CUDA events on the call's stream around its kernels (up to
+ * 2048 calls): before the plan kernel, before the main kernel (the split-K
+ * partition pass, or the tcgen05 kernel), after it, and after the merge kernel.
+ * pa_profile_enable(2) records the same marks except the one between the main
+ * and the merge kernel, so those two keep their programmatic overlap and the
+ * main figure covers both.  pa_profile_read_parts() waits for the recorded
+ * events and returns the summed milliseconds of the plan, main and merge
+ * kernels (merge 0 in mode 2) and the number of calls, and clears the record;
+ * pa_profile_read() returns the main figure only (and clears the record too).
+ * pa_profile_enable(0) stops recording; changing the mode clears the record.
+ * Events between kernels suspend their programmatic overlap, so a recorded
+ * call runs a little slower than an unrecorded one.
  */
 int pa_profile_enable(int on);
 int pa_profile_read(float* total_ms, int* launches);
+int pa_profile_read_parts(float* plan_ms, float* main_ms, float* merge_ms, int* calls);
+
+/*
+ * Limit of the kernels' pipeline waits (a test hook for their failure path:
+ * every mbarrier wait inside a kernel gives up after a limit, sets
+ * PA_DEVERR_TIMEOUT and stops the CTA, and the context stays usable).  Launches made after this
+ * call use `ns` nanoseconds; 0 restores the default (2 s).  A limit below the
+ * default also makes those waits poll without suspending, so a test can make
+ * them run out on an ordinary call.  The waits a CTA makes for its own copies
+ * and tensor-core products before it exits keep the default limit, so no CTA
+ * leaves work in flight.  Process-wide; not thread safe.
+ */
+int pa_set_wait_limit_ns(unsigned long long ns);
 
 /*
  * Split-K partition (tokens) the last decode call on this thread used: the caller's size,

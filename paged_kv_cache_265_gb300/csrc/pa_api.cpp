@@ -45,6 +45,42 @@ int check_decode(const void* out, const void* query, const void* key_cache, cons
     return PA_OK;
 }
 
+pa::DecodeArgs decode_args(void* out, const void* query, const void* key_cache, const void* value_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                           int num_seqs, int q_len, int num_heads, int num_kv_heads, int head_dim,
+                           int64_t num_blocks, int max_context_len, float scale, int dtype, int partition_size,
+                           void* workspace) {
+    pa::DecodeArgs a;
+    a.out = out;
+    a.query = query;
+    a.key_cache = key_cache;
+    a.value_cache = value_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_seqs = num_seqs;
+    a.q_len = q_len;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.num_blocks = num_blocks;
+    a.max_context_len = max_context_len;
+    a.scale = scale;
+    a.dtype = dtype;
+    a.partition = partition_size == 0 ? PA_DEFAULT_PARTITION : partition_size;
+    a.partition_auto = partition_size == 0;
+    a.workspace = workspace;
+    return a;
+}
+
+int run_decode(const pa::DecodeArgs& a, void* stream) {
+    int launches = 0, part = 0;
+    const int rc = pa::launch_decode(a, static_cast<cudaStream_t>(stream), &launches, &part);
+    t_last_launches = launches;
+    t_last_partition = part;
+    return rc;
+}
+
 }  // namespace
 
 extern "C" {
@@ -149,34 +185,12 @@ int pa_decode_attention_ex(void* out, const void* query, const void* key_cache, 
                                 context_lens, num_seqs, q_len, num_heads, num_kv_heads, head_dim, block_size,
                                 num_blocks, max_context_len, scale, dtype, partition_size);
     if (st != PA_OK || num_seqs == 0) return st;
-    const int partition = partition_size == 0 ? PA_DEFAULT_PARTITION : partition_size;
-    const size_t need = pa::ws_layout(num_seqs, q_len, num_heads, head_dim, max_context_len, partition).total;
+    const pa::DecodeArgs a = decode_args(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                                         context_lens, num_seqs, q_len, num_heads, num_kv_heads, head_dim,
+                                         num_blocks, max_context_len, scale, dtype, partition_size, workspace);
+    const size_t need = pa::ws_layout(num_seqs, q_len, num_heads, head_dim, max_context_len, a.partition).total;
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
-    pa::DecodeArgs a;
-    a.out = out;
-    a.query = query;
-    a.key_cache = key_cache;
-    a.value_cache = value_cache;
-    a.block_tables = block_tables;
-    a.context_lens = context_lens;
-    a.max_blocks_per_seq = max_blocks_per_seq;
-    a.num_seqs = num_seqs;
-    a.q_len = q_len;
-    a.num_heads = num_heads;
-    a.num_kv_heads = num_kv_heads;
-    a.head_dim = head_dim;
-    a.num_blocks = num_blocks;
-    a.max_context_len = max_context_len;
-    a.scale = scale;
-    a.dtype = dtype;
-    a.partition = partition;
-    a.partition_auto = partition_size == 0;
-    a.workspace = workspace;
-    int launches = 0, part = 0;
-    const int rc = pa::launch_decode(a, static_cast<cudaStream_t>(stream), &launches, &part);
-    t_last_launches = launches;
-    t_last_partition = part;
-    return rc;
+    return run_decode(a, stream);
 }
 
 int pa_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache, void* value_cache,
@@ -217,36 +231,16 @@ int pa_decode_attention_fp8kv(void* out, const void* query, const void* key_cach
     if (head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
         return PA_ERR_INVALID_ARG;
-    const int partition = partition_size == 0 ? PA_DEFAULT_PARTITION : partition_size;
-    const size_t need = pa::ws_layout(num_seqs, q_len, num_heads, head_dim, max_context_len, partition).total;
+    pa::DecodeArgs a = decode_args(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                                   context_lens, num_seqs, q_len, num_heads, num_kv_heads, head_dim, num_blocks,
+                                   max_context_len, scale, dtype, partition_size, workspace);
+    const size_t need = pa::ws_layout(num_seqs, q_len, num_heads, head_dim, max_context_len, a.partition).total;
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
-    pa::DecodeArgs a;
-    a.out = out;
-    a.query = query;
-    a.key_cache = key_cache;
-    a.value_cache = value_cache;
-    a.block_tables = block_tables;
-    a.context_lens = context_lens;
-    a.max_blocks_per_seq = max_blocks_per_seq;
-    a.num_seqs = num_seqs;
-    a.q_len = q_len;
-    a.num_heads = num_heads;
-    a.num_kv_heads = num_kv_heads;
-    a.head_dim = head_dim;
-    a.num_blocks = num_blocks;
-    a.max_context_len = max_context_len;
-    a.scale = scale;
-    a.dtype = dtype;
-    a.partition = partition;
-    a.workspace = workspace;
+    a.partition_auto = false;  // FP8 caches keep the default split unless the caller chooses one
     a.fp8 = true;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
-    int launches = 0, part = 0;
-    const int rc = pa::launch_decode(a, static_cast<cudaStream_t>(stream), &launches, &part);
-    t_last_launches = launches;
-    t_last_partition = part;
-    return rc;
+    return run_decode(a, stream);
 }
 
 int pa_decode_attention(void* out, const void* query, const void* key_cache, const void* value_cache,
@@ -280,15 +274,15 @@ int pa_decode_attention_noalloc(void* out, const void* query, const void* key_ca
                                 context_lens, num_seqs, q_len, num_heads, num_kv_heads, head_dim, block_size,
                                 num_blocks, max_context_len, scale, dtype, partition_size);
     if (st != PA_OK || num_seqs == 0) return st;
-    const int partition = partition_size == 0 ? PA_DEFAULT_PARTITION : partition_size;
-    const size_t need = pa::ws_layout(num_seqs, q_len, num_heads, head_dim, max_context_len, partition).total;
+    pa::DecodeArgs a = decode_args(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                                   context_lens, num_seqs, q_len, num_heads, num_kv_heads, head_dim, num_blocks,
+                                   max_context_len, scale, dtype, partition_size, nullptr);
+    // A call the tcgen05 kernel runs (no split) needs no scratch at all.
+    if (pa::use_prefill_tc(a)) return run_decode(a, stream);
+    const size_t need = pa::ws_layout(num_seqs, q_len, num_heads, head_dim, max_context_len, a.partition).total;
     if (need > (size_t)PA_NOALLOC_WORKSPACE_BYTES) return PA_ERR_WORKSPACE;  // too big for the fixed scratch
-    void* scratch = nullptr;
-    if (const int ws = pa::noalloc_workspace(&scratch)) return ws;
-    return pa_decode_attention_ex(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
-                                  context_lens, num_seqs, q_len, num_heads, num_kv_heads, head_dim, block_size,
-                                  num_blocks, max_context_len, scale, dtype, partition_size, scratch,
-                                  (size_t)PA_NOALLOC_WORKSPACE_BYTES, stream);
+    if (const int ws = pa::noalloc_workspace(&a.workspace)) return ws;
+    return run_decode(a, stream);
 }
 
 int pa_get_device_error(int32_t* host_flags, int clear, void* stream) {
@@ -302,7 +296,15 @@ int pa_profile_enable(int on) { return pa::profile_enable(on); }
 
 int pa_profile_read(float* total_ms, int* launches) {
     if (!total_ms || !launches) return PA_ERR_INVALID_ARG;
-    return pa::profile_read(total_ms, launches);
+    float plan = 0.f, merge = 0.f;
+    return pa::profile_read_parts(&plan, total_ms, &merge, launches);
 }
+
+int pa_profile_read_parts(float* plan_ms, float* main_ms, float* merge_ms, int* calls) {
+    if (!plan_ms || !main_ms || !merge_ms || !calls) return PA_ERR_INVALID_ARG;
+    return pa::profile_read_parts(plan_ms, main_ms, merge_ms, calls);
+}
+
+int pa_set_wait_limit_ns(unsigned long long ns) { return pa::set_wait_limit_ns(ns); }
 
 }  // extern "C"

@@ -11,7 +11,8 @@
 namespace pa {
 
 // A bounded wait gives up after this long and raises PA_DEVERR_TIMEOUT; every
-// legitimate wait in these kernels ends within microseconds.
+// legitimate wait in these kernels ends within microseconds.  Pipeline waits
+// take the limit of their launch (pa_set_wait_limit_ns), this by default.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -61,11 +62,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe: never suspends the thread.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// A pipeline wait under a limit shorter than the default (a test setting): polls with the
+// non-blocking probe and reads the timer on every turn, so the wait gives up soon after
+// `limit_ns` even where a blocking probe would have slept until the phase completed.
+static __device__ __noinline__ bool mbar_wait_polled(uint32_t bar, uint32_t parity, int* err, volatile int* abort_flag,
+                                              unsigned long long limit_ns) {
+    const unsigned long long t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicOr(err, PA_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
 // Waits until the phase with the given parity has completed.  Returns false
-// (and records PA_DEVERR_TIMEOUT) if that takes longer than kWaitLimitNs or if
-// `abort_flag` (shared, may be null) becomes non-zero.
+// (and records PA_DEVERR_TIMEOUT) if that takes longer than the limit or if
+// `abort_flag` (shared, may be null) becomes non-zero.  A pipeline wait (one
+// given an abort flag) uses `limit_ns`, the launch's setting; a drain wait (no
+// abort flag: a CTA waiting for its own copies or products before it exits)
+// always uses kWaitLimitNs, so no CTA leaves with work still in flight.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
+    if (abort_flag && limit_ns < kWaitLimitNs) return mbar_wait_polled(bar, parity, err, abort_flag, limit_ns);
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {

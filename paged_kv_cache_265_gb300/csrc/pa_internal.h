@@ -84,8 +84,10 @@ int launch_reshape_and_cache(const void* key, const void* value, void* key_cache
                              int64_t num_slots, cudaStream_t stream, int* launches);
 // `partition_used` receives the split-K partition in tokens (0: the tcgen05 kernel, no split).
 int launch_decode(const DecodeArgs& a, cudaStream_t stream, int* launches, int* partition_used);
-// Chunked-prefill attention on tcgen05 (pa_prefill.cu); launch_decode routes calls to it.
+// Chunked-prefill attention on tcgen05 (pa_prefill.cu); launch_decode routes calls to it
+// when use_prefill_tc() holds (that path does not split and uses no workspace).
 int launch_prefill_tc(const DecodeArgs& a, cudaStream_t stream, int* launches);
+bool use_prefill_tc(const DecodeArgs& a);
 int launch_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* target_probs,
                        const float* draft_probs, const int32_t* draft_tokens, const float* u_accept,
                        const float* u_sample, int num_seqs, int k, int vocab, cudaStream_t stream, int* launches);
@@ -100,15 +102,24 @@ int read_device_error(int32_t* flags, int clear, cudaStream_t stream);
 // (looked up on the first call per device, then cached).
 int noalloc_workspace(void** ptr);
 
+// Limit (ns) of the kernels' pipeline waits for launches made from now on; 0 restores the
+// default (kWaitLimitNs).  wait_limit_ns() is the current setting.
+int set_wait_limit_ns(unsigned long long ns);
+unsigned long long wait_limit_ns();
+
 // Consumer arithmetic: 0 auto, 1 CUDA-core FMA, 2 mma.sync tensor-core tiles, 3 tcgen05 prefill kernel.
 int set_decode_math(int math);
 
-// Benchmark timing hook around the main decode kernel.
+// Benchmark timing hook: CUDA events around each decode call's kernels.
 int profile_enable(int on);
-int profile_read(float* total_ms, int* launches);
-// Inside a launcher: records the start event if timing is on (then profile_end after the launch).
-bool profile_begin(cudaStream_t stream);
-void profile_end(cudaStream_t stream);
+// Summed milliseconds of the plan kernel, the main kernel and the merge kernel over the
+// recorded calls (waits for them), then clears the record.
+int profile_read_parts(float* plan_ms, float* main_ms, float* merge_ms, int* calls);
+// Inside a launcher: profile_call_begin() returns the call's record index (-1 when timing is
+// off or the record is full); profile_mark(call, k, stream) records mark k (0 before the plan
+// kernel, 1 before the main kernel, 2 after it, 3 after the merge) on the launch stream.
+int profile_call_begin();
+void profile_mark(int call, int mark, cudaStream_t stream);
 
 // Tensor map of a 16-bit pool [num_blocks, 16, Hkv, head_dim]: one box = 64 elements of one
 // kv head for the 16 positions of one block, 128-byte swizzled.

@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 #include <type_traits>
@@ -546,6 +547,7 @@ struct alignas(128) DecodeParams {
     int slot_rows;     // min(16, rows): rows each warp leaves in the combine buffer
     float scale_log2;  // scale * log2(e) (times the K dequantisation scale for an FP8 cache)
     float v_scale;     // V dequantisation scale (1 for 16-bit caches)
+    unsigned long long wait_limit_ns;  // limit of the pipeline waits (pa_set_wait_limit_ns)
 };
 
 struct UnitInfo {
@@ -750,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
         for (; ok; ++ul) {
             const int qb = ul & 1;
             if (ul >= 2 &&
-                !__all_sync(0xffffffffu, mbar_wait(qempty0 + 8 * qb, ((ul - 2) >> 1) & 1, &g_pa_error, abort_flag))) {
+                !__all_sync(0xffffffffu, mbar_wait(qempty0 + 8 * qb, ((ul - 2) >> 1) & 1, &g_pa_error, abort_flag, p.wait_limit_ns))) {
                 ok = false;
                 break;
             }
@@ -812,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                     const int s = (int)(k % stages);
                     if (k >= (uint32_t)stages &&
                         !__all_sync(0xffffffffu,
-                                    mbar_wait(empty0 + 8 * s, ((k / stages) - 1) & 1, &g_pa_error, abort_flag))) {
+                                    mbar_wait(empty0 + 8 * s, ((k / stages) - 1) & 1, &g_pa_error, abort_flag, p.wait_limit_ns))) {
                         ok = false;
                         break;
                     }
@@ -863,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                 const int s = (int)(k % stages);
                 if (k >= (uint32_t)stages &&
                     !__all_sync(0xffffffffu,
-                                mbar_wait(empty0 + 8 * s, ((k / stages) - 1) & 1, &g_pa_error, abort_flag))) {
+                                mbar_wait(empty0 + 8 * s, ((k / stages) - 1) & 1, &g_pa_error, abort_flag, p.wait_limit_ns))) {
                     ok = false;
                     break;
                 }
@@ -905,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
     for (;; ++ul) {
         const int qb = ul & 1;
         // (all waits below are made warp-uniform: a timeout seen by one lane stops the warp)
-        bool ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8 * qb, (ul >> 1) & 1, &g_pa_error, abort_flag));
+        bool ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8 * qb, (ul >> 1) & 1, &g_pa_error, abort_flag, p.wait_limit_ns));
         const UnitInfo ui = info[qb];
         const bool done = ok && ui.seq < 0;  // end marker: no unit follows
         const int rows_here = min(TR, ui.nrows - mt * TR);  // <= 0 for an all-padding tile
@@ -978,7 +980,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                 for (int j = bsg; j < nblk_pad; j += p.block_splits) {
                     const uint32_t kj = k + j;
                     const int s = (int)(kj % stages);
-                    if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (kj / stages) & 1, &g_pa_error, abort_flag))) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (kj / stages) & 1, &g_pa_error, abort_flag, p.wait_limit_ns))) {
                         ok = false;
                         break;
                     }
@@ -1197,7 +1199,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                     const uint32_t kj = k + j;
                     const int s = (int)(kj % stages);
                     if (!__all_sync(0xffffffffu,
-                                    mbar_wait(full0 + 8 * s, (kj / stages) & 1, &g_pa_error, abort_flag))) {
+                                    mbar_wait(full0 + 8 * s, (kj / stages) & 1, &g_pa_error, abort_flag, p.wait_limit_ns))) {
                         ok = false;
                         break;
                     }
@@ -1494,11 +1496,16 @@ int decode_blocks_per_sm(const void* fn, int smem, int& blocks) {
 // 3: the tcgen05 prefill kernel for every call over 16-bit caches
 int g_decode_math = 0;
 
+// Benchmark timing marks of each decode call: 0 before the plan kernel, 1 before the main
+// kernel (the split-K partition pass or the tcgen05 kernel), 2 after it, 3 after the merge.
+// In mode 2 mark 2 is not recorded, so nothing separates the main kernel from the merge kernel
+// (their programmatic overlap is kept) and the main figure covers both.
+constexpr int kProfCalls = 2048;
 struct Profile {
-    bool on = false;
+    int mode = 0;  // 0 off, 1 every mark, 2 marks 0, 1 and 3
     int dev = -1;
     int n = 0;
-    cudaEvent_t ev[2 * 4096] = {};
+    cudaEvent_t ev[4 * kProfCalls] = {};
     bool created = false;
 } g_prof;
 
@@ -1607,6 +1614,8 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     DeviceInfo dev;
     if (int st = device_info(dev)) return st;
 
+    const int pc = profile_call_begin();
+    profile_mark(pc, 0, stream);
     PlanParams pp;
     pp.context_lens = a.context_lens;
     pp.header = header;
@@ -1620,6 +1629,7 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     pp.max_context_len = a.max_context_len;
     if (launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, pp) != cudaSuccess) return PA_ERR_CUDA;
     *launches += 1;
+    profile_mark(pc, 1, stream);
 
     DecodeParams p;
     if (a.fp8) {
@@ -1651,6 +1661,7 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     p.partition = a.partition;
     p.scale_log2 = a.scale * (a.fp8 ? a.k_scale : 1.f) * 1.4426950408889634f;
     p.v_scale = a.fp8 ? a.v_scale : 1.f;
+    p.wait_limit_ns = wait_limit_ns();
     // Each consumer warp owns 8 (NT = 1) or 16 (NT = 2) query rows of the kv head; the row
     // tiles per kv head are rounded up to a divisor of the consumer warp count (a third
     // tile becomes a fourth, all-padding one) so that every consumer warp owns exactly one
@@ -1697,14 +1708,9 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     const long long max_units = (long long)a.num_seqs * w.pmax * a.num_kv_heads * p.row_groups;
     const int grid = (int)std::max(1LL, std::min<long long>((long long)dev.sms * per_sm, max_units));
 
-    const bool prof = g_prof.on && g_prof.n < 4096;
-    if (prof) cudaEventRecord(g_prof.ev[2 * g_prof.n], stream);
     const cudaError_t le = launch_pdl(kfn, dim3(grid), dim3(kThreads), lay.total, stream, p);
     if (le != cudaSuccess) return PA_ERR_CUDA;
-    if (prof) {
-        cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], stream);
-        g_prof.n++;
-    }
+    profile_mark(pc, 2, stream);
     *launches += 1;
 
     if (w.pmax > 1) {
@@ -1724,6 +1730,7 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
         if (launch_pdl(merge_kernel<T, D>, dim3(blocks), dim3(128), 0, stream, mp) != cudaSuccess) return PA_ERR_CUDA;
         *launches += 1;
     }
+    profile_mark(pc, 3, stream);
     return PA_OK;
 }
 
@@ -1767,15 +1774,14 @@ int ensure_dynamic_smem(const void* fn, int smem) {
     return PA_OK;
 }
 
-bool profile_begin(cudaStream_t stream) {
-    const bool prof = g_prof.on && g_prof.n < 4096;
-    if (prof) cudaEventRecord(g_prof.ev[2 * g_prof.n], stream);
-    return prof;
+int profile_call_begin() {
+    if (!g_prof.mode || g_prof.n >= kProfCalls) return -1;
+    return g_prof.n++;
 }
 
-void profile_end(cudaStream_t stream) {
-    cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], stream);
-    g_prof.n++;
+void profile_mark(int call, int mark, cudaStream_t stream) {
+    if (call < 0 || (mark == 2 && g_prof.mode == 2)) return;
+    cudaEventRecord(g_prof.ev[4 * call + mark], stream);
 }
 
 int launch_reshape_and_cache(const void* key, const void* value, void* key_cache, void* value_cache,
@@ -1900,6 +1906,16 @@ int read_device_error(int32_t* flags, int clear, cudaStream_t stream) {
     return PA_OK;
 }
 
+// Limit of the kernels' pipeline waits, copied into every launch's parameters.
+std::atomic<unsigned long long> g_wait_limit_ns{kWaitLimitNs};
+
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+int set_wait_limit_ns(unsigned long long ns) {
+    g_wait_limit_ns.store(ns == 0 || ns > kWaitLimitNs ? kWaitLimitNs : ns, std::memory_order_relaxed);
+    return PA_OK;
+}
+
 int set_decode_math(int math) {
     if (math < 0 || math > 3) return PA_ERR_INVALID_ARG;
     g_decode_math = math;
@@ -1907,28 +1923,39 @@ int set_decode_math(int math) {
 }
 
 int profile_enable(int on) {
+    if (on < 0 || on > 2) return PA_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(g_mu);
     if (on && !g_prof.created) {
-        for (int i = 0; i < 2 * 4096; ++i)
+        for (int i = 0; i < 4 * kProfCalls; ++i)
             if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) return PA_ERR_CUDA;
         g_prof.created = true;
         cudaGetDevice(&g_prof.dev);
     }
-    g_prof.on = on != 0;
+    if (on != g_prof.mode) g_prof.n = 0;  // a record never mixes modes
+    g_prof.mode = on;
     return PA_OK;
 }
 
-int profile_read(float* total_ms, int* launches) {
+int profile_read_parts(float* plan_ms, float* main_ms, float* merge_ms, int* calls) {
     std::lock_guard<std::mutex> lk(g_mu);
-    float sum = 0.f;
+    float sum[3] = {0.f, 0.f, 0.f};
     for (int i = 0; i < g_prof.n; ++i) {
-        if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess) return PA_ERR_CUDA;
-        float ms = 0.f;
-        if (cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess) return PA_ERR_CUDA;
-        sum += ms;
+        const cudaEvent_t* e = g_prof.ev + 4 * i;
+        if (cudaEventSynchronize(e[3]) != cudaSuccess) return PA_ERR_CUDA;
+        float ms[3] = {0.f, 0.f, 0.f};
+        if (cudaEventElapsedTime(&ms[0], e[0], e[1]) != cudaSuccess) return PA_ERR_CUDA;
+        if (g_prof.mode == 2) {
+            if (cudaEventElapsedTime(&ms[1], e[1], e[3]) != cudaSuccess) return PA_ERR_CUDA;
+        } else {
+            if (cudaEventElapsedTime(&ms[1], e[1], e[2]) != cudaSuccess) return PA_ERR_CUDA;
+            if (cudaEventElapsedTime(&ms[2], e[2], e[3]) != cudaSuccess) return PA_ERR_CUDA;
+        }
+        for (int k = 0; k < 3; ++k) sum[k] += ms[k];
     }
-    *total_ms = sum;
-    *launches = g_prof.n;
+    *plan_ms = sum[0];
+    *main_ms = sum[1];
+    *merge_ms = sum[2];
+    *calls = g_prof.n;
     g_prof.n = 0;
     return PA_OK;
 }

@@ -88,6 +88,7 @@ struct PrefillTcParams {
     int mtiles;      // 128-row tiles per kv head
     int max_context_len;
     float scale_log2;
+    unsigned long long wait_limit_ns;  // limit of the pipeline waits (pa_set_wait_limit_ns)
 };
 
 template <int D>
@@ -216,7 +217,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             }
             if (j >= kTcStages) {
                 bool w = true;
-                if (lane == 0) w = mbar_wait(kvempty + 8 * s, ((j / kTcStages) - 1) & 1, err, abort_flag);
+                if (lane == 0) w = mbar_wait(kvempty + 8 * s, ((j / kTcStages) - 1) & 1, err, abort_flag, p.wait_limit_ns);
                 if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
             }
             const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
@@ -257,12 +258,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             // 256 KB, so the 14-bit field never carries into the next one.
             const uint64_t kdesc0 = tc::smem_desc_sw128(st_s, 16, 1024);
             const uint64_t vdesc0 = tc::smem_desc_sw128(st_s + Lay::kKBytes, kRegion, 1024);
-            bool ok = mbar_wait(qready, 0, err, abort_flag);
+            bool ok = mbar_wait(qready, 0, err, abort_flag, p.wait_limit_ns);
             for (int j = 0; ok && j <= ntiles; ++j) {
                 if (j < ntiles) {
                     const int s = j % kTcStages;
-                    ok = mbar_wait(kvfull + 8 * s, (j / kTcStages) & 1, err, abort_flag) &&
-                         (j < 2 || mbar_wait(odone, (j - 2) & 1, err, abort_flag));
+                    ok = mbar_wait(kvfull + 8 * s, (j / kTcStages) & 1, err, abort_flag, p.wait_limit_ns) &&
+                         (j < 2 || mbar_wait(odone, (j - 2) & 1, err, abort_flag, p.wait_limit_ns));
                     if (!ok) break;
                     tc::fence_after_sync();
                     const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
                 }
                 if (j > 0) {
                     const int i = j - 1, s = i % kTcStages;
-                    ok = mbar_wait(pfull, i & 1, err, abort_flag);
+                    ok = mbar_wait(pfull, i & 1, err, abort_flag, p.wait_limit_ns);
                     if (!ok) break;
                     tc::fence_after_sync();
                     const int nb = min(kTcBlocks, nblk - kTcBlocks * i);
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            if (!__all_sync(0xffffffffu, mbar_wait(sfull + 8 * (j & 1), (j >> 1) & 1, err, abort_flag))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(sfull + 8 * (j & 1), (j >> 1) & 1, err, abort_flag, p.wait_limit_ns))) {
                 ok = false;
                 break;
             }
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             tc::st_x32(buf + 64 * hf, ph);
             tc::st_x32(buf + 64 * hf + 32, pl);
             // P_{j-1} V_{j-1} must be done before O is rescaled.
-            if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(odone, (j - 1) & 1, err, abort_flag))) {
+            if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(odone, (j - 1) & 1, err, abort_flag, p.wait_limit_ns))) {
                 ok = false;
                 break;
             }
@@ -462,13 +463,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             tc::fence_before_sync();
             mbar_arrive(pfull);
         }
+        // A wait that gave up above may have left this thread's P stores in flight: they
+        // complete before tensor memory is freed.
+        tc::wait_st();
 
         // Epilogue: the row's two half sums, then O / l, rounded once, to out[seq, t, hq, :]
         // (this thread's half of the columns).
-        if (ok && __all_sync(0xffffffffu, mbar_wait(odone, (ntiles - 1) & 1, err, abort_flag))) {
+        if (ok && __all_sync(0xffffffffu, mbar_wait(odone, (ntiles - 1) & 1, err, abort_flag, p.wait_limit_ns))) {
             lsum[hf * kTcRows + r] = l_run;
             mbar_arrive(lready);
-            if (__all_sync(0xffffffffu, mbar_wait(lready, 0, err, abort_flag))) {
+            if (__all_sync(0xffffffffu, mbar_wait(lready, 0, err, abort_flag, p.wait_limit_ns))) {
                 tc::fence_after_sync();
                 const float inv = 1.f / (lsum[r] + lsum[kTcRows + r]);
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row_off) + hf * (D / 16);
@@ -521,15 +525,19 @@ int launch_prefill_tc_typed(const DecodeArgs& a, cudaStream_t stream, int* launc
     p.mtiles = (p.total_rows + kTcRows - 1) / kTcRows;
     p.max_context_len = a.max_context_len;
     p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.wait_limit_ns = wait_limit_ns();
     const long long grid = (long long)a.num_seqs * a.num_kv_heads * p.mtiles;
     if (grid > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     auto kfn = prefill_tc_kernel<T, D>;
     const int smem = TcLayout<D>::kAlloc;
     if (int st = ensure_dynamic_smem(reinterpret_cast<const void*>(kfn), smem)) return st;
-    const bool prof = profile_begin(stream);
+    const int pc = profile_call_begin();
+    profile_mark(pc, 0, stream);  // no plan kernel: marks 0 and 1 coincide
+    profile_mark(pc, 1, stream);
     if (launch_pdl(kfn, dim3((unsigned)grid), dim3(kTcThreads), (size_t)smem, stream, p) != cudaSuccess)
         return PA_ERR_CUDA;
-    if (prof) profile_end(stream);
+    profile_mark(pc, 2, stream);
+    profile_mark(pc, 3, stream);  // no merge kernel
     *launches += 1;
     return PA_OK;
 }

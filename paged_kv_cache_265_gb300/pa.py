@@ -54,6 +54,9 @@ _SIGS = {
     "pa_set_decode_math": (_c_int, [_c_int]),
     "pa_profile_enable": (_c_int, [_c_int]),
     "pa_profile_read": (_c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
+    "pa_profile_read_parts": (_c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float),
+                                       ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
+    "pa_set_wait_limit_ns": (_c_int, [ctypes.c_ulonglong]),
     "pa_last_launch_count": (_c_int, []),
     "pa_last_partition_size": (_c_int, []),
     "pa_version": (_c_int, []),
@@ -246,11 +249,9 @@ def alloc_workspace(num_seqs: int, q_len: int, num_heads: int, head_dim: int, ma
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
 
 
-def decode_attention(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
-                     block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, max_context_len: int,
-                     workspace: torch.Tensor, partition_size: int = 0, stream=None) -> torch.Tensor:
-    """Paged decode attention.  query/out are [N, Hq, d] (one query row) or [N, q_len, Hq, d]
-    (q_len rows, causal inside the chunk)."""
+def _decode_shapes(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                   block_tables: torch.Tensor, context_lens: torch.Tensor):
+    """Checks the tensors of a 16-bit decode call; returns (N, q_len, Hq, Hkv, d, block_size, num_blocks)."""
     if query.dim() == 3:
         n, hq, d = query.shape
         q_len = 1
@@ -269,6 +270,15 @@ def decode_attention(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Te
         raise ValueError("block_tables and context_lens must be int32")
     if block_tables.dim() != 2 or block_tables.shape[0] != n or context_lens.shape != (n,):
         raise ValueError("block_tables must be [N, max_blocks] and context_lens [N]")
+    return n, q_len, hq, hkv, d, bs, nb
+
+
+def decode_attention(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                     block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, max_context_len: int,
+                     workspace: torch.Tensor, partition_size: int = 0, stream=None) -> torch.Tensor:
+    """Paged decode attention (pa_decode_attention_ex).  query/out are [N, Hq, d] (one query row)
+    or [N, q_len, Hq, d] (q_len rows, causal inside the chunk)."""
+    n, q_len, hq, hkv, d, bs, nb = _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens)
     with _device_of(out, query, key_cache, value_cache, block_tables, context_lens, workspace, stream=stream):
         st = lib().pa_decode_attention_ex(
             _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
@@ -279,6 +289,44 @@ def decode_attention(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Te
     return out
 
 
+def decode_attention_single(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                            value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                            scale: float, max_context_len: int, workspace: torch.Tensor, stream=None) -> torch.Tensor:
+    """pa_decode_attention: one query token per sequence, query/out [N, Hq, d]; the library
+    chooses the split."""
+    if query.dim() != 3:
+        raise ValueError("query must be [N, Hq, d]")
+    n, _, hq, hkv, d, bs, nb = _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens)
+    with _device_of(out, query, key_cache, value_cache, block_tables, context_lens, workspace, stream=stream):
+        st = lib().pa_decode_attention(
+            _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+            _dev(block_tables, "block_tables"), block_tables.shape[1], _dev(context_lens, "context_lens"), n, hq, hkv,
+            d, bs, nb, int(max_context_len), float(scale), dtype_code(query), _dev(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("pa_decode_attention", st)
+    return out
+
+
+def decode_attention_multiquery(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                                value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                scale: float, max_context_len: int, workspace: torch.Tensor,
+                                stream=None) -> torch.Tensor:
+    """pa_decode_attention_multiquery: q_len query rows per sequence, query/out [N, q_len, Hq, d],
+    causal inside the chunk; the library chooses the split (and the tcgen05 kernel from 128 rows
+    per kv head)."""
+    if query.dim() != 4:
+        raise ValueError("query must be [N, q_len, Hq, d]")
+    n, q_len, hq, hkv, d, bs, nb = _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens)
+    with _device_of(out, query, key_cache, value_cache, block_tables, context_lens, workspace, stream=stream):
+        st = lib().pa_decode_attention_multiquery(
+            _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+            _dev(block_tables, "block_tables"), block_tables.shape[1], _dev(context_lens, "context_lens"), n, q_len,
+            hq, hkv, d, bs, nb, int(max_context_len), float(scale), dtype_code(query), _dev(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("pa_decode_attention_multiquery", st)
+    return out
+
+
 def decode_attention_noalloc(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                              value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
                              scale: float, max_context_len: int, partition_size: int = 0, stream=None) -> torch.Tensor:
@@ -286,24 +334,7 @@ def decode_attention_noalloc(out: torch.Tensor, query: torch.Tensor, key_cache: 
     memory: the split-K scratch comes from the library's fixed 32 MiB device array.  Calls share
     that array, so calls that overlap on the GPU must not be issued; a problem needing more
     scratch than the array holds raises PaError (status PA_ERR_WORKSPACE)."""
-    if query.dim() == 3:
-        n, hq, d = query.shape
-        q_len = 1
-    elif query.dim() == 4:
-        n, q_len, hq, d = query.shape
-    else:
-        raise ValueError("query must be [N, Hq, d] or [N, q_len, Hq, d]")
-    if out.shape != query.shape or out.dtype != query.dtype:
-        raise ValueError("out must match query in shape and dtype")
-    nb, bs, hkv, d2 = key_cache.shape
-    if d2 != d or value_cache.shape != key_cache.shape:
-        raise ValueError("cache shape mismatch")
-    if query.dtype != key_cache.dtype or value_cache.dtype != key_cache.dtype:
-        raise ValueError("query and caches must share one dtype")
-    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
-        raise ValueError("block_tables and context_lens must be int32")
-    if block_tables.dim() != 2 or block_tables.shape[0] != n or context_lens.shape != (n,):
-        raise ValueError("block_tables must be [N, max_blocks] and context_lens [N]")
+    n, q_len, hq, hkv, d, bs, nb = _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens)
     with _device_of(out, query, key_cache, value_cache, block_tables, context_lens, stream=stream):
         st = lib().pa_decode_attention_noalloc(
             _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
@@ -335,14 +366,30 @@ def last_partition_size() -> int:
     return int(lib().pa_last_partition_size())
 
 
-def profile_enable(on: bool = True) -> None:
+def profile_enable(on=True) -> None:
+    """True / 1: time the plan, main and merge kernels of every decode call apart; 2: time the
+    main and merge kernels together (their overlap kept); False / 0: stop."""
     _check("pa_profile_enable", lib().pa_profile_enable(int(on)))
 
 
 def profile_read() -> tuple[float, int]:
+    """(summed ms of the main kernel, calls) since the last read."""
     ms, n = ctypes.c_float(0.0), ctypes.c_int(0)
     _check("pa_profile_read", lib().pa_profile_read(ctypes.byref(ms), ctypes.byref(n)))
     return float(ms.value), int(n.value)
+
+
+def profile_read_parts() -> tuple[float, float, float, int]:
+    """(summed ms of the plan, main and merge kernels, calls) since the last read."""
+    a, b, c, n = ctypes.c_float(0.0), ctypes.c_float(0.0), ctypes.c_float(0.0), ctypes.c_int(0)
+    _check("pa_profile_read_parts",
+           lib().pa_profile_read_parts(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), ctypes.byref(n)))
+    return float(a.value), float(b.value), float(c.value), int(n.value)
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Limit of the kernels' pipeline waits for later launches (a test hook); 0 = the default 2 s."""
+    _check("pa_set_wait_limit_ns", lib().pa_set_wait_limit_ns(int(ns)))
 
 
 def last_launch_count() -> int:

@@ -53,7 +53,8 @@ def test_dram_counters_count_only_for_the_sources_they_were_taken_on(monkeypatch
     with open(os.path.join(ROOT, "profiles", "decode_kernel_traffic.json")) as f:
         entry = json.load(f)["gqa_batch128"]
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: entry["source_hash"])
-    assert bench.ncu_traffic("gqa_batch128") == entry["dram_bytes_per_launch_full"]
+    assert bench.ncu_traffic("gqa_batch128") == {"partition": entry["dram_bytes_per_launch_full"],
+                                                  "merge": entry.get("merge_dram_bytes_per_launch")}
     assert bench.ncu_traffic("no_such_workload") is None
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
     assert bench.ncu_traffic("gqa_batch128") is None

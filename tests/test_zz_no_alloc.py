@@ -40,12 +40,16 @@ def test_noalloc_matches_workspace_entry_point_twice(gpu):
     step = G.GpuStep(w)
     step.append()
     ref = G.to_bits(step.attend().clone())
+    outs = [torch.full_like(step.query, float("nan")) for _ in range(2)]
+    torch.cuda.synchronize()
     for call in range(2):
-        out = torch.full_like(step.query, float("nan"))
-        pa.decode_attention_noalloc(out, step.query, step.key_cache, step.value_cache, step.block_tables,
+        free_before = torch.cuda.mem_get_info()[0]
+        pa.decode_attention_noalloc(outs[call], step.query, step.key_cache, step.value_cache, step.block_tables,
                                     step.context_lens, w.scale, w.max_context_len)
         torch.cuda.synchronize()
-        got = G.to_bits(out)
+        if call == 1:   # the first call may load the library's kernels; the second allocates nothing
+            assert torch.cuda.mem_get_info()[0] == free_before, "device memory changed during the call"
+        got = G.to_bits(outs[call])
         G.compare(got, G.bits_to_f64(ref, w.dtype), w.dtype, f"noalloc call {call}")
         assert np.array_equal(got, ref), f"call {call} differs from the workspace entry point"
     assert pa.get_device_error(clear=True) == 0
@@ -65,6 +69,40 @@ def test_noalloc_multiquery_and_small_partitions(gpu):
         got = G.to_bits(out)
         G.compare(got, G.bits_to_f64(ref, w.dtype), w.dtype, "noalloc multi-query")
         assert np.array_equal(got, ref)
+    assert pa.get_device_error(clear=True) == 0
+
+
+def test_noalloc_prefill_chunk_needs_no_scratch(gpu):
+    """A chunk with >= 128 query rows per kv head runs on the tcgen05 kernel, which uses no
+    scratch: the call is accepted even where a split of the same shape would not fit the array,
+    and it matches the oracle."""
+    G = gpu
+    w = W.make_workload("noalloc_chunk", [600, 1400], num_heads=32, num_kv_heads=8, head_dim=128, q_len=64,
+                        num_blocks=140, seed=43)
+    step = G.GpuStep(w)
+    step.append()
+    torch.cuda.synchronize()
+    for call in range(2):
+        out = torch.full_like(step.query, float("nan"))
+        pa.decode_attention_noalloc(out, step.query, step.key_cache, step.value_cache, step.block_tables,
+                                    step.context_lens, w.scale, w.max_context_len)
+        torch.cuda.synchronize()
+        assert pa.last_partition_size() == 0          # the tcgen05 kernel, no split
+        _, _, ref = G.oracle_step(w)
+        G.compare(G.to_bits(out), ref, w.dtype, f"noalloc chunk call {call}")
+    # a 512-row chunk per kv head over a 131072-token bound: a split layout of 256 partitions would
+    # need far more than the array holds, the tcgen05 kernel needs none of it
+    big = W.make_workload("noalloc_big_bound", [700], num_heads=32, num_kv_heads=8, head_dim=128, q_len=128,
+                          num_blocks=60, seed=44, max_blocks_per_seq=8192)
+    assert pa.workspace_size(1, 128, 32, 128, 131072) > pa.NOALLOC_WORKSPACE_BYTES
+    bstep = G.GpuStep(big)
+    bstep.append()
+    out = torch.empty_like(bstep.query)
+    pa.decode_attention_noalloc(out, bstep.query, bstep.key_cache, bstep.value_cache, bstep.block_tables,
+                                bstep.context_lens, big.scale, 131072)
+    torch.cuda.synchronize()
+    _, _, ref = G.oracle_step(big)
+    G.compare(G.to_bits(out), ref, big.dtype, "noalloc chunk with a large length bound")
     assert pa.get_device_error(clear=True) == 0
 
 
