@@ -396,7 +396,15 @@ def run_ours(args, rank, world, local):
     staging = Staging(host_in, dev)
     q, nk, nv, sm, bt, cl = staging.views
     out = torch.empty_like(q)
-    ws = pa.alloc_workspace(w.num_seqs, w.q_len, w.num_heads, w.head_dim, w.max_context_len, device=dev)
+    # A batch whose sequences share prefix blocks declares them as one prefix group (as the
+    # block manager that mapped them would); the prefix is then attended once per kv head.
+    groups = None
+    if w.shared_prefix_blocks and not kv8 and not args.no_prefix_groups:
+        groups = ([0, w.num_seqs], [w.shared_prefix_blocks * w.block_size])
+        ws = pa.alloc_workspace_shared_prefix(w.num_seqs, w.q_len, w.num_heads, w.head_dim, w.max_context_len,
+                                              device=dev)
+    else:
+        ws = pa.alloc_workspace(w.num_seqs, w.q_len, w.num_heads, w.head_dim, w.max_context_len, device=dev)
     pa.set_decode_math(args.math)
     stream = torch.cuda.current_stream(dev)
     pa.get_device_error(clear=True)
@@ -412,7 +420,11 @@ def run_ours(args, rank, world, local):
             return n1 + pa.last_launch_count()
         pa.reshape_and_cache(nk_, nv_, kc, vc, sm_, stream=stream)
         n1 = pa.last_launch_count()
-        pa.decode_attention(o, q_, kc, vc, bt_, cl_, w.scale, w.max_context_len, ws, stream=stream)
+        if groups:
+            pa.decode_attention_shared_prefix(o, q_, kc, vc, bt_, cl_, w.scale, w.max_context_len, ws, *groups,
+                                              stream=stream)
+        else:
+            pa.decode_attention(o, q_, kc, vc, bt_, cl_, w.scale, w.max_context_len, ws, stream=stream)
         return n1 + pa.last_launch_count()
 
     for _ in range(max(3, args.warmup)):
@@ -562,9 +574,11 @@ def run_ours(args, rank, world, local):
     achieved_k2 = attn_bytes / (kern_ms * 1e-3) / 1e9
     # The library runs a call with >= 128 query rows per kv head (and the default split) on the
     # tcgen05 prefill kernel, everything else on the split-K decode kernel.
-    tc_path = not kv8 and (args.math == "tcgen05" or
-                           (args.math == "auto" and (w.num_heads // w.num_kv_heads) * w.q_len >= 128))
-    kernel_name = ("prefill_tc_kernel (tcgen05, no split)" if tc_path else
+    tc_path = not kv8 and not groups and (args.math == "tcgen05" or
+                                          (args.math == "auto" and (w.num_heads // w.num_kv_heads) * w.q_len >= 128))
+    kernel_name = ("prefill_tc_kernel (tcgen05, no split)" if tc_path and not groups else
+                   "prefix_tc_kernel + decode_kernel + merge_kernel (shared prefix on tcgen05, the rest split-K, "
+                   "log-sum-exp merge)" if groups else
                    "decode_kernel + merge_kernel (split-K partition pass and log-sum-exp merge)")
     t = ncu_traffic(args.workload) if not kv8 and not tc_path and args.math == "auto" else None
     traffic = t["partition"] + t["merge"] if t and t["partition"] and t["merge"] is not None else None
@@ -577,7 +591,7 @@ def run_ours(args, rank, world, local):
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": DESCR[cfg], "seq_tokens_per_step": seq_tokens, "bytes_per_step": step_bytes,
                    "attention_bytes": attn_bytes, "partition_tokens": partition_used or None, "math": args.math,
-                   "kv_cache": args.kv,
+                   "kv_cache": args.kv, "prefix_groups": len(groups[1]) if groups else 0,
                    "l2": "flushed between steps" if flush is not None else
                    f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step vs 129 MB L2)",
                    "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
@@ -709,6 +723,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa_batch128")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefix-groups", action="store_true",
+                    help="run a shared-prefix batch through the plain multi-query call (no prefix group declared)")
     ap.add_argument("--op", choices=["decode_step", "copy_blocks", "spec_verify"], default="decode_step",
                     help="decode_step: the timed hot path; copy_blocks / spec_verify: those steps alone")
     ap.add_argument("--kv", choices=["16bit", "fp8"], default="16bit",

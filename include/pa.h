@@ -230,6 +230,50 @@ int pa_decode_attention_ex(void* out, const void* query, const void* key_cache, 
                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Multi-query decode attention over sequences that share a prefix of pool blocks.
+ * Where sequences share blocks ([P1] section "KV Cache 又大又碎，为何不用操作系统分页的
+ * 思路管它？": parallel samples share one prompt, beam-search branches a prefix, and one
+ * physical block is mapped by the logical blocks of many sequences under a reference count;
+ * [P2] section 1.6 and its prefix-caching example: requests that hit the same cached prefix
+ * blocks reuse them), the prefix's K/V are the same for every sharing sequence.  This call
+ * computes exactly what pa_decode_attention_multiquery computes, but attends the shared
+ * prefix once per kv head for the query rows of all sequences of a group together (on the
+ * tcgen05 tensor cores, 128 rows at a time), the rest of each sequence with the split-K
+ * partition pass, and merges the pieces by their log-sum-exp (the blockwise softmax of [P1]
+ * and the tiling of [P3] section 4.2 change the order of the sums, not the result).
+ *
+ * Groups (HOST arrays, read before the call returns):
+ *   num_groups        0 .. PA_MAX_PREFIX_GROUPS
+ *   group_seq_start   [num_groups + 1], non-decreasing, in [0, num_seqs]: group k is
+ *                     sequences group_seq_start[k] .. group_seq_start[k + 1] - 1; sequences
+ *                     outside [group_seq_start[0], group_seq_start[num_groups]) share nothing
+ *   group_prefix_len  [num_groups] positions, a multiple of 16 (whole blocks), 0 for a group
+ *                     that shares nothing, and at most max_context_len - q_len
+ * Contract: every sequence i of group k maps its block-table entries 0 .. len/16 - 1 to the
+ * same physical blocks as the group's first sequence (only the first sequence's entries are
+ * read), and context_lens[i] - q_len >= len (the chunk's rows lie after the prefix and each
+ * sees all of it); a sequence that breaks the length rule sets PA_DEVERR_CONTEXT and its rows
+ * are left untouched.  Everything else as pa_decode_attention_multiquery (16-bit caches; the
+ * prefix pass uses the tcgen05 kernel whatever pa_set_decode_math says).  The workspace must
+ * hold pa_decode_workspace_size_shared_prefix() bytes for the same partition size (0: the
+ * library chooses 128 to 2048 tokens for the positions after the prefixes).  Results agree
+ * with pa_decode_attention_multiquery within fp32 rounding.
+ */
+#define PA_MAX_PREFIX_GROUPS 256
+
+size_t pa_decode_workspace_size_shared_prefix(int num_seqs, int q_len, int num_heads, int head_dim,
+                                              int max_context_len, int partition_size);
+
+int pa_decode_attention_shared_prefix(void* out, const void* query, const void* key_cache,
+                                      const void* value_cache, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                                      int q_len, int num_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int64_t num_blocks, int max_context_len, float scale,
+                                      int dtype, int num_groups, const int32_t* group_seq_start,
+                                      const int32_t* group_prefix_len, int partition_size, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
+/*
  * Decode attention that allocates nothing, not even a workspace argument.
  * (The pages describe no such call; it exists for callers of this library.)
  *

@@ -285,6 +285,62 @@ int pa_decode_attention_noalloc(void* out, const void* query, const void* key_ca
     return run_decode(a, stream);
 }
 
+size_t pa_decode_workspace_size_shared_prefix(int num_seqs, int q_len, int num_heads, int head_dim,
+                                              int max_context_len, int partition_size) {
+    if (num_seqs < 0 || q_len < 1 || num_heads < 1 || head_dim < 1 || max_context_len < 1) return 0;
+    if (partition_size == 0) partition_size = pa::kMinPrefixPartition;
+    if (partition_size < 0 || partition_size % PA_BLOCK_SIZE != 0) return 0;
+    return pa::ws_layout(num_seqs, q_len, num_heads, head_dim, max_context_len, partition_size, true).total;
+}
+
+int pa_decode_attention_shared_prefix(void* out, const void* query, const void* key_cache, const void* value_cache,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* context_lens, int num_seqs, int q_len, int num_heads,
+                                      int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                      int max_context_len, float scale, int dtype, int num_groups,
+                                      const int32_t* group_seq_start, const int32_t* group_prefix_len,
+                                      int partition_size, void* workspace, size_t workspace_bytes, void* stream) {
+    t_last_launches = 0;
+    const int st = check_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                                context_lens, num_seqs, q_len, num_heads, num_kv_heads, head_dim, block_size,
+                                num_blocks, max_context_len, scale, dtype, partition_size);
+    if (st != PA_OK) return st;
+    if (num_groups < 0 || num_groups > PA_MAX_PREFIX_GROUPS) return PA_ERR_INVALID_ARG;
+    if (num_groups > 0 && (!group_seq_start || !group_prefix_len)) return PA_ERR_INVALID_ARG;
+    // The group table, validated on the host and handed to the kernels by value.
+    pa::PrefixGroups g;
+    g.n = num_groups;
+    g.tile_start[0] = 0;
+    g.seq_start[0] = 0;
+    const int group = num_heads / num_kv_heads;
+    for (int k = 0; k <= num_groups && num_groups > 0; ++k) {
+        const int v = group_seq_start[k];
+        if (v < 0 || v > num_seqs || (k > 0 && v < g.seq_start[k - 1])) return PA_ERR_INVALID_ARG;
+        g.seq_start[k] = v;
+    }
+    for (int k = 0; k < num_groups; ++k) {
+        const int len = group_prefix_len[k];
+        if (len < 0 || len % PA_BLOCK_SIZE != 0 || (len > 0 && len > max_context_len - q_len))
+            return PA_ERR_INVALID_ARG;
+        g.len[k] = len;
+        const long long rows = (long long)(g.seq_start[k + 1] - g.seq_start[k]) * group * q_len;
+        const long long tiles = len > 0 ? (long long)num_kv_heads * ((rows + 127) / 128) : 0;
+        const long long next = g.tile_start[k] + tiles;
+        if (next > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+        g.tile_start[k + 1] = (int)next;
+    }
+    if (num_seqs == 0) return PA_OK;
+    pa::DecodeArgs a = decode_args(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                                   context_lens, num_seqs, q_len, num_heads, num_kv_heads, head_dim, num_blocks,
+                                   max_context_len, scale, dtype, partition_size, workspace);
+    if (partition_size == 0) a.partition = pa::kMinPrefixPartition;
+    const size_t need =
+        pa::ws_layout(num_seqs, q_len, num_heads, head_dim, max_context_len, a.partition, true).total;
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+    a.groups = &g;
+    return run_decode(a, stream);
+}
+
 int pa_get_device_error(int32_t* host_flags, int clear, void* stream) {
     if (!host_flags) return PA_ERR_INVALID_ARG;
     return pa::read_device_error(host_flags, clear, static_cast<cudaStream_t>(stream));

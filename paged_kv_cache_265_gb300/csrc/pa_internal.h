@@ -12,14 +12,15 @@
 namespace pa {
 
 // Workspace of one decode call (byte offsets from the workspace base).
-//   header      int32[64]: [0] = number of (sequence, partition) work entries,
-//               [1] = dynamic work counter
+//   header      int32[64]: [0] = number of work entries, [1] = dynamic work counter
 //   part_start  int32[N+1]: first partial slot of each sequence (exclusive scan)
-//   units       int4[N * Pmax]: work entries (sequence, partition, context length,
-//               first partial slot), full partitions first, then each
-//               sequence's shorter last partition
-//   pml         float2[slots, q_len, Hq]: per-partition (max, sum) in log2 units
-//   pacc        float[slots, q_len, Hq, D]: per-partition unnormalised outputs
+//   units       int4[N * Pmax]: work entries (sequence, first position, context length,
+//               partial slot or -1), largest first
+//   pml         float2[slots, q_len, Hq]: per-piece (max, sum) in log2 units
+//   pacc        float[slots, q_len, Hq, D]: per-piece unnormalised outputs
+// Pmax = ceil(max_context_len / partition) pieces per sequence, plus one for a shared prefix's
+// piece when `prefix` (which also always reserves the partials: a grouped sequence merges its
+// prefix piece with the rest even when the rest is one partition).
 struct WsLayout {
     size_t header, part_start, units, pml, pacc, total;
     int pmax;
@@ -28,10 +29,11 @@ struct WsLayout {
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 inline WsLayout ws_layout(int num_seqs, int q_len, int num_heads, int head_dim, int max_context_len,
-                          int partition) {
+                          int partition, bool prefix = false) {
     WsLayout w{};
     int pmax = (max_context_len + partition - 1) / partition;
     if (pmax < 1) pmax = 1;
+    if (prefix) pmax += 1;
     const size_t n = num_seqs > 0 ? (size_t)num_seqs : 0;
     const size_t slots = n * (size_t)pmax;
     size_t off = 0;
@@ -51,6 +53,38 @@ inline WsLayout ws_layout(int num_seqs, int q_len, int num_heads, int head_dim, 
     w.total = off;
     w.pmax = pmax;
     return w;
+}
+
+// Sequences that share a prefix of pool blocks: group k covers sequences seq_start[k] ..
+// seq_start[k + 1] - 1, whose first len[k] positions (a multiple of 16; 0 = no sharing) lie in
+// the same physical blocks, those named by the group's first sequence's block table.  Passed
+// by value to the kernels that need it.
+constexpr int kMaxPrefixGroups = 256;
+struct PrefixGroups {
+    int n;                                // number of groups
+    int seq_start[kMaxPrefixGroups + 1];
+    int len[kMaxPrefixGroups];
+    int tile_start[kMaxPrefixGroups + 1]; // first prefix-kernel CTA of each group
+};
+
+// Shared-prefix positions of sequence i (0 outside every group).
+__host__ __device__ inline int prefix_of(const PrefixGroups& g, int i) {
+    if (g.n <= 0 || i < g.seq_start[0] || i >= g.seq_start[g.n]) return 0;
+    int lo = 0, hi = g.n - 1;  // the last group whose start is <= i
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (g.seq_start[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    return g.len[lo];
+}
+
+// Whether a sequence of length L can be computed: at least one position and the q_len
+// query rows, within the stated bound and the block table; with a shared prefix of `skip`
+// positions, every query row must see the whole prefix (L - q_len >= skip).
+__host__ __device__ inline bool seq_len_valid(int L, int q_len, int skip, int max_context_len,
+                                              int max_blocks_per_seq) {
+    return L >= 1 && L >= q_len && L <= max_context_len && (L + 15) / 16 <= max_blocks_per_seq &&
+           (skip == 0 || L - q_len >= skip);
 }
 
 struct DecodeArgs {
@@ -76,6 +110,7 @@ struct DecodeArgs {
     float k_scale = 1.f;  // their dequantisation scales
     float v_scale = 1.f;
     bool partition_auto = false;  // the caller passed partition size 0 (the library chooses)
+    const PrefixGroups* groups = nullptr;  // shared prefixes (pa_decode_attention_shared_prefix)
 };
 
 // Launchers: return a pa_status; `launches` receives the number of kernels enqueued.
@@ -88,6 +123,13 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int* launches, int* 
 // when use_prefill_tc() holds (that path does not split and uses no workspace).
 int launch_prefill_tc(const DecodeArgs& a, cudaStream_t stream, int* launches);
 bool use_prefill_tc(const DecodeArgs& a);
+// The shared prefixes of a.groups on tcgen05 (pa_prefill.cu): one CTA per (group, kv head,
+// 128-row tile), each writing its rows' prefix pieces into the partials at part_start.
+int launch_prefix_tc(const DecodeArgs& a, const int* part_start, float2* pml, float* pacc, cudaStream_t stream,
+                     int* launches);
+// Smallest split-K partition the library chooses for a shared-prefix call (the workspace of a
+// call with partition 0 is sized for it).
+constexpr int kMinPrefixPartition = 128;
 int launch_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* target_probs,
                        const float* draft_probs, const int32_t* draft_tokens, const float* u_accept,
                        const float* u_sample, int num_seqs, int k, int vocab, cudaStream_t stream, int* launches);

@@ -416,35 +416,41 @@ __device__ int block_exclusive_scan(int v, int* scratch32, int& total) {
     return before + x - v;
 }
 
-// Partitions of sequence i (0 past the batch or for an invalid length, which is flagged);
-// its context length goes to L.
-__device__ __forceinline__ int seq_parts(const PlanParams& p, int i, int& L) {
-    L = 0;
-    if (i >= p.num_seqs) return 0;
-    L = p.context_lens[i];
-    const bool ok = L >= 1 && L >= p.q_len && L <= p.max_context_len &&
-                    (L + kBlock - 1) / kBlock <= p.max_blocks_per_seq;
-    if (!ok) {
+// One sequence as the plan sees it: its length, the shared-prefix positions another kernel
+// computes for it (0 without a prefix group), how many of its partial results the merge
+// combines (`pieces`: the prefix piece, if any, then the split-K partitions of the rest;
+// 0 for an invalid length, which is flagged) and its first partial slot.
+struct PlanSeq {
+    int len, skip, pieces, slot;
+};
+
+__device__ __forceinline__ PlanSeq plan_seq(const PlanParams& p, const PrefixGroups* g, int i) {
+    PlanSeq s{0, 0, 0, 0};
+    if (i >= p.num_seqs) return s;
+    s.len = p.context_lens[i];
+    s.skip = g ? prefix_of(*g, i) : 0;
+    if (!seq_len_valid(s.len, p.q_len, s.skip, p.max_context_len, p.max_blocks_per_seq)) {
         atomicOr(&g_pa_error, PA_DEVERR_CONTEXT);
-        return 0;
+        return s;
     }
-    return (L + p.partition - 1) / p.partition;
+    s.pieces = (s.skip > 0) + (s.len - s.skip + p.partition - 1) / p.partition;
+    return s;
 }
 
-// Size bucket of a partition: its block count, capped; larger buckets go first.
+// Size bucket of a work entry: its block count, capped; larger buckets go first.
 constexpr int kPlanBuckets = 64;
-__device__ __forceinline__ int part_bucket(const PlanParams& p, int L, int part) {
-    const int nb = (min(p.partition, L - part * p.partition) + kBlock - 1) / kBlock;
+__device__ __forceinline__ int part_bucket(const PlanParams& p, int L, int tok0) {
+    const int nb = (min(p.partition, L - tok0) + kBlock - 1) / kBlock;
     return min(nb, kPlanBuckets - 1);
 }
 
-// One CTA: numbers each sequence's partitions (part_start), then lays the
-// (sequence, partition) entries out largest first (a counting sort on block
-// count), so that CTAs taking entries in order finish close together.  The
-// order within a size bucket does not affect any result.
-__global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
-    griddep_launch_dependents();  // the partition pass may start its set-up now ...
-    griddep_wait();               // ... but the lengths may come from the kernel before this one
+// One CTA: numbers each sequence's partial results (part_start), then lays the work entries
+// (sequence, first position, length, partial slot or -1 when the entry is the sequence's only
+// piece and writes the output itself) out largest first (a counting sort on block count), so
+// that CTAs taking entries in order finish close together.  The order within a size bucket
+// does not affect any result.  With prefix groups, a grouped sequence's entries cover only the
+// positions after its shared prefix; its partial slot part_start[i] is the prefix piece's.
+__device__ __forceinline__ void plan_body(const PlanParams& p, const PrefixGroups* g) {
     static_assert(kPlanBuckets == 64, "the bucket scan below gives each lane of one warp two buckets");
     __shared__ int scratch[32];
     __shared__ int hist[kPlanBuckets];
@@ -452,22 +458,19 @@ __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
     __syncthreads();
     // Each thread keeps its first sequence (all of them, up to 1024 sequences) in registers
     // for the second pass.
-    int carry = 0, L0 = 0, np0 = 0, slot0 = 0;
+    int carry = 0;
+    PlanSeq s0{0, 0, 0, 0};
     for (int base = 0; base < p.num_seqs; base += 1024) {
         const int i = base + threadIdx.x;
-        int L;
-        const int np = seq_parts(p, i, L);
+        PlanSeq s = plan_seq(p, g, i);
         int tot;
-        const int slot = carry + block_exclusive_scan(np, scratch, tot);
+        s.slot = carry + block_exclusive_scan(s.pieces, scratch, tot);
         if (i < p.num_seqs) {
-            p.part_start[i] = slot;
-            for (int c = 0; c < np; ++c) atomicAdd(&hist[part_bucket(p, L, c)], 1);
+            p.part_start[i] = s.slot;
+            for (int tok0 = s.skip; tok0 < s.len && s.pieces > 0; tok0 += p.partition)
+                atomicAdd(&hist[part_bucket(p, s.len, tok0)], 1);
         }
-        if (base == 0) {
-            L0 = L;
-            np0 = np;
-            slot0 = slot;
-        }
+        if (base == 0) s0 = s;
         carry += tot;
     }
     __syncthreads();
@@ -486,25 +489,39 @@ __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
         const int start = x - (n0 + n1);
         hist[b0] = start;
         hist[b1] = start + n0;
+        if (lane == 31) p.header[0] = x;  // work entries (every bucket counted)
         if (lane == 0) {
             p.part_start[p.num_seqs] = carry;
-            p.header[0] = carry;
             p.header[1] = 0;
         }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) {
-        int L = L0, np = np0, slot = slot0;
+        PlanSeq s = s0;
         if (i >= 1024) {
-            np = seq_parts(p, i, L);
-            slot = p.part_start[i];
+            s = plan_seq(p, g, i);
+            s.slot = p.part_start[i];
         }
-        if (np == 0) continue;
-        for (int c = 0; c < np; ++c) {
-            const int pos = atomicAdd(&hist[part_bucket(p, L, c)], 1);
-            p.units[pos] = make_int4(i, c, L, slot);
+        if (s.pieces == 0) continue;
+        int slot = s.pieces == 1 ? -1 : s.slot + (s.skip > 0);
+        for (int tok0 = s.skip; tok0 < s.len; tok0 += p.partition) {
+            const int pos = atomicAdd(&hist[part_bucket(p, s.len, tok0)], 1);
+            p.units[pos] = make_int4(i, tok0, s.len, slot);
+            if (slot >= 0) ++slot;
         }
     }
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
+    griddep_launch_dependents();  // the partition pass may start its set-up now ...
+    griddep_wait();               // ... but the lengths may come from the kernel before this one
+    plan_body(p, nullptr);
+}
+
+__global__ void __launch_bounds__(1024) plan_prefix_kernel(const PlanParams p, const __grid_constant__ PrefixGroups g) {
+    griddep_launch_dependents();
+    griddep_wait();
+    plan_body(p, &g);
 }
 
 // ---------------------------------------------------------------------------
@@ -528,7 +545,7 @@ struct alignas(128) DecodeParams {
     const int* block_tables;
     const int* header;
     int* work_counter;   // next work unit to hand out (reset by the plan kernel)
-    const int4* units;   // (seq, partition, context_len, first partial slot), largest first
+    const int4* units;   // (seq, first position, context_len, partial slot or -1), largest first
     float2* pml;
     float* pacc;
     long long num_blocks;
@@ -544,14 +561,17 @@ struct alignas(128) DecodeParams {
     int stages;        // ring length, a multiple of block_splits, <= kMaxStages
     int mtiles;        // ceil(rows / 16) tensor-core row tiles
     int block_splits;  // kConsumerWarps / mtiles warps share a tile's blocks
-    int slot_rows;     // min(16, rows): rows each warp leaves in the combine buffer
+    int slot_rows;     // min(8 NT, rows): rows each warp leaves in the combine buffer
     float scale_log2;  // scale * log2(e) (times the K dequantisation scale for an FP8 cache)
     float v_scale;     // V dequantisation scale (1 for 16-bit caches)
     unsigned long long wait_limit_ns;  // limit of the pipeline waits (pa_set_wait_limit_ns)
 };
 
+// One work unit: positions tok0 .. tok0 + ntok - 1 of sequence `seq` (length len) for the kv
+// head's query rows row0 .. row0 + nrows - 1; its result goes to partial slot `slot`, or
+// straight to the output when slot < 0 (the sequence's only piece).
 struct UnitInfo {
-    int seq, part, len, slot0, kvh, ntok, row0, nrows;  // rows row0 .. row0+nrows-1 of the kv head
+    int seq, tok0, len, slot, kvh, ntok, row0, nrows;
 };
 
 struct SmemLayout {
@@ -563,6 +583,8 @@ struct SmemLayout {
 // Per consumer warp, the CUDA-core path exchanges P (8 rows x 16 tokens) and the
 // 8 rows' rescale factors through shared memory.
 constexpr int kFmaWarpFloats = 8 * 16 + 8;
+// Per consumer warp, slots for the running (max, sum) of up to this many query rows.
+constexpr int kCombRows = 32;
 
 __host__ __device__ inline SmemLayout smem_layout(int head_dim, int stages, int mtiles, int tile_rows, int slot_rows,
                                                   bool fma = false, bool f8 = false) {
@@ -574,8 +596,8 @@ __host__ __device__ inline SmemLayout smem_layout(int head_dim, int stages, int 
     s.off_q = stages * s.stage_bytes;
     s.off_comb = s.off_q + 2 * s.q_half_bytes;
     s.off_m = s.off_comb + kConsumerWarps * slot_rows * head_dim * 4;
-    s.off_l = s.off_m + kConsumerWarps * 16 * 4;
-    s.off_bars = s.off_l + kConsumerWarps * 16 * 4;
+    s.off_l = s.off_m + kConsumerWarps * kCombRows * 4;
+    s.off_bars = s.off_l + kConsumerWarps * kCombRows * 4;
     s.off_info = s.off_bars + (2 * kMaxStages + 4) * 8;
     s.off_fma = s.off_info + 2 * (int)sizeof(UnitInfo) + 16;
     s.total = s.off_fma + (fma ? kConsumerWarps * kFmaWarpFloats * 4 : 0) + 1024;  // + alignment slack
@@ -730,7 +752,6 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
         // ===================== producer warp =====================
         const uint64_t pol_stream = l2_policy_evict_first();
         const uint64_t pol_keep = l2_policy_evict_last();
-        const int blocks_per_part = p.partition / kBlock;
         uint32_t k = 0;
         int ul = 0;
         bool ok = true;
@@ -744,10 +765,9 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
         int bids = 0;
         if (u < total_units) {
             cur = p.units[u / units_per_entry];
-            const int nb0 = ((min(p.partition, cur.z - cur.y * p.partition)) + kBlock - 1) / kBlock;
+            const int nb0 = ((min(p.partition, cur.z - cur.y)) + kBlock - 1) / kBlock;
             if (lane < nb0)
-                bids = __ldg(p.block_tables + (long long)cur.x * p.max_blocks_per_seq +
-                             (long long)cur.y * blocks_per_part + lane);
+                bids = __ldg(p.block_tables + (long long)cur.x * p.max_blocks_per_seq + cur.y / kBlock + lane);
         }
         for (; ok; ++ul) {
             const int qb = ul & 1;
@@ -768,8 +788,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
             const int kvh = rem / p.row_groups;
             const int row0 = (rem - kvh * p.row_groups) * p.rows;
             const int nrows = min(p.rows, p.total_rows - row0);
-            const int seq = cur.x, part = cur.y, L = cur.z;
-            const int tok0 = part * p.partition;
+            const int seq = cur.x, tok0 = cur.y, L = cur.z;
             const int ntok = min(p.partition, L - tok0);
             const int nblk = (ntok + kBlock - 1) / kBlock;
             // Next unit: its number is requested now and read two blocks later, its entry is
@@ -782,9 +801,9 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
             if (lane == 0) {
                 UnitInfo ui;
                 ui.seq = seq;
-                ui.part = part;
+                ui.tok0 = tok0;
                 ui.len = L;
-                ui.slot0 = cur.w;
+                ui.slot = cur.w;
                 ui.kvh = kvh;
                 ui.ntok = ntok;
                 ui.row0 = row0;
@@ -800,7 +819,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                 bulk_g2s(smem_addr(qbuf + qb * lay.q_half_bytes + r * qpitch), src, kRowBytes, qfull0 + 8 * qb,
                          pol_keep);
             }
-            const int* bt = p.block_tables + (long long)seq * p.max_blocks_per_seq + (long long)part * blocks_per_part;
+            const int* bt = p.block_tables + (long long)seq * p.max_blocks_per_seq + tok0 / kBlock;
             const int next_at = min(nblk, 2) - 1;      // read the next unit's number, load its entry
             const int prefetch_at = min(nblk, 4) - 1;  // load its first 32 block ids
             for (int c = 0; c < nblk && ok; c += 32) {
@@ -849,10 +868,10 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                         if (un < total_units) nxt = p.units[un / units_per_entry];
                     }
                     if (c == 0 && jj == prefetch_at && un < total_units) {
-                        const int nb1 = (min(p.partition, nxt.z - nxt.y * p.partition) + kBlock - 1) / kBlock;
+                        const int nb1 = (min(p.partition, nxt.z - nxt.y) + kBlock - 1) / kBlock;
                         if (lane < nb1)
-                            nbids = __ldg(p.block_tables + (long long)nxt.x * p.max_blocks_per_seq +
-                                          (long long)nxt.y * blocks_per_part + lane);
+                            nbids = __ldg(p.block_tables + (long long)nxt.x * p.max_blocks_per_seq + nxt.y / kBlock +
+                                          lane);
                     }
                 }
             }
@@ -964,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
 
                 nblk = (ui.ntok + kBlock - 1) / kBlock;
                 nblk_pad = ((nblk + p.block_splits - 1) / p.block_splits) * p.block_splits;
-                const int tok0 = ui.part * p.partition;
+                const int tok0 = ui.tok0;
                 // Last position (relative to the partition) each of this lane's rows may see:
                 // row j of the q_len-row chunk is position L - q_len + j.
                 int lim[NT][2];
@@ -984,7 +1003,10 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                         ok = false;
                         break;
                     }
-                    if (j < nblk) {  // data-free padding stages are only waited for and released
+                    // Data-free padding stages are only waited for and released, and so is every stage
+                    // by a warp whose row tile holds only padding rows (a third row tile rounded up to
+                    // four): its results are never read.
+                    if (j < nblk && rows_here > 0) {
                         const uint32_t kst = smem_addr(stage_base + s * lay.stage_bytes);
                         const uint32_t vst = kst + kBoxes * kBoxBytes;
                         // smem row i holds token i - shift of this block (shift > 0 only for a short last block)
@@ -1128,7 +1150,8 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                         }
                     }
                     __syncwarp();
-                    if (lane == 0 && !(F8 && j < nblk)) mbar_arrive(empty0 + 8 * s);  // FP8: released after its loads
+                    // (FP8: a computing warp released the stage right after its loads)
+                    if (lane == 0 && !(F8 && j < nblk && rows_here > 0)) mbar_arrive(empty0 + 8 * s);
                 }
             }
             k += nblk_pad;
@@ -1160,8 +1183,8 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                                 }
                             }
                             if (gid == 0) {
-                                comb_m[warp * 16 + row] = m[nt][c];
-                                comb_l[warp * 16 + row] = l[nt][c];
+                                comb_m[warp * kCombRows + row] = m[nt][c];
+                                comb_l[warp * kCombRows + row] = l[nt][c];
                             }
                         }
                     }
@@ -1194,7 +1217,7 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                 if (lane == 0) mbar_arrive(qempty0 + 8 * qb);
                 nblk = (ui.ntok + kBlock - 1) / kBlock;
                 nblk_pad = ((nblk + p.block_splits - 1) / p.block_splits) * p.block_splits;
-                const int lim_r = ui.len - p.q_len + min((ui.row0 + rr) / p.group, p.q_len - 1) - ui.part * p.partition;
+                const int lim_r = ui.len - p.q_len + min((ui.row0 + rr) / p.group, p.q_len - 1) - ui.tok0;
                 for (int j = bsg; j < nblk_pad; j += p.block_splits) {
                     const uint32_t kj = k + j;
                     const int s = (int)(kj % stages);
@@ -1302,8 +1325,8 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                             *reinterpret_cast<float4*>(co + r * D + c * 8 + 4) = make_float4(o[r][4], o[r][5], o[r][6], o[r][7]);
                         }
                     if (row_owner && rr < rows_here) {
-                        comb_m[warp * 16 + rr] = m_r;
-                        comb_l[warp * 16 + rr] = l_r;
+                        comb_m[warp * kCombRows + rr] = m_r;
+                        comb_l[warp * kCombRows + rr] = l_r;
                     }
                 }
             }
@@ -1312,29 +1335,28 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
         // ordered before the reads below).
         if (consumers_any(!ok || done)) break;
         // Merge the block-split warps of each row tile; write the output or the partial.
-        const int nparts = (ui.len + p.partition - 1) / p.partition;
         const int nthreads = kConsumerWarps * 32;
         for (int idx = threadIdx.x; idx < ui.nrows * D; idx += nthreads) {
             const int r = idx / D, e = idx - r * D;
             const int tile = r / TR, rr = r - tile * TR;
             float M = -INFINITY;
-            for (int b = 0; b < p.block_splits; ++b) M = fmaxf(M, comb_m[(tile * p.block_splits + b) * 16 + rr]);
+            for (int b = 0; b < p.block_splits; ++b) M = fmaxf(M, comb_m[(tile * p.block_splits + b) * kCombRows + rr]);
             float lsum = 0.f, acc = 0.f;
             if (M != -INFINITY) {
                 for (int b = 0; b < p.block_splits; ++b) {
                     const int w = tile * p.block_splits + b;
-                    const float f = ex2(comb_m[w * 16 + rr] - M);
-                    lsum += comb_l[w * 16 + rr] * f;
+                    const float f = ex2(comb_m[w * kCombRows + rr] - M);
+                    lsum += comb_l[w * kCombRows + rr] * f;
                     acc += comb_o[(w * p.slot_rows + rr) * D + e] * f;
                 }
             }
             const int qi = (ui.row0 + r) / p.group;
             const int h = ui.kvh * p.group + (ui.row0 + r - qi * p.group);
             const long long orow = (long long)(ui.seq * p.q_len + qi) * p.num_heads + h;
-            if (nparts == 1) {
+            if (ui.slot < 0) {
                 static_cast<uint16_t*>(p.out)[orow * D + e] = Elem<T>::to_bits(acc * p.v_scale / lsum);
             } else {
-                const long long prow = ((long long)(ui.slot0 + ui.part) * p.q_len + qi) * p.num_heads + h;
+                const long long prow = ((long long)ui.slot * p.q_len + qi) * p.num_heads + h;
                 p.pacc[prow * D + e] = acc * p.v_scale;
                 if (e == 0) p.pml[prow] = make_float2(M, lsum);
             }
@@ -1348,21 +1370,20 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
 // ---------------------------------------------------------------------------
 struct MergeParams {
     void* out;
-    const int* context_lens;
     const int* part_start;
     const float2* pml;
     const float* pacc;
     int num_seqs;
     int q_len;
     int num_heads;
-    int partition;
-    int max_context_len;
 };
 
-// One warp per output row (sequence, query row, head) of a split sequence.  The
-// partitions' (max, sum) pairs are read lane-parallel and turned into weights
-// e^{m_p - M} / sum_p' e^{m_p' - M} l_p' once; the unnormalised partial outputs
-// are then summed in partition order, so the result does not depend on timing.
+// One warp per output row (sequence, query row, head) of a sequence with more than one
+// piece (part_start[i + 1] - part_start[i] partial results: split-K partitions, and a shared
+// prefix's piece first).  The pieces' (max, sum) pairs are read lane-parallel and turned into
+// weights e^{m_p - M} / sum_p' e^{m_p' - M} l_p' once; the unnormalised partial outputs are
+// then summed in slot order, so the result does not depend on timing.  Sequences with one
+// piece (written by the partition pass) or none (an invalid length) are skipped.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
     griddep_wait();  // the partition pass must have finished
@@ -1374,10 +1395,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
     const int per_seq = p.q_len * p.num_heads;
     const int seq = (int)(row / per_seq);
     const int rem = (int)(row - (long long)seq * per_seq);
-    const int L = p.context_lens[seq];
-    const long long slot0 = p.part_start[seq];  // loaded with L, not after it
-    if (L < 1 || L < p.q_len || L > p.max_context_len) return;
-    const int nparts = (L + p.partition - 1) / p.partition;
+    const long long slot0 = p.part_start[seq];
+    const int nparts = p.part_start[seq + 1] - (int)slot0;
     if (nparts <= 1) return;
     // Lane l keeps the (max, sum) pairs of partitions l and l + 32; any further ones are re-read.
     const float2 ml0 = lane < nparts ? p.pml[(slot0 + lane) * per_seq + rem] : make_float2(-INFINITY, 0.f);
@@ -1601,9 +1620,39 @@ int auto_partition(const DecodeArgs& a, int sms) {
     return best;
 }
 
+// The same choice for a shared-prefix call, over the positions after each group's prefix
+// (taken as half of what is left of max_context_len), from 128 tokens up: the suffixes are
+// short, and a finer split keeps every CTA busy.
+int auto_partition_prefix(const DecodeArgs& a, int sms) {
+    const PrefixGroups& g = *a.groups;
+    const int group = a.num_heads / a.num_kv_heads;
+    const long long total_rows = (long long)group * a.q_len;
+    const int rows = (int)std::min<long long>(PA_ROW_GROUP_ROWS, total_rows);
+    const long long row_groups = (total_rows + rows - 1) / rows;
+    int rt, nt;
+    decode_variant(rows, false, rt, nt);
+    const long long slots = (long long)sms * decode_ctas_per_sm(nt, rt, false);
+    int best = kMinPrefixPartition;
+    for (int part = kMinPrefixPartition; part <= 4 * PA_DEFAULT_PARTITION; part *= 2) {
+        long long units = 0;
+        int grouped = 0;
+        for (int k = 0; k < g.n; ++k) {
+            const int n_k = g.seq_start[k + 1] - g.seq_start[k];
+            const long long rest = std::max(16, (a.max_context_len - g.len[k]) / 2);
+            units += (long long)n_k * ((rest + part - 1) / part);
+            grouped += n_k;
+        }
+        const long long half = std::max(1, a.max_context_len / 2);
+        units += (long long)(a.num_seqs - grouped) * ((half + part - 1) / part);
+        if (units * a.num_kv_heads * row_groups >= 3 * slots) best = part;
+    }
+    return best;
+}
+
 template <typename T, int D>
 int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches) {
-    const WsLayout w = ws_layout(a.num_seqs, a.q_len, a.num_heads, D, a.max_context_len, a.partition);
+    const bool prefix = a.groups != nullptr;
+    const WsLayout w = ws_layout(a.num_seqs, a.q_len, a.num_heads, D, a.max_context_len, a.partition, prefix);
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     int* header = reinterpret_cast<int*>(ws + w.header);
     int* part_start = reinterpret_cast<int*>(ws + w.part_start);
@@ -1627,9 +1676,15 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     pp.partition = a.partition;
     pp.max_blocks_per_seq = a.max_blocks_per_seq;
     pp.max_context_len = a.max_context_len;
-    if (launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, pp) != cudaSuccess) return PA_ERR_CUDA;
+    const cudaError_t pe = prefix ? launch_pdl(plan_prefix_kernel, dim3(1), dim3(1024), 0, stream, pp, *a.groups)
+                                  : launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, pp);
+    if (pe != cudaSuccess) return PA_ERR_CUDA;
     *launches += 1;
     profile_mark(pc, 1, stream);
+    // Shared prefixes: one tcgen05 pass per (group, kv head) over every grouped row, before the
+    // partition pass takes the rest of each sequence.
+    if (prefix)
+        if (int st = launch_prefix_tc(a, part_start, pml, pacc, stream, launches)) return st;
 
     DecodeParams p;
     if (a.fp8) {
@@ -1716,15 +1771,12 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     if (w.pmax > 1) {
         MergeParams mp;
         mp.out = a.out;
-        mp.context_lens = a.context_lens;
         mp.part_start = part_start;
         mp.pml = pml;
         mp.pacc = pacc;
         mp.num_seqs = a.num_seqs;
         mp.q_len = a.q_len;
         mp.num_heads = a.num_heads;
-        mp.partition = a.partition;
-        mp.max_context_len = a.max_context_len;
         const long long rows = (long long)a.num_seqs * a.q_len * a.num_heads;
         const unsigned blocks = (unsigned)((rows * 32 + 127) / 128);
         if (launch_pdl(merge_kernel<T, D>, dim3(blocks), dim3(128), 0, stream, mp) != cudaSuccess) return PA_ERR_CUDA;
@@ -1873,12 +1925,13 @@ bool use_prefill_tc(const DecodeArgs& a) {
 
 int launch_decode(const DecodeArgs& args, cudaStream_t stream, int* launches, int* partition_used) {
     *partition_used = 0;
-    if (use_prefill_tc(args)) return launch_prefill_tc(args, stream, launches);  // no split
+    if (!args.groups && use_prefill_tc(args)) return launch_prefill_tc(args, stream, launches);  // no split
     DecodeArgs a = args;
     if (a.partition_auto) {
         DeviceInfo dev;
         if (int st = device_info(dev)) return st;
-        a.partition = auto_partition(a, dev.sms);  // >= the default, so the workspace suffices
+        // >= the partition the workspace was sized for (the default, or the smallest prefix one)
+        a.partition = a.groups ? auto_partition_prefix(a, dev.sms) : auto_partition(a, dev.sms);
     }
     *partition_used = a.partition;
     if (a.dtype == PA_BF16) {

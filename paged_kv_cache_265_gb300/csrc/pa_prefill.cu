@@ -89,6 +89,10 @@ struct PrefillTcParams {
     int max_context_len;
     float scale_log2;
     unsigned long long wait_limit_ns;  // limit of the pipeline waits (pa_set_wait_limit_ns)
+    // Shared-prefix mode: where each row's partial result goes.
+    const int* part_start;  // first partial slot of each sequence (its prefix piece)
+    float2* pml;            // (max in log2 units, sum) per partial row
+    float* pacc;            // unnormalised partial outputs, fp32
 };
 
 template <int D>
@@ -136,8 +140,63 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
+// The tile's sequence, rows and positions.  Chunk mode: one sequence's q_len chunk rows of one
+// kv head against its positions 0 .. L - 1 under the causal limits.  Prefix mode: rows of every
+// sequence of one prefix group (row r = sequence r / (g q_len), chunk token, head) against the
+// group's shared prefix, which every row sees whole.
+struct TcTile {
+    int seq;       // the sequence whose block table the tile walks (prefix mode: the group's first)
+    int kvh;
+    int row0;      // first row of the tile among the kv head's rows
+    int rows;      // rows of the kv head (past them a tile row is padding)
+    int L;         // chunk mode: the sequence's length; prefix mode: the prefix length
+    bool valid;
+    int nblk;      // pool blocks the tile streams
+    int lastblk;   // the last of them is short by sh rows (chunk mode only)
+    int sh;
+};
+
+template <bool kPrefix>
+__device__ __forceinline__ TcTile tc_tile(const PrefillTcParams& p, const PrefixGroups* g) {
+    TcTile w;
+    const int idx = blockIdx.x;
+    if constexpr (kPrefix) {
+        int lo = 0, hi = g->n - 1;  // the group whose tiles hold this CTA
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) / 2;
+            if (g->tile_start[mid] <= idx) lo = mid; else hi = mid - 1;
+        }
+        w.seq = g->seq_start[lo];
+        w.rows = (g->seq_start[lo + 1] - w.seq) * p.total_rows;
+        const int mtiles = (w.rows + kTcRows - 1) / kTcRows;
+        const int local = idx - g->tile_start[lo];
+        w.row0 = (local % mtiles) * kTcRows;
+        w.kvh = local / mtiles;
+        w.L = g->len[lo];
+        w.valid = w.L > 0;
+        w.nblk = w.L / 16;
+        w.lastblk = w.nblk - 1;
+        w.sh = 0;
+    } else {
+        // Tiles of one (sequence, kv head) are adjacent and share its K/V in L2; the
+        // last rows (the longest causal ranges) go first.
+        const int mt = p.mtiles - 1 - idx % p.mtiles;
+        w.kvh = (idx / p.mtiles) % p.num_kv_heads;
+        w.seq = idx / (p.mtiles * p.num_kv_heads);
+        w.row0 = mt * kTcRows;
+        w.rows = p.total_rows;
+        w.L = p.context_lens[w.seq];
+        w.valid = seq_len_valid(w.L, p.q_len, 0, p.max_context_len, p.max_blocks_per_seq);
+        const int t_last = min((w.row0 + kTcRows - 1) / p.group, p.q_len - 1);
+        w.nblk = w.valid ? (w.L - p.q_len + t_last) / 16 + 1 : 0;  // blocks this tile sees
+        w.lastblk = (w.L - 1) / 16;           // the sequence's last block ...
+        w.sh = 16 * (w.lastblk + 1) - w.L;    // ... is short by sh rows, fetched as leading zeros
+    }
+    return w;
+}
+
+template <typename T, int D, bool kPrefix>
+__device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const PrefixGroups* g) {
     using Lay = TcLayout<D>;
     using IsBf16 = std::integral_constant<bool, std::is_same<T, __nv_bfloat16>::value>;
     extern __shared__ uint8_t smem_raw[];
@@ -153,12 +212,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     int* err = p.err;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Tiles of one (sequence, kv head) are adjacent and share its K/V in L2; the
-    // last rows (the longest causal ranges) go first.
-    const int idx = blockIdx.x;
-    const int mt = p.mtiles - 1 - idx % p.mtiles;
-    const int kvh = (idx / p.mtiles) % p.num_kv_heads;
-    const int seq = idx / (p.mtiles * p.num_kv_heads);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcStages; ++s) {
@@ -185,18 +238,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     const uint32_t tmem = *tmem_slot;
 
     griddep_launch_dependents();
-    griddep_wait();  // the appended K/V rows and the query come from earlier kernels
+    // Chunk mode: the appended K/V rows and the query come from earlier kernels.  Prefix mode
+    // reads only the shared prefix (never appended to by this step) until its epilogue, which
+    // waits for the plan kernel's partial slots.
+    if constexpr (!kPrefix) griddep_wait();
 
-    const int L = p.context_lens[seq];
-    const bool valid = L >= p.q_len && L <= p.max_context_len && L <= p.max_blocks_per_seq * 16;
-    if (!valid && threadIdx.x == 0) atomicOr(err, PA_DEVERR_CONTEXT);  // rows left untouched
-    const int row0 = mt * kTcRows;
-    const int t_first = row0 / p.group;
-    const int t_last = min((row0 + kTcRows - 1) / p.group, p.q_len - 1);
-    const int nblk = valid ? (L - p.q_len + t_last) / 16 + 1 : 0;  // blocks this tile sees
+    const TcTile tile = tc_tile<kPrefix>(p, g);
+    const int seq = tile.seq, kvh = tile.kvh, row0 = tile.row0, L = tile.L, nblk = tile.nblk;
+    const int lastblk = tile.lastblk, sh = tile.sh;
+    const bool valid = tile.valid;
+    if (!kPrefix && !valid && threadIdx.x == 0) atomicOr(err, PA_DEVERR_CONTEXT);  // rows left untouched
     const int ntiles = (nblk + kTcBlocks - 1) / kTcBlocks;
-    const int lastblk = (L - 1) / 16;           // the sequence's last block ...
-    const int sh = 16 * (lastblk + 1) - L;      // ... is short by sh rows, fetched as leading zeros
 
     if (valid && warp == 8) {
         // ===================== TMA producer =====================
@@ -314,14 +366,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         const int hf = warp >> 2;                   // column half of the row this thread owns
         const int r = threadIdx.x & (kTcRows - 1);  // tile row = TMEM lane
         const int gr = row0 + r;
-        const bool real = gr < p.total_rows;
-        const int t = real ? gr / p.group : p.q_len - 1;
-        const int hq = kvh * p.group + (real ? gr - t * p.group : 0);
-        const int lim = L - p.q_len + t;               // last position this row sees
-        const int lim_min = L - p.q_len + t_first;     // smallest limit in the tile
+        const bool real = gr < tile.rows;
+        // the row's sequence, chunk token and query head (padding rows: the tile's first row)
+        const int rseq = kPrefix ? seq + (real ? gr / p.total_rows : 0) : seq;
+        const int rrow = kPrefix ? (real ? gr % p.total_rows : 0) : gr;
+        const int t = real ? rrow / p.group : (kPrefix ? 0 : p.q_len - 1);
+        const int hq = kvh * p.group + (real ? rrow - t * p.group : 0);
+        // Last position this row sees, and the smallest such limit in the tile; a prefix row
+        // sees the whole prefix.
+        const int lim = kPrefix ? L - 1 : L - p.q_len + t;
+        const int lim_min = kPrefix ? L - 1 : L - p.q_len + row0 / p.group;
         const uint32_t lane_tmem = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t o_half = lane_tmem + kTmemO + (D / 2) * hf;  // this thread's half of O
-        const long long row_off = (((long long)seq * p.q_len + t) * p.num_heads + hq) * D;
+        const long long row_id = ((long long)rseq * p.q_len + t) * p.num_heads + hq;
+        const long long row_off = row_id * D;
         const float c2 = p.scale_log2;
 
         // This thread's half of the Q row into TMEM lane r (rows past the chunk are zeros):
@@ -468,11 +526,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         tc::wait_st();
 
         // Epilogue: the row's two half sums, then O / l, rounded once, to out[seq, t, hq, :]
-        // (this thread's half of the columns).
+        // (this thread's half of the columns); in prefix mode the unnormalised fp32 partial
+        // (m, l, O) of the row, in its sequence's first partial slot.
         if (ok && __all_sync(0xffffffffu, mbar_wait(odone, (ntiles - 1) & 1, err, abort_flag, p.wait_limit_ns))) {
             lsum[hf * kTcRows + r] = l_run;
             mbar_arrive(lready);
-            if (__all_sync(0xffffffffu, mbar_wait(lready, 0, err, abort_flag, p.wait_limit_ns))) {
+            if constexpr (kPrefix) {
+                if (__all_sync(0xffffffffu, mbar_wait(lready, 0, err, abort_flag, p.wait_limit_ns))) {
+                    tc::fence_after_sync();
+                    griddep_wait();  // the plan kernel's partial slots
+                    // A sequence the plan found invalid has no slot of its own: nothing is written.
+                    const bool write = real && seq_len_valid(p.context_lens[rseq], p.q_len, L, p.max_context_len,
+                                                             p.max_blocks_per_seq);
+                    const long long prow =
+                        write ? ((long long)p.part_start[rseq] * p.q_len + t) * p.num_heads + hq : 0;
+                    if (write && hf == 0) p.pml[prow] = make_float2(m_run, lsum[r] + lsum[kTcRows + r]);
+                    float4* dst = reinterpret_cast<float4*>(p.pacc + prow * D) + hf * (D / 8);
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h) {
+                        uint32_t o[32];
+                        tc::ld_x32(o_half + 32 * h, o);
+                        if (write) {
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                dst[h * 8 + c] = make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
+                                                             __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3]));
+                        }
+                    }
+                }
+            } else if (__all_sync(0xffffffffu, mbar_wait(lready, 0, err, abort_flag, p.wait_limit_ns))) {
                 tc::fence_after_sync();
                 const float inv = 1.f / (lsum[r] + lsum[kTcRows + r]);
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row_off) + hf * (D / 16);
@@ -506,8 +588,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 }
 
 template <typename T, int D>
-int launch_prefill_tc_typed(const DecodeArgs& a, cudaStream_t stream, int* launches) {
-    PrefillTcParams p;
+__global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
+    tc_attention<T, D, false>(p, nullptr);
+}
+
+// The shared prefix of every prefix group once per kv head for all the group's query rows.
+template <typename T, int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefix_tc_kernel(const __grid_constant__ PrefillTcParams p, const __grid_constant__ PrefixGroups g) {
+    tc_attention<T, D, true>(p, &g);
+}
+
+// Parameters shared by the chunk and prefix launches.
+template <int D>
+int tc_params(const DecodeArgs& a, PrefillTcParams& p) {
     if (int st = kv_tensor_map(&p.tmap_k, a.key_cache, a.dtype, a.num_blocks, a.num_kv_heads, D)) return st;
     if (int st = kv_tensor_map(&p.tmap_v, a.value_cache, a.dtype, a.num_blocks, a.num_kv_heads, D)) return st;
     p.out = a.out;
@@ -526,6 +620,16 @@ int launch_prefill_tc_typed(const DecodeArgs& a, cudaStream_t stream, int* launc
     p.max_context_len = a.max_context_len;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.wait_limit_ns = wait_limit_ns();
+    p.part_start = nullptr;
+    p.pml = nullptr;
+    p.pacc = nullptr;
+    return PA_OK;
+}
+
+template <typename T, int D>
+int launch_prefill_tc_typed(const DecodeArgs& a, cudaStream_t stream, int* launches) {
+    PrefillTcParams p;
+    if (int st = tc_params<D>(a, p)) return st;
     const long long grid = (long long)a.num_seqs * a.num_kv_heads * p.mtiles;
     if (grid > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     auto kfn = prefill_tc_kernel<T, D>;
@@ -542,6 +646,26 @@ int launch_prefill_tc_typed(const DecodeArgs& a, cudaStream_t stream, int* launc
     return PA_OK;
 }
 
+template <typename T, int D>
+int launch_prefix_tc_typed(const DecodeArgs& a, const int* part_start, float2* pml, float* pacc, cudaStream_t stream,
+                           int* launches) {
+    const PrefixGroups& g = *a.groups;
+    const int grid = g.tile_start[g.n];
+    if (grid == 0) return PA_OK;
+    PrefillTcParams p;
+    if (int st = tc_params<D>(a, p)) return st;
+    p.part_start = part_start;
+    p.pml = pml;
+    p.pacc = pacc;
+    auto kfn = prefix_tc_kernel<T, D>;
+    const int smem = TcLayout<D>::kAlloc;
+    if (int st = ensure_dynamic_smem(reinterpret_cast<const void*>(kfn), smem)) return st;
+    if (launch_pdl(kfn, dim3((unsigned)grid), dim3(kTcThreads), (size_t)smem, stream, p, g) != cudaSuccess)
+        return PA_ERR_CUDA;
+    *launches += 1;
+    return PA_OK;
+}
+
 }  // namespace
 
 int launch_prefill_tc(const DecodeArgs& a, cudaStream_t stream, int* launches) {
@@ -552,6 +676,19 @@ int launch_prefill_tc(const DecodeArgs& a, cudaStream_t stream, int* launches) {
     } else {
         if (a.head_dim == 128) return launch_prefill_tc_typed<__half, 128>(a, stream, launches);
         if (a.head_dim == 64) return launch_prefill_tc_typed<__half, 64>(a, stream, launches);
+    }
+    return PA_ERR_UNSUPPORTED;
+}
+
+int launch_prefix_tc(const DecodeArgs& a, const int* part_start, float2* pml, float* pacc, cudaStream_t stream,
+                     int* launches) {
+    if (a.fp8 || !a.groups) return PA_ERR_UNSUPPORTED;
+    if (a.dtype == PA_BF16) {
+        if (a.head_dim == 128) return launch_prefix_tc_typed<__nv_bfloat16, 128>(a, part_start, pml, pacc, stream, launches);
+        if (a.head_dim == 64) return launch_prefix_tc_typed<__nv_bfloat16, 64>(a, part_start, pml, pacc, stream, launches);
+    } else {
+        if (a.head_dim == 128) return launch_prefix_tc_typed<__half, 128>(a, part_start, pml, pacc, stream, launches);
+        if (a.head_dim == 64) return launch_prefix_tc_typed<__half, 64>(a, part_start, pml, pacc, stream, launches);
     }
     return PA_ERR_UNSUPPORTED;
 }

@@ -24,6 +24,7 @@ PA_DEVERR_TOKEN = 32
 BLOCK_SIZE = 16
 DEFAULT_PARTITION = 512
 NOALLOC_WORKSPACE_BYTES = 32 << 20
+MAX_PREFIX_GROUPS = 256
 
 _DT = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16}
 
@@ -49,6 +50,10 @@ _SIGS = {
                                         _c_int, _c_int, _c_i64, _c_int, _c_f, _c_int, _c_int, _vp, _c_sz, _vp]),
     "pa_decode_attention_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int,
                                              _c_int, _c_int, _c_i64, _c_int, _c_f, _c_int, _c_int, _vp]),
+    "pa_decode_workspace_size_shared_prefix": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "pa_decode_attention_shared_prefix": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int,
+                                                   _c_int, _c_int, _c_int, _c_i64, _c_int, _c_f, _c_int, _c_int,
+                                                   _vp, _vp, _c_int, _vp, _c_sz, _vp]),
     "pa_status_string": (ctypes.c_char_p, [_c_int]),
     "pa_get_device_error": (_c_int, [ctypes.POINTER(ctypes.c_int32), _c_int, _vp]),
     "pa_set_decode_math": (_c_int, [_c_int]),
@@ -324,6 +329,45 @@ def decode_attention_multiquery(out: torch.Tensor, query: torch.Tensor, key_cach
             hq, hkv, d, bs, nb, int(max_context_len), float(scale), dtype_code(query), _dev(workspace, "workspace"),
             workspace.numel() * workspace.element_size(), _stream(stream))
     _check("pa_decode_attention_multiquery", st)
+    return out
+
+
+def workspace_size_shared_prefix(num_seqs: int, q_len: int, num_heads: int, head_dim: int, max_context_len: int,
+                                 partition_size: int = 0) -> int:
+    return int(lib().pa_decode_workspace_size_shared_prefix(num_seqs, q_len, num_heads, head_dim, max_context_len,
+                                                            partition_size))
+
+
+def alloc_workspace_shared_prefix(num_seqs: int, q_len: int, num_heads: int, head_dim: int, max_context_len: int,
+                                  partition_size: int = 0, device=None) -> torch.Tensor:
+    n = workspace_size_shared_prefix(num_seqs, q_len, num_heads, head_dim, max_context_len, partition_size)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def decode_attention_shared_prefix(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                                   value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                   scale: float, max_context_len: int, workspace: torch.Tensor, group_seq_start,
+                                   group_prefix_len, partition_size: int = 0, stream=None) -> torch.Tensor:
+    """pa_decode_attention_shared_prefix: decode attention where the sequences of group k
+    (group_seq_start[k] .. group_seq_start[k+1] - 1) share their first group_prefix_len[k]
+    positions' blocks.  The group arrays are host integer sequences."""
+    n, q_len, hq, hkv, d, bs, nb = _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens)
+    starts = [int(x) for x in group_seq_start]
+    lens = [int(x) for x in group_prefix_len]
+    ng = len(lens)
+    if len(starts) != ng + 1 and not (ng == 0 and len(starts) in (0, 1)):
+        raise ValueError("group_seq_start must have one more entry than group_prefix_len")
+    c_starts = (ctypes.c_int32 * max(1, len(starts)))(*starts)
+    c_lens = (ctypes.c_int32 * max(1, ng))(*lens)
+    with _device_of(out, query, key_cache, value_cache, block_tables, context_lens, workspace, stream=stream):
+        st = lib().pa_decode_attention_shared_prefix(
+            _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+            _dev(block_tables, "block_tables"), block_tables.shape[1], _dev(context_lens, "context_lens"), n, q_len,
+            hq, hkv, d, bs, nb, int(max_context_len), float(scale), dtype_code(query), ng,
+            ctypes.cast(c_starts, _vp) if starts else None, ctypes.cast(c_lens, _vp) if ng else None,
+            int(partition_size), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+            _stream(stream))
+    _check("pa_decode_attention_shared_prefix", st)
     return out
 
 

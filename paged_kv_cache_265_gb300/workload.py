@@ -199,6 +199,34 @@ def make_workload(name: str, context_lens: Sequence[int], *, num_heads: int, num
         shared_prefix_blocks=shared_prefix_blocks)
 
 
+def concat_workloads(name: str, parts: Sequence[Workload]) -> Workload:
+    """One batch made of several workloads side by side: their pools laid end to end (block ids
+    and slots shifted accordingly), their sequences, queries and appended rows in order.  All
+    parts must share dtype, head counts, head dim, q_len and scale.  Used to build batches in
+    which several groups of sequences each share a different prefix."""
+    first = parts[0]
+    for w in parts[1:]:
+        assert (w.dtype, w.num_heads, w.num_kv_heads, w.head_dim, w.q_len, w.block_size, w.scale) == \
+            (first.dtype, first.num_heads, first.num_kv_heads, first.head_dim, first.q_len, first.block_size,
+             first.scale), "parts must share their shapes"
+    mbps = max(w.max_blocks_per_seq for w in parts)
+    tables, slots, off = [], [], 0
+    for w in parts:
+        bt = np.full((w.num_seqs, mbps), -1, dtype=np.int32)
+        bt[:, :w.max_blocks_per_seq] = np.where(w.block_tables >= 0, w.block_tables + off, -1)
+        tables.append(bt)
+        slots.append(w.slot_mapping + off * w.block_size)
+        off += w.num_blocks
+    cat = lambda xs: np.ascontiguousarray(np.concatenate(xs))  # noqa: E731
+    return Workload(
+        name=name, dtype=first.dtype, num_heads=first.num_heads, num_kv_heads=first.num_kv_heads,
+        head_dim=first.head_dim, q_len=first.q_len, block_size=first.block_size, num_blocks=off, scale=first.scale,
+        context_lens=cat([w.context_lens for w in parts]), block_tables=cat(tables),
+        query=cat([w.query for w in parts]), key_cache=cat([w.key_cache for w in parts]),
+        value_cache=cat([w.value_cache for w in parts]), new_key=cat([w.new_key for w in parts]),
+        new_value=cat([w.new_value for w in parts]), slot_mapping=cat(slots).astype(np.int64))
+
+
 # ---------------------------------------------------------------------------
 # The five named decode workloads.  Seeds are 2650 + the workload number.
 # ---------------------------------------------------------------------------

@@ -93,3 +93,40 @@ def test_reshape_host_validation(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 4, 64, 16, 64, 0, None) == 1
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 1 << 20, 128, 16, 64, 0, None) == 2   # absurd head count
     assert lib.pa_copy_blocks(FAKE, FAKE, FAKE, 1, 1 << 20, 128, 16, 64, 0, None) == 2
+
+
+def _prefix_call(lib, starts, lens, **kw):
+    a = dict(n=4, q_len=1, hq=4, hkv=4, d=64, max_ctx=100, ws=FAKE, ws_bytes=1 << 30)
+    a.update(kw)
+    ng = len(lens)
+    c_starts = (ctypes.c_int32 * max(1, len(starts)))(*starts)
+    c_lens = (ctypes.c_int32 * max(1, ng))(*lens)
+    return lib.pa_decode_attention_shared_prefix(
+        FAKE, FAKE, FAKE, FAKE, FAKE, 8, FAKE, a["n"], a["q_len"], a["hq"], a["hkv"], a["d"], 16, 64, a["max_ctx"],
+        ctypes.c_float(0.125), 0, ng, ctypes.cast(c_starts, ctypes.c_void_p) if starts else None,
+        ctypes.cast(c_lens, ctypes.c_void_p) if ng else None, 0, a["ws"], ctypes.c_size_t(a["ws_bytes"]), None)
+
+
+def test_shared_prefix_host_validation(lib):
+    """The group table is checked on the host before anything is enqueued."""
+    lib.pa_decode_attention_shared_prefix.restype = ctypes.c_int
+    assert _prefix_call(lib, [0, 5], [16]) == 1            # a group past the batch
+    assert _prefix_call(lib, [2, 1], [16]) == 1            # starts decreasing
+    assert _prefix_call(lib, [0, 2], [8]) == 1             # not whole blocks
+    assert _prefix_call(lib, [0, 2], [-16]) == 1
+    assert _prefix_call(lib, [0, 2], [112]) == 1           # more than max_context_len - q_len
+    assert _prefix_call(lib, [], [1] * 0, n=0) == 0        # nothing to do
+    assert _prefix_call(lib, [0, 1] + [1] * 256, [16] * 257) == 1   # more than PA_MAX_PREFIX_GROUPS groups
+    assert _prefix_call(lib, [0, 2], [16], ws=None) == 3
+    assert _prefix_call(lib, [0, 2], [16], ws_bytes=64) == 3
+
+
+def test_shared_prefix_workspace_size(lib):
+    f = lib.pa_decode_workspace_size_shared_prefix
+    f.restype = ctypes.c_size_t
+    plain = lib.pa_decode_workspace_size_ex
+    plain.restype = ctypes.c_size_t
+    # one extra piece per sequence (the prefix's), partials always reserved
+    assert f(4, 5, 32, 128, 1536, 512) > plain(4, 5, 32, 128, 1536, 512)
+    assert f(4, 5, 32, 128, 1536, 0) == f(4, 5, 32, 128, 1536, 128)   # sized for the finest split
+    assert f(4, 5, 32, 128, 1536, 24) == 0
