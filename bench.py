@@ -402,9 +402,10 @@ def run_ours(args, rank, world, local):
     if w.shared_prefix_blocks and not kv8 and not args.no_prefix_groups:
         groups = ([0, w.num_seqs], [w.shared_prefix_blocks * w.block_size])
         ws = pa.alloc_workspace_shared_prefix(w.num_seqs, w.q_len, w.num_heads, w.head_dim, w.max_context_len,
-                                              device=dev)
+                                              args.partition, device=dev)
     else:
-        ws = pa.alloc_workspace(w.num_seqs, w.q_len, w.num_heads, w.head_dim, w.max_context_len, device=dev)
+        ws = pa.alloc_workspace(w.num_seqs, w.q_len, w.num_heads, w.head_dim, w.max_context_len, args.partition,
+                                device=dev)
     pa.set_decode_math(args.math)
     stream = torch.cuda.current_stream(dev)
     pa.get_device_error(clear=True)
@@ -416,15 +417,16 @@ def run_ours(args, rank, world, local):
             pa.reshape_and_cache_fp8(nk_, nv_, kc, vc, sm_, K_SCALE, V_SCALE, stream=stream)
             n1 = pa.last_launch_count()
             pa.decode_attention_fp8kv(o, q_, kc, vc, bt_, cl_, w.scale, w.max_context_len, ws, K_SCALE, V_SCALE,
-                                      stream=stream)
+                                      partition_size=args.partition, stream=stream)
             return n1 + pa.last_launch_count()
         pa.reshape_and_cache(nk_, nv_, kc, vc, sm_, stream=stream)
         n1 = pa.last_launch_count()
         if groups:
             pa.decode_attention_shared_prefix(o, q_, kc, vc, bt_, cl_, w.scale, w.max_context_len, ws, *groups,
-                                              stream=stream)
+                                              partition_size=args.partition, stream=stream)
         else:
-            pa.decode_attention(o, q_, kc, vc, bt_, cl_, w.scale, w.max_context_len, ws, stream=stream)
+            pa.decode_attention(o, q_, kc, vc, bt_, cl_, w.scale, w.max_context_len, ws,
+                                partition_size=args.partition, stream=stream)
         return n1 + pa.last_launch_count()
 
     for _ in range(max(3, args.warmup)):
@@ -723,6 +725,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa_batch128")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--partition", type=int, default=0,
+                    help="split-K partition in tokens (a multiple of 16); 0 lets the library choose")
     ap.add_argument("--no-prefix-groups", action="store_true",
                     help="run a shared-prefix batch through the plain multi-query call (no prefix group declared)")
     ap.add_argument("--op", choices=["decode_step", "copy_blocks", "spec_verify"], default="decode_step",

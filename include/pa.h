@@ -256,7 +256,7 @@ int pa_decode_attention_ex(void* out, const void* query, const void* key_cache, 
  * are left untouched.  Everything else as pa_decode_attention_multiquery (16-bit caches; the
  * prefix pass uses the tcgen05 kernel whatever pa_set_decode_math says).  The workspace must
  * hold pa_decode_workspace_size_shared_prefix() bytes for the same partition size (0: the
- * library chooses 128 to 2048 tokens for the positions after the prefixes).  Results agree
+ * library chooses 512 to 2048 tokens for the positions after the prefixes).  Results agree
  * with pa_decode_attention_multiquery within fp32 rounding.
  */
 #define PA_MAX_PREFIX_GROUPS 256

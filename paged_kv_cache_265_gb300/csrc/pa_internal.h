@@ -124,12 +124,13 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int* launches, int* 
 int launch_prefill_tc(const DecodeArgs& a, cudaStream_t stream, int* launches);
 bool use_prefill_tc(const DecodeArgs& a);
 // The shared prefixes of a.groups on tcgen05 (pa_prefill.cu): one CTA per (group, kv head,
-// 128-row tile), each writing its rows' prefix pieces into the partials at part_start.
-int launch_prefix_tc(const DecodeArgs& a, const int* part_start, float2* pml, float* pacc, cudaStream_t stream,
-                     int* launches);
+// 128-row tile).  Launched after the partition pass; each row's epilogue merges the prefix piece
+// with the sequence's other pieces (partial slots part_start[i] + 1 ..) and writes the output.
+int launch_prefix_tc(const DecodeArgs& a, const int* part_start, const float2* pml, const float* pacc,
+                     cudaStream_t stream, int* launches);
 // Smallest split-K partition the library chooses for a shared-prefix call (the workspace of a
 // call with partition 0 is sized for it).
-constexpr int kMinPrefixPartition = 128;
+constexpr int kMinPrefixPartition = 512;
 int launch_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* target_probs,
                        const float* draft_probs, const int32_t* draft_tokens, const float* u_accept,
                        const float* u_sample, int num_seqs, int k, int vocab, cudaStream_t stream, int* launches);

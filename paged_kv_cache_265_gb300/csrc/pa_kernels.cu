@@ -1385,8 +1385,7 @@ struct MergeParams {
 // then summed in slot order, so the result does not depend on timing.  Sequences with one
 // piece (written by the partition pass) or none (an invalid length) are skipped.
 template <typename T, int D>
-__global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
-    griddep_wait();  // the partition pass must have finished
+__device__ __forceinline__ void merge_body(const MergeParams& p, const PrefixGroups* g) {
     constexpr int kPer = D / 32;
     const long long row = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -1398,6 +1397,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
     const long long slot0 = p.part_start[seq];
     const int nparts = p.part_start[seq + 1] - (int)slot0;
     if (nparts <= 1) return;
+    if (g && prefix_of(*g, seq) > 0) return;  // finished by the shared-prefix kernel
     // Lane l keeps the (max, sum) pairs of partitions l and l + 32; any further ones are re-read.
     const float2 ml0 = lane < nparts ? p.pml[(slot0 + lane) * per_seq + rem] : make_float2(-INFINITY, 0.f);
     const float2 ml1 = lane + 32 < nparts ? p.pml[(slot0 + lane + 32) * per_seq + rem] : make_float2(-INFINITY, 0.f);
@@ -1444,6 +1444,19 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
     uint16_t* dst = static_cast<uint16_t*>(p.out) + row * D + lane * kPer;
 #pragma unroll
     for (int c = 0; c < kPer; ++c) dst[c] = Elem<T>::to_bits(acc[c]);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
+    griddep_wait();  // the partition pass must have finished
+    merge_body<T, D>(p, nullptr);
+}
+
+// After a shared-prefix call's prefix kernel (which merges its own sequences): the others.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) merge_ungrouped_kernel(const MergeParams p, const __grid_constant__ PrefixGroups g) {
+    griddep_wait();
+    merge_body<T, D>(p, &g);
 }
 
 // ---------------------------------------------------------------------------
@@ -1621,8 +1634,10 @@ int auto_partition(const DecodeArgs& a, int sms) {
 }
 
 // The same choice for a shared-prefix call, over the positions after each group's prefix
-// (taken as half of what is left of max_context_len), from 128 tokens up: the suffixes are
-// short, and a finer split keeps every CTA busy.
+// (taken as half of what is left of max_context_len).  Measured on the shared-prefix batch
+// (64 sequences, 1024-token prefix, suffixes of 16-512 positions, 20 rows per kv head), step
+// time: 64 / 128 / 256 / 512 tokens 98.4 / 83.4 / 76.3 / 73.6 us: every partition costs its CTA
+// a fixed set-up and combine, so finer splits of short suffixes lose.
 int auto_partition_prefix(const DecodeArgs& a, int sms) {
     const PrefixGroups& g = *a.groups;
     const int group = a.num_heads / a.num_kv_heads;
@@ -1681,11 +1696,6 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     if (pe != cudaSuccess) return PA_ERR_CUDA;
     *launches += 1;
     profile_mark(pc, 1, stream);
-    // Shared prefixes: one tcgen05 pass per (group, kv head) over every grouped row, before the
-    // partition pass takes the rest of each sequence.
-    if (prefix)
-        if (int st = launch_prefix_tc(a, part_start, pml, pacc, stream, launches)) return st;
-
     DecodeParams p;
     if (a.fp8) {
         if (D != 128) return PA_ERR_UNSUPPORTED;
@@ -1767,8 +1777,22 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     if (le != cudaSuccess) return PA_ERR_CUDA;
     profile_mark(pc, 2, stream);
     *launches += 1;
+    // Shared prefixes: one tcgen05 pass per (group, kv head) over every grouped row, after the
+    // partition pass under programmatic launch.  Its CTAs (one per SM) take the SMs the partition
+    // pass's CTAs leave as they run out of work, and its epilogue, once the partition pass has
+    // finished, merges every grouped sequence's pieces and writes the output rows.
+    bool merge_needed = w.pmax > 1;
+    if (prefix) {
+        if (int st = launch_prefix_tc(a, part_start, pml, pacc, stream, launches)) return st;
+        // Only sequences outside every group with a prefix can still be split.
+        const PrefixGroups& g = *a.groups;
+        int covered = 0;
+        for (int k = 0; k < g.n; ++k)
+            if (g.len[k] > 0) covered += g.seq_start[k + 1] - g.seq_start[k];
+        merge_needed = covered < a.num_seqs;
+    }
 
-    if (w.pmax > 1) {
+    if (merge_needed) {
         MergeParams mp;
         mp.out = a.out;
         mp.part_start = part_start;
@@ -1779,7 +1803,11 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
         mp.num_heads = a.num_heads;
         const long long rows = (long long)a.num_seqs * a.q_len * a.num_heads;
         const unsigned blocks = (unsigned)((rows * 32 + 127) / 128);
-        if (launch_pdl(merge_kernel<T, D>, dim3(blocks), dim3(128), 0, stream, mp) != cudaSuccess) return PA_ERR_CUDA;
+        const cudaError_t me = prefix
+                                   ? launch_pdl(merge_ungrouped_kernel<T, D>, dim3(blocks), dim3(128), 0, stream, mp,
+                                                *a.groups)
+                                   : launch_pdl(merge_kernel<T, D>, dim3(blocks), dim3(128), 0, stream, mp);
+        if (me != cudaSuccess) return PA_ERR_CUDA;
         *launches += 1;
     }
     profile_mark(pc, 3, stream);

@@ -46,6 +46,15 @@
 // block table, three stages of one K/V tile), 9 TMEM owner and MMA issuer (one
 // thread).  Every wait is bounded (PA_DEVERR_TIMEOUT); a failed wait stops all
 // roles, and the CTA lets its copies and products finish before it frees TMEM.
+//
+// Shared-prefix mode (prefix_tc_kernel): sequences that map the same prefix blocks
+// ("每生成一个字都要把全部权重读一遍：从 vLLM 看 LLM 推理提速", section "KV Cache 又大又碎，
+// 为何不用操作系统分页的思路管它？": one physical block mapped by many sequences) see the
+// same prefix K/V, so one CTA takes 128 query rows of several sequences of a group (row r =
+// sequence r / (g q_len), then chunk token, then head) against the whole prefix, with no
+// causal mask (every chunk row lies after the prefix).  It is launched after the split-K
+// partition pass has covered the rest of each sequence; its epilogue merges the prefix piece
+// with those pieces by their log-sum-exp and writes the output rows.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -89,10 +98,10 @@ struct PrefillTcParams {
     int max_context_len;
     float scale_log2;
     unsigned long long wait_limit_ns;  // limit of the pipeline waits (pa_set_wait_limit_ns)
-    // Shared-prefix mode: where each row's partial result goes.
-    const int* part_start;  // first partial slot of each sequence (its prefix piece)
-    float2* pml;            // (max in log2 units, sum) per partial row
-    float* pacc;            // unnormalised partial outputs, fp32
+    // Shared-prefix mode: the other pieces of each sequence, merged with the prefix's.
+    const int* part_start;  // first partial slot of each sequence (the prefix piece's, not stored)
+    const float2* pml;      // (max in log2 units, sum) per partial row
+    const float* pacc;      // unnormalised partial outputs, fp32
 };
 
 template <int D>
@@ -526,31 +535,67 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
         tc::wait_st();
 
         // Epilogue: the row's two half sums, then O / l, rounded once, to out[seq, t, hq, :]
-        // (this thread's half of the columns); in prefix mode the unnormalised fp32 partial
-        // (m, l, O) of the row, in its sequence's first partial slot.
+        // (this thread's half of the columns); in prefix mode merged first with the sequence's
+        // other pieces.
         if (ok && __all_sync(0xffffffffu, mbar_wait(odone, (ntiles - 1) & 1, err, abort_flag, p.wait_limit_ns))) {
             lsum[hf * kTcRows + r] = l_run;
             mbar_arrive(lready);
             if constexpr (kPrefix) {
                 if (__all_sync(0xffffffffu, mbar_wait(lready, 0, err, abort_flag, p.wait_limit_ns))) {
                     tc::fence_after_sync();
-                    griddep_wait();  // the plan kernel's partial slots
+                    // The plan kernel's partial slots and the partition pass's pieces.
+                    griddep_wait();
                     // A sequence the plan found invalid has no slot of its own: nothing is written.
                     const bool write = real && seq_len_valid(p.context_lens[rseq], p.q_len, L, p.max_context_len,
                                                              p.max_blocks_per_seq);
-                    const long long prow =
-                        write ? ((long long)p.part_start[rseq] * p.q_len + t) * p.num_heads + hq : 0;
-                    if (write && hf == 0) p.pml[prow] = make_float2(m_run, lsum[r] + lsum[kTcRows + r]);
-                    float4* dst = reinterpret_cast<float4*>(p.pacc + prow * D) + hf * (D / 8);
+                    const long long slot0 = write ? p.part_start[rseq] : 0;
+                    const float l_pre = lsum[r] + lsum[kTcRows + r];
+                    // Merge the prefix piece (m_run, l_pre, O in TMEM) with the sequence's other
+                    // pieces, in slot order, by their log-sum-exp, and write the output row.
+                    const int npieces = write ? p.part_start[rseq + 1] - (int)slot0 : 1;
+                    const long long stride = (long long)p.q_len * p.num_heads;
+                    const long long prow0 = (slot0 * p.q_len + t) * p.num_heads + hq;
+                    float M = m_run;
+                    for (int c = 1; c < npieces; ++c) M = fmaxf(M, p.pml[prow0 + c * stride].x);
+                    const float f0 = ex2(m_run - M);
+                    float ltot = l_pre * f0;
+                    for (int c = 1; c < npieces; ++c) {
+                        const float2 ml = p.pml[prow0 + c * stride];
+                        ltot += ml.y * ex2(ml.x - M);
+                    }
+                    const float inv = 1.f / ltot;
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row_off) + hf * (D / 16);
 #pragma unroll
                     for (int h = 0; h < D / 64; ++h) {
                         uint32_t o[32];
                         tc::ld_x32(o_half + 32 * h, o);
+                        float acc[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(o[e]) * f0;
+                        for (int c = 1; c < npieces; ++c) {
+                            const long long prow = prow0 + c * stride;
+                            const float fc = ex2(p.pml[prow].x - M);
+                            const float4* src = reinterpret_cast<const float4*>(p.pacc + prow * D) +
+                                                hf * (D / 8) + h * 8;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float4 v = src[e];
+                                acc[4 * e] += v.x * fc;
+                                acc[4 * e + 1] += v.y * fc;
+                                acc[4 * e + 2] += v.z * fc;
+                                acc[4 * e + 3] += v.w * fc;
+                            }
+                        }
                         if (write) {
 #pragma unroll
-                            for (int c = 0; c < 8; ++c)
-                                dst[h * 8 + c] = make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
-                                                             __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3]));
+                            for (int c = 0; c < 4; ++c) {
+                                uint4 v;
+                                v.x = Elem<T>::pack(acc[8 * c + 0] * inv, acc[8 * c + 1] * inv);
+                                v.y = Elem<T>::pack(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv);
+                                v.z = Elem<T>::pack(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv);
+                                v.w = Elem<T>::pack(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv);
+                                dst[h * 4 + c] = v;
+                            }
                         }
                     }
                 }
@@ -647,8 +692,8 @@ int launch_prefill_tc_typed(const DecodeArgs& a, cudaStream_t stream, int* launc
 }
 
 template <typename T, int D>
-int launch_prefix_tc_typed(const DecodeArgs& a, const int* part_start, float2* pml, float* pacc, cudaStream_t stream,
-                           int* launches) {
+int launch_prefix_tc_typed(const DecodeArgs& a, const int* part_start, const float2* pml, const float* pacc,
+                           cudaStream_t stream, int* launches) {
     const PrefixGroups& g = *a.groups;
     const int grid = g.tile_start[g.n];
     if (grid == 0) return PA_OK;
@@ -680,12 +725,14 @@ int launch_prefill_tc(const DecodeArgs& a, cudaStream_t stream, int* launches) {
     return PA_ERR_UNSUPPORTED;
 }
 
-int launch_prefix_tc(const DecodeArgs& a, const int* part_start, float2* pml, float* pacc, cudaStream_t stream,
-                     int* launches) {
+int launch_prefix_tc(const DecodeArgs& a, const int* part_start, const float2* pml, const float* pacc,
+                     cudaStream_t stream, int* launches) {
     if (a.fp8 || !a.groups) return PA_ERR_UNSUPPORTED;
     if (a.dtype == PA_BF16) {
-        if (a.head_dim == 128) return launch_prefix_tc_typed<__nv_bfloat16, 128>(a, part_start, pml, pacc, stream, launches);
-        if (a.head_dim == 64) return launch_prefix_tc_typed<__nv_bfloat16, 64>(a, part_start, pml, pacc, stream, launches);
+        if (a.head_dim == 128)
+            return launch_prefix_tc_typed<__nv_bfloat16, 128>(a, part_start, pml, pacc, stream, launches);
+        if (a.head_dim == 64)
+            return launch_prefix_tc_typed<__nv_bfloat16, 64>(a, part_start, pml, pacc, stream, launches);
     } else {
         if (a.head_dim == 128) return launch_prefix_tc_typed<__half, 128>(a, part_start, pml, pacc, stream, launches);
         if (a.head_dim == 64) return launch_prefix_tc_typed<__half, 64>(a, part_start, pml, pacc, stream, launches);

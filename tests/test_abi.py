@@ -128,5 +128,5 @@ def test_shared_prefix_workspace_size(lib):
     plain.restype = ctypes.c_size_t
     # one extra piece per sequence (the prefix's), partials always reserved
     assert f(4, 5, 32, 128, 1536, 512) > plain(4, 5, 32, 128, 1536, 512)
-    assert f(4, 5, 32, 128, 1536, 0) == f(4, 5, 32, 128, 1536, 128)   # sized for the finest split
+    assert f(4, 5, 32, 128, 1536, 0) == f(4, 5, 32, 128, 1536, 512)   # sized for the finest split
     assert f(4, 5, 32, 128, 1536, 24) == 0

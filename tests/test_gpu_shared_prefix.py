@@ -49,7 +49,8 @@ def test_shared_prefix_workload(partition):
     """The named shared-prefix workload: 64 sequences, one 1024-token prefix, q = 5."""
     w = W.shared_prefix_verify()
     step, got = run_prefix(w, [0, w.num_seqs], [w.shared_prefix_blocks * 16], partition)
-    assert pa.last_launch_count() == 4           # plan, prefix (tcgen05), partition pass, merge
+    # plan, partition pass, prefix kernel (tcgen05; it merges every grouped sequence's pieces)
+    assert pa.last_launch_count() in (3, 4)
     _, _, ref = G.oracle_step(w)
     G.compare(got, ref, w.dtype, f"shared prefix, partition {partition}")
     assert G.ulps_from_rounded_oracle(got, ref, w.dtype) <= 1
