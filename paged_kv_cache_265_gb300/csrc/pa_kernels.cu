@@ -198,6 +198,13 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ ke
 // first rejection, or a bonus token from p_large[k] if all were accepted.
 // Draws are inverse-CDF over weights converted exactly to 2^-40 fixed point, so
 // prefix sums are integer-exact whatever the summation order.
+//
+// One cluster of kSpecCluster CTAs per sequence.  Every CTA takes the accept decisions
+// (k lookups), then sums the fixed-point weights of its share of the vocabulary chunks
+// (chunk j belongs to CTA j % kSpecCluster) and stores each chunk total into the shared
+// memory of every CTA of the cluster; after one cluster barrier every CTA holds all totals,
+// finds the threshold and the chunk holding it, and the chunk's owner scans it and writes
+// the sequence's outputs.
 // ---------------------------------------------------------------------------
 struct SpecParams {
     int* num_accepted;
@@ -211,143 +218,232 @@ struct SpecParams {
     int vocab;
 };
 
-// floor(x * 2^shift) for a non-negative fp32 x < 2, from its bits (integer-only:
-// fp64 is slow on this GPU).  Exact: the mathematical value, as the oracle's fp64 floor.
-__device__ __forceinline__ unsigned long long fixed_from_float(float x, int shift) {
-    const unsigned bits = __float_as_uint(x);
-    const int ebits = (bits >> 23) & 0xff;
-    if (ebits == 0) return 0ull;  // zero or subnormal: below 2^-126, floor gives 0 for shift <= 64
-    const unsigned long long m = (bits & 0x7fffffu) | 0x800000u;
-    const int e = ebits - 127 - 23 + shift;  // value = m * 2^e
-    if (e >= 0) return m << e;
-    if (e <= -64) return 0ull;
-    return m >> (-e);
-}
+constexpr int kSpecCluster = 4;                      // CTAs per sequence
+constexpr int kSpecThreads = 256;                    // threads per CTA
+constexpr int kSpecChunk = 4 * kSpecThreads;         // entries per chunk: thread t holds 4t .. 4t + 3
+constexpr int kSpecMaxChunks = 256;                  // vocabulary up to 262,144
+constexpr int kSpecOwn = kSpecMaxChunks / kSpecCluster;  // chunks one CTA may own
+constexpr int kSpecGroup = 8;                        // own chunks whose loads are in flight together
 
-__device__ __forceinline__ float draw_weight(const float* a, const float* b, int v) {
-    const float w = b ? a[v] - b[v] : a[v];
-    return w > 0.f ? w : 0.f;
-}
-
-constexpr int kSpecThreads = 1024;
-constexpr int kSpecChunk = 4 * kSpecThreads;  // vocabulary entries per pass
-constexpr int kSpecMaxChunks = 64;            // vocabulary up to 262,144
+// floor(x * 2^40) for 0 <= x < 2: the product is exact in fp32 (a power-of-two scale) and
+// the truncating conversion of a non-negative value is its floor.
+__device__ __forceinline__ unsigned long long fixed40(float x) { return __float2ull_rz(x * 1099511627776.0f); }
 
 struct DrawSmem {
-    unsigned long long red[kSpecThreads / 32][kSpecMaxChunks];
-    unsigned long long chunk_prefix[kSpecMaxChunks + 1];
-    unsigned long long thresh;                    // the draw's threshold (a slot of its own: with 64
-                                                  // chunks every prefix slot is in use)
+    unsigned long long red[kSpecThreads / 32][kSpecOwn];  // per-warp sums of this CTA's chunks
+    unsigned long long tot[2][kSpecMaxChunks];            // totals of every chunk, per draw
     unsigned long long scan[kSpecThreads / 32];
     int tok;
-    int chunk;
 };
 
-// Inverse-CDF draw with uniform u over weights (a - b)+ (or a): the smallest v whose prefix
-// sum of floor(w * 2^40) exceeds floor(floor(u * 2^24) * total / 2^24).  Pass 1 sums each
-// 4096-entry chunk (thread t takes entries c * 1024 + t of it, coalesced); the chunk holding
-// the threshold is then scanned in order, 1024 entries at a time.  Returns -1 when all weights
-// are 0.  Every thread of the block must call it.
-__device__ int block_draw(const float* a, const float* b, int vocab, float u, DrawSmem& sm) {
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int chunks = (vocab + kSpecChunk - 1) / kSpecChunk;
-#pragma unroll 4
-    for (int j = 0; j < chunks; ++j) {
-        float w[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {  // all loads of the chunk first
-            const int v = j * kSpecChunk + c * kSpecThreads + t;
-            w[c] = v < vocab ? draw_weight(a, b, v) : 0.f;
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Stores v at this CTA's shared address `addr` in CTA `rank` of the cluster.
+__device__ __forceinline__ void st_cluster_u64(uint32_t addr, uint32_t rank, unsigned long long v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(remote), "l"(v) : "memory");
+}
+
+// Every thread of every CTA of the cluster; shared-memory stores before it (local or remote)
+// are visible to every CTA after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The four weights (a - b)+ (or a) of entries v0 .. v0 + 3 (0 past the vocabulary): one 16-byte
+// load per array where the rows allow it, else four scalar loads.
+__device__ __forceinline__ float4 draw_weights4(const float* a, const float* b, int v0, int vocab, bool vec) {
+    float4 w;
+    if (vec && v0 + 3 < vocab) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(a + v0));
+        if (b) {
+            const float4 y = __ldg(reinterpret_cast<const float4*>(b + v0));
+            w = make_float4(x.x - y.x, x.y - y.y, x.z - y.z, x.w - y.w);
+        } else {
+            w = x;
         }
-        unsigned long long s = 0;
+    } else {
+        float e[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) s += fixed_from_float(w[c], 40);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) sm.red[warp][j] = s;
-    }
-    __syncthreads();
-    if (t < chunks) {
-        unsigned long long s = 0;
-        for (int w = 0; w < kSpecThreads / 32; ++w) s += sm.red[w][t];
-        sm.chunk_prefix[t + 1] = s;
-    }
-    __syncthreads();
-    if (t == 0) {
-        sm.chunk_prefix[0] = 0;
-        for (int j = 1; j <= chunks; ++j) sm.chunk_prefix[j] += sm.chunk_prefix[j - 1];
-        sm.tok = -1;
-        sm.chunk = -1;
-        const unsigned long long total = sm.chunk_prefix[chunks];
-        if (total) {
-            const unsigned long long u24 = fixed_from_float(u, 24);
-            const unsigned long long thresh = (__umul64hi(u24, total) << 40) | ((u24 * total) >> 24);
-            sm.thresh = thresh;
-            for (int j = 0; j < chunks; ++j)
-                if (sm.chunk_prefix[j + 1] > thresh) {
-                    sm.chunk = j;
-                    break;
-                }
-        }
-    }
-    __syncthreads();
-    const int j = sm.chunk;
-    if (j >= 0) {
-        const unsigned long long thresh = sm.thresh;
-        unsigned long long base = sm.chunk_prefix[j];
         for (int c = 0; c < 4; ++c) {
-            const int v = j * kSpecChunk + c * kSpecThreads + t;
-            const unsigned long long x0 = v < vocab ? fixed_from_float(draw_weight(a, b, v), 40) : 0ull;
-            unsigned long long x = x0;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            if (lane == 31) sm.scan[warp] = x;
-            __syncthreads();
-            unsigned long long before = base, sub = 0;
-            for (int w = 0; w < kSpecThreads / 32; ++w) {
-                if (w < warp) before += sm.scan[w];
-                sub += sm.scan[w];
-            }
-            if (v < vocab && before + x > thresh && before + x - x0 <= thresh) sm.tok = v;
-            __syncthreads();
-            if (sm.tok >= 0) break;
-            base += sub;
+            const int v = v0 + c;
+            e[c] = v < vocab ? (b ? __ldg(a + v) - __ldg(b + v) : __ldg(a + v)) : 0.f;
         }
+        w = make_float4(e[0], e[1], e[2], e[3]);
+    }
+    w.x = w.x > 0.f ? w.x : 0.f;
+    w.y = w.y > 0.f ? w.y : 0.f;
+    w.z = w.z > 0.f ? w.z : 0.f;
+    w.w = w.w > 0.f ? w.w : 0.f;
+    return w;
+}
+
+// Inverse-CDF draw with uniform u over weights (a - b)+ (or a), `round` (0 or 1) naming the
+// draw's slot of chunk totals: the smallest v whose prefix sum of floor(w * 2^40) exceeds
+// floor(floor(u * 2^24) * total / 2^24).  Returns the token (-1 when all weights are 0) in
+// the CTA that owns the threshold's chunk and -2 in the others.  Every thread of every CTA of
+// the cluster must call it.
+__device__ int cluster_draw(const float* a, const float* b, int vocab, float u, int round, DrawSmem& sm) {
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const uint32_t rank = cluster_rank();
+    const int chunks = (vocab + kSpecChunk - 1) / kSpecChunk;
+    const int own = chunks > (int)rank ? (chunks - 1 - (int)rank) / kSpecCluster + 1 : 0;
+    const bool vec = ((reinterpret_cast<uintptr_t>(a) | (b ? reinterpret_cast<uintptr_t>(b) : 0)) & 15) == 0;
+    // Pass 1: this CTA's chunks, the loads of kSpecGroup chunks in flight together.  The last
+    // group's weights stay in registers for pass 2.
+    float4 w[kSpecGroup];
+    int g_last = 0;
+    for (int g0 = 0; g0 < own; g0 += kSpecGroup) {
+        g_last = g0;
+#pragma unroll
+        for (int q = 0; q < kSpecGroup; ++q)
+            w[q] = g0 + q < own ? draw_weights4(a, b, ((g0 + q) * kSpecCluster + (int)rank) * kSpecChunk + 4 * t, vocab, vec)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < kSpecGroup; ++q) {
+            unsigned long long s = fixed40(w[q].x) + fixed40(w[q].y) + fixed40(w[q].z) + fixed40(w[q].w);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0 && g0 + q < own) sm.red[warp][g0 + q] = s;
+        }
+    }
+    __syncthreads();
+    // This CTA's chunk totals (eight warp sums each) into every CTA's table.
+    for (int jl = warp; jl < own; jl += kSpecThreads / 32) {
+        unsigned long long s = lane < kSpecThreads / 32 ? sm.red[lane][jl] : 0ull;
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane < kSpecCluster) {
+            const int j = jl * kSpecCluster + (int)rank;
+            st_cluster_u64(smem_addr(&sm.tot[round][j]), lane, s);
+        }
+    }
+    cluster_sync();
+    // Every CTA: prefix over all chunk totals (lane l holds chunks 8l .. 8l + 7), the threshold
+    // and the first chunk whose inclusive prefix exceeds it.
+    int chunk = -1;
+    unsigned long long base = 0, thresh = 0;
+    if (warp == 0) {
+        unsigned long long c[kSpecMaxChunks / 32];
+        unsigned long long mine = 0;
+#pragma unroll
+        for (int e = 0; e < kSpecMaxChunks / 32; ++e) {
+            const int j = lane * (kSpecMaxChunks / 32) + e;
+            c[e] = j < chunks ? sm.tot[round][j] : 0ull;
+            mine += c[e];
+        }
+        unsigned long long incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
+        if (total) {
+            const unsigned long long u24 = __float2ull_rz(u * 16777216.0f);
+            thresh = (__umul64hi(u24, total) << 40) | ((u24 * total) >> 24);
+            // the lane whose range holds the first prefix above the threshold
+            const unsigned m = __ballot_sync(0xffffffffu, incl > thresh);
+            const int l = __ffs(m) - 1;  // m != 0: the last lane's prefix is the total > thresh
+            unsigned long long run = __shfl_sync(0xffffffffu, incl - mine, l);
+            int found = -1;
+            unsigned long long found_base = 0;
+            if (lane == l) {
+#pragma unroll
+                for (int e = 0; e < kSpecMaxChunks / 32; ++e) {
+                    if (found < 0 && run + c[e] > thresh) {
+                        found = lane * (kSpecMaxChunks / 32) + e;
+                        found_base = run;
+                    }
+                    run += c[e];
+                }
+            }
+            chunk = __shfl_sync(0xffffffffu, found, l);
+            base = __shfl_sync(0xffffffffu, found_base, l);
+        }
+        if (lane == 0) {
+            sm.tok = chunk < 0 ? -1 : -2;
+            sm.scan[0] = base;
+            sm.scan[1] = thresh;
+            sm.scan[2] = (unsigned long long)(long long)chunk;
+        }
+    }
+    __syncthreads();
+    chunk = (int)(long long)sm.scan[2];
+    if (chunk < 0) return -1;                               // every weight is 0 (all CTAs agree)
+    if (chunk % kSpecCluster != (int)rank) return -2;       // another CTA owns the threshold's chunk
+    base = sm.scan[0];
+    thresh = sm.scan[1];
+    __syncthreads();  // scan[] is reused below
+    // Pass 2, in the owner: the chunk's entries in order (each thread's four, then a block scan),
+    // from the registers of pass 1 when the chunk was in its last group.
+    const int v0 = chunk * kSpecChunk + 4 * t;
+    const int jl = chunk / kSpecCluster - g_last;
+    float4 wc;
+    if (jl >= 0 && jl < kSpecGroup) {
+        wc = w[0];
+#pragma unroll
+        for (int q = 1; q < kSpecGroup; ++q)
+            if (q == jl) wc = w[q];
+    } else {
+        wc = draw_weights4(a, b, v0, vocab, vec);
+    }
+    const unsigned long long x[4] = {fixed40(wc.x), fixed40(wc.y), fixed40(wc.z), fixed40(wc.w)};
+    const unsigned long long mine = x[0] + x[1] + x[2] + x[3];
+    unsigned long long incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) sm.scan[warp] = incl;
+    __syncthreads();
+    unsigned long long before = base + (incl - mine);
+    for (int w2 = 0; w2 < warp; ++w2) before += sm.scan[w2];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (before <= thresh && before + x[c] > thresh && v0 + c < vocab) sm.tok = v0 + c;
+        before += x[c];
     }
     __syncthreads();
     const int tok = sm.tok;
-    __syncthreads();
-    if (j < 0) return -1;
     return tok < 0 ? vocab - 1 : tok;
 }
 
-// One CTA per sequence.
-__global__ void __launch_bounds__(kSpecThreads) spec_verify_kernel(const SpecParams p) {
+// One cluster of kSpecCluster CTAs per sequence (grid: num_seqs * kSpecCluster).
+__global__ void __launch_bounds__(kSpecThreads, 2) spec_verify_kernel(const SpecParams p) {
     griddep_launch_dependents();
     __shared__ DrawSmem sm;
     __shared__ int s_pos;
     __shared__ int s_ok[64];
     __shared__ int s_tokv[64];
-    const int n = blockIdx.x;
+    const int n = blockIdx.x / kSpecCluster;
     const long long V = p.vocab;
     const float* pl = p.target + (long long)n * (p.k + 1) * V;
     const float* pd = p.draft + (long long)n * p.k * V;
     int* out = p.out_tokens + (long long)n * (p.k + 1);
+    // The uniforms are loaded up front, beside the draft tokens: on cold data every dependent
+    // load is a DRAM round trip, and only the probability lookups depend on the tokens.
+    const float u = __ldg(p.u_sample + n);
     // Every draft position's accept decision in parallel (thread i), then the left-to-right
-    // scan for the first rejection on the flags.
+    // scan for the first rejection on the flags.  Every CTA of the cluster takes the same
+    // decisions from the same values.
     if (threadIdx.x < p.k) {
         const int i = threadIdx.x;
-        const int t = p.draft_tokens[(long long)n * p.k + i];
+        const int t = __ldg(p.draft_tokens + (long long)n * p.k + i);
+        const float ua = __ldg(p.u_accept + (long long)n * p.k + i);
         bool accept = false;
         if (t < 0 || t >= p.vocab) {  // not a token: counts as a rejection
-            atomicOr(&g_pa_error, PA_DEVERR_TOKEN);
+            if (cluster_rank() == 0) atomicOr(&g_pa_error, PA_DEVERR_TOKEN);
         } else {
-            const float a = pl[i * V + t], b = pd[i * V + t];
-            accept = a >= b;
-            if (!accept) accept = p.u_accept[(long long)n * p.k + i] < __fdiv_rn(a, b);
+            const float a = __ldg(pl + i * V + t), b = __ldg(pd + i * V + t);
+            accept = a >= b || ua < __fdiv_rn(a, b);
         }
         s_ok[i] = accept;
         s_tokv[i] = t;
@@ -355,18 +451,17 @@ __global__ void __launch_bounds__(kSpecThreads) spec_verify_kernel(const SpecPar
     __syncthreads();
     if (threadIdx.x == 0) {
         int i = 0;
-        while (i < p.k && s_ok[i]) {
-            out[i] = s_tokv[i];
-            ++i;
-        }
+        while (i < p.k && s_ok[i]) ++i;
         s_pos = i;
     }
     __syncthreads();
     const int i = s_pos;
-    const float u = p.u_sample[n];
-    int tok = block_draw(pl + i * V, i < p.k ? pd + i * V : nullptr, p.vocab, u, sm);
-    if (tok < 0 && i < p.k) tok = block_draw(pl + i * V, nullptr, p.vocab, u, sm);
-    if (threadIdx.x == 0) {
+    int tok = cluster_draw(pl + i * V, i < p.k ? pd + i * V : nullptr, p.vocab, u, 0, sm);
+    // An all-zero residual: the draw falls back to p_large[i] (every CTA takes this branch).
+    if (tok == -1 && i < p.k) tok = cluster_draw(pl + i * V, nullptr, p.vocab, u, 1, sm);
+    // The CTA that drew the token (rank 0 if nothing was drawable) writes the outputs.
+    if (threadIdx.x == 0 && (tok != -2) && (tok != -1 || cluster_rank() == 0)) {
+        for (int jj = 0; jj < i; ++jj) out[jj] = s_tokv[jj];
         out[i] = tok;
         for (int jj = i + 1; jj <= p.k; ++jj) out[jj] = -1;
         p.num_accepted[n] = i;
@@ -1935,8 +2030,21 @@ int launch_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* 
     p.u_sample = u_sample;
     p.k = k;
     p.vocab = vocab;
-    spec_verify_kernel<<<num_seqs, kSpecThreads, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    // One cluster of kSpecCluster CTAs per sequence.
+    if (num_seqs > 0x7fffffff / kSpecCluster) return PA_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)num_seqs * kSpecCluster);
+    cfg.blockDim = dim3(kSpecThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kSpecCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, spec_verify_kernel, p) != cudaSuccess) return PA_ERR_CUDA;
     *launches += 1;
     return PA_OK;
 }

@@ -35,7 +35,9 @@ def run_both(x: W.SpecInputs):
 
 
 @pytest.mark.parametrize("n,k,v,noise,seed", [(64, 4, 32000, 1.0, 1), (257, 1, 1000, 0.5, 2), (16, 8, 32000, 3.0, 3),
-                                              (64, 4, 32000, 0.0, 4), (33, 4, 4096, 6.0, 5), (8, 0, 513, 1.0, 6)])
+                                              (64, 4, 32000, 0.0, 4), (33, 4, 4096, 6.0, 5), (8, 0, 513, 1.0, 6),
+                                              (16, 4, 32001, 1.0, 10), (12, 3, 4097, 2.0, 11),
+                                              (10, 2, 20478, 1.5, 12)])
 def test_spec_verify_matches_oracle(n, k, v, noise, seed):
     x = W.spec_verify_inputs(num_seqs=n, k=k, vocab=v, seed=seed, noise=noise)
     acc, out, ra, ro = run_both(x)
@@ -64,8 +66,8 @@ def test_spec_verify_bad_draft_token_is_flagged():
 
 
 def test_spec_verify_largest_vocabulary_last_chunk():
-    """The largest vocabulary (64 chunks of 4096 entries, split over the cluster's CTAs) with
-    uniforms that put every draw in the last chunk."""
+    """The largest vocabulary (64 chunks of 4096 entries) with uniforms that put every draw in
+    the last chunk."""
     x = W.spec_verify_inputs(num_seqs=8, k=2, vocab=262144, seed=9)
     x.u_sample[:] = np.float32(0.999999)
     acc, out, ra, ro = run_both(x)
