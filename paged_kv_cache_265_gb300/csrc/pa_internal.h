@@ -128,6 +128,12 @@ bool use_prefill_tc(const DecodeArgs& a);
 // with the sequence's other pieces (partial slots part_start[i] + 1 ..) and writes the output.
 int launch_prefix_tc(const DecodeArgs& a, const int* part_start, const float2* pml, const float* pacc,
                      cudaStream_t stream, int* launches);
+// A shared-prefix call with at least kTcSuffixMinRows query rows per kv head, entirely on
+// tcgen05 (pa_prefill.cu): the suffix kernel (positions after each sequence's prefix; suffix
+// pieces to partial slot i) then the prefix kernel (merges them and writes the output).
+constexpr int kTcSuffixMinRows = 16;
+int launch_shared_prefix_tc(const DecodeArgs& a, float2* pml, float* pacc, cudaStream_t stream, int* launches);
+
 // Smallest split-K partition the library chooses for a shared-prefix call (the workspace of a
 // call with partition 0 is sized for it).
 constexpr int kMinPrefixPartition = 512;

@@ -2062,6 +2062,15 @@ bool use_prefill_tc(const DecodeArgs& a) {
 int launch_decode(const DecodeArgs& args, cudaStream_t stream, int* launches, int* partition_used) {
     *partition_used = 0;
     if (!args.groups && use_prefill_tc(args)) return launch_prefill_tc(args, stream, launches);  // no split
+    if (args.groups && !args.fp8 && (args.num_heads / args.num_kv_heads) * args.q_len >= kTcSuffixMinRows) {
+        // Shared prefixes with enough rows per kv head: suffixes and prefixes on tcgen05 (no split;
+        // the suffix pieces go to the workspace's first per-sequence partial slots).
+        const WsLayout w = ws_layout(args.num_seqs, args.q_len, args.num_heads, args.head_dim, args.max_context_len,
+                                     args.partition, true);
+        uint8_t* ws = static_cast<uint8_t*>(args.workspace);
+        return launch_shared_prefix_tc(args, reinterpret_cast<float2*>(ws + w.pml), reinterpret_cast<float*>(ws + w.pacc),
+                                       stream, launches);
+    }
     DecodeArgs a = args;
     if (a.partition_auto) {
         DeviceInfo dev;

@@ -102,6 +102,9 @@ struct PrefillTcParams {
     const int* part_start;  // first partial slot of each sequence (the prefix piece's, not stored)
     const float2* pml;      // (max in log2 units, sum) per partial row
     const float* pacc;      // unnormalised partial outputs, fp32
+    // Suffix mode: where a sequence with a shared prefix leaves its suffix piece (slot i).
+    float2* pml_out;
+    float* pacc_out;
 };
 
 template <int D>
@@ -161,12 +164,18 @@ struct TcTile {
     int L;         // chunk mode: the sequence's length; prefix mode: the prefix length
     bool valid;
     int nblk;      // pool blocks the tile streams
-    int lastblk;   // the last of them is short by sh rows (chunk mode only)
+    int lastblk;   // the last of them (counted from blk0) is short by sh rows (chunk modes only)
     int sh;
+    int blk0;      // first pool block of the tile's positions, in the sequence's table
 };
 
-template <bool kPrefix>
+// Kernel modes: the chunk kernel, the shared-prefix kernel, and the suffix kernel (chunk rows
+// against the positions after each sequence's shared prefix).
+enum : int { kModeChunk = 0, kModePrefix = 1, kModeSuffix = 2 };
+
+template <int kMode>
 __device__ __forceinline__ TcTile tc_tile(const PrefillTcParams& p, const PrefixGroups* g) {
+    constexpr bool kPrefix = kMode == kModePrefix;
     TcTile w;
     const int idx = blockIdx.x;
     if constexpr (kPrefix) {
@@ -186,6 +195,7 @@ __device__ __forceinline__ TcTile tc_tile(const PrefillTcParams& p, const Prefix
         w.nblk = w.L / 16;
         w.lastblk = w.nblk - 1;
         w.sh = 0;
+        w.blk0 = 0;
     } else {
         // Tiles of one (sequence, kv head) are adjacent and share its K/V in L2; the
         // last rows (the longest causal ranges) go first.
@@ -195,17 +205,22 @@ __device__ __forceinline__ TcTile tc_tile(const PrefillTcParams& p, const Prefix
         w.row0 = mt * kTcRows;
         w.rows = p.total_rows;
         w.L = p.context_lens[w.seq];
-        w.valid = seq_len_valid(w.L, p.q_len, 0, p.max_context_len, p.max_blocks_per_seq);
+        // Suffix mode: the positions before the sequence's shared prefix end are another kernel's.
+        const int skip = kMode == kModeSuffix ? prefix_of(*g, w.seq) : 0;
+        w.blk0 = skip / 16;
+        w.valid = seq_len_valid(w.L, p.q_len, skip, p.max_context_len, p.max_blocks_per_seq);
         const int t_last = min((w.row0 + kTcRows - 1) / p.group, p.q_len - 1);
-        w.nblk = w.valid ? (w.L - p.q_len + t_last) / 16 + 1 : 0;  // blocks this tile sees
-        w.lastblk = (w.L - 1) / 16;           // the sequence's last block ...
-        w.sh = 16 * (w.lastblk + 1) - w.L;    // ... is short by sh rows, fetched as leading zeros
+        // blocks this tile sees, counted from block blk0
+        w.nblk = w.valid ? (w.L - p.q_len + t_last) / 16 + 1 - w.blk0 : 0;
+        w.lastblk = (w.L - 1) / 16 - w.blk0;      // the sequence's last block ...
+        w.sh = 16 * ((w.L - 1) / 16 + 1) - w.L;   // ... is short by sh rows, fetched as leading zeros
     }
     return w;
 }
 
-template <typename T, int D, bool kPrefix>
+template <typename T, int D, int kMode>
 __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const PrefixGroups* g) {
+    constexpr bool kPrefix = kMode == kModePrefix;
     using Lay = TcLayout<D>;
     using IsBf16 = std::integral_constant<bool, std::is_same<T, __nv_bfloat16>::value>;
     extern __shared__ uint8_t smem_raw[];
@@ -252,7 +267,7 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
     // waits for the plan kernel's partial slots.
     if constexpr (!kPrefix) griddep_wait();
 
-    const TcTile tile = tc_tile<kPrefix>(p, g);
+    const TcTile tile = tc_tile<kMode>(p, g);
     const int seq = tile.seq, kvh = tile.kvh, row0 = tile.row0, L = tile.L, nblk = tile.nblk;
     const int lastblk = tile.lastblk, sh = tile.sh;
     const bool valid = tile.valid;
@@ -261,7 +276,7 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
 
     if (valid && warp == 8) {
         // ===================== TMA producer =====================
-        const int* bt = p.block_tables + (long long)seq * p.max_blocks_per_seq;
+        const int* bt = p.block_tables + (long long)seq * p.max_blocks_per_seq + tile.blk0;
         int armed[kTcStages] = {0, 0, 0};
         // Block ids arrive 32 at a time (four tiles): lane l holds the id of block 32c + l
         // of chunk c, and chunk c + 1 is requested when chunk c starts, so no tile waits on
@@ -419,15 +434,28 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
 
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
+        // A warp whose 32 tile rows are all padding (a tile of a few real rows) computes nothing:
+        // its weights and outputs are never used.  It still waits for each tile's scores and for
+        // the previous tile's products before it arrives, so its arrivals for a tile never mix
+        // with the next tile's.
+        const bool idle = row0 + 32 * (warp & 3) >= tile.rows;
         for (int j = 0; j < ntiles; ++j) {
             if (!__all_sync(0xffffffffu, mbar_wait(sfull + 8 * (j & 1), (j >> 1) & 1, err, abort_flag, p.wait_limit_ns))) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
+            if (idle) {
+                if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(odone, (j - 1) & 1, err, abort_flag, p.wait_limit_ns))) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive(pfull);
+                continue;
+            }
             const uint32_t buf = lane_tmem + kTmemS + (uint32_t)(j & 1) * 128;
             const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
-            const int pos0 = kTcPos * j;
+            const int pos0 = 16 * tile.blk0 + kTcPos * j;
             // Column c holds position pos0 + c, except in the sequence's short last block
             // (columns lastc .. lastc + 15), whose first sh columns are zero rows and whose
             // column c holds position pos0 + c - sh.
@@ -548,11 +576,13 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
                     // A sequence the plan found invalid has no slot of its own: nothing is written.
                     const bool write = real && seq_len_valid(p.context_lens[rseq], p.q_len, L, p.max_context_len,
                                                              p.max_blocks_per_seq);
-                    const long long slot0 = write ? p.part_start[rseq] : 0;
+                    // The sequence's other pieces: partial slots part_start[i] + 1 .. (split-K
+                    // partitions), or without part_start the one suffix piece in slot i.
+                    const long long slot0 = !write ? 0 : p.part_start ? p.part_start[rseq] : rseq - 1;
                     const float l_pre = lsum[r] + lsum[kTcRows + r];
                     // Merge the prefix piece (m_run, l_pre, O in TMEM) with the sequence's other
                     // pieces, in slot order, by their log-sum-exp, and write the output row.
-                    const int npieces = write ? p.part_start[rseq + 1] - (int)slot0 : 1;
+                    const int npieces = !write ? 1 : p.part_start ? p.part_start[rseq + 1] - (int)slot0 : 2;
                     const long long stride = (long long)p.q_len * p.num_heads;
                     const long long prow0 = (slot0 * p.q_len + t) * p.num_heads + hq;
                     float M = m_run;
@@ -599,6 +629,27 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
                         }
                     }
                 }
+            } else if (kMode == kModeSuffix && tile.blk0 > 0) {
+                // A sequence with a shared prefix: its suffix piece (m, l, unnormalised O) goes to
+                // partial slot i for the prefix kernel, which merges and writes the output.
+                if (__all_sync(0xffffffffu, mbar_wait(lready, 0, err, abort_flag, p.wait_limit_ns))) {
+                    tc::fence_after_sync();
+                    const long long prow = row_id;  // slot i: (i * q_len + t) * Hq + hq
+                    if (real && hf == 0) p.pml_out[prow] = make_float2(m_run, lsum[r] + lsum[kTcRows + r]);
+                    float4* dst = reinterpret_cast<float4*>(p.pacc_out + prow * D) + hf * (D / 8);
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h) {
+                        uint32_t o[32];
+                        tc::ld_x32(o_half + 32 * h, o);
+                        if (real) {
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                dst[h * 8 + c] =
+                                    make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
+                                                __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3]));
+                        }
+                    }
+                }
             } else if (__all_sync(0xffffffffu, mbar_wait(lready, 0, err, abort_flag, p.wait_limit_ns))) {
                 tc::fence_after_sync();
                 const float inv = 1.f / (lsum[r] + lsum[kTcRows + r]);
@@ -634,14 +685,22 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillTcParams p) {
-    tc_attention<T, D, false>(p, nullptr);
+    tc_attention<T, D, kModeChunk>(p, nullptr);
 }
 
 // The shared prefix of every prefix group once per kv head for all the group's query rows.
 template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefix_tc_kernel(const __grid_constant__ PrefillTcParams p, const __grid_constant__ PrefixGroups g) {
-    tc_attention<T, D, true>(p, &g);
+    tc_attention<T, D, kModePrefix>(p, &g);
+}
+
+// Each sequence's chunk rows against its positions after its group's shared prefix (all of
+// them for a sequence outside every group, which then gets its output here).
+template <typename T, int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    suffix_tc_kernel(const __grid_constant__ PrefillTcParams p, const __grid_constant__ PrefixGroups g) {
+    tc_attention<T, D, kModeSuffix>(p, &g);
 }
 
 // Parameters shared by the chunk and prefix launches.
@@ -668,6 +727,8 @@ int tc_params(const DecodeArgs& a, PrefillTcParams& p) {
     p.part_start = nullptr;
     p.pml = nullptr;
     p.pacc = nullptr;
+    p.pml_out = nullptr;
+    p.pacc_out = nullptr;
     return PA_OK;
 }
 
@@ -693,6 +754,37 @@ int launch_prefill_tc_typed(const DecodeArgs& a, cudaStream_t stream, int* launc
 
 template <typename T, int D>
 int launch_prefix_tc_typed(const DecodeArgs& a, const int* part_start, const float2* pml, const float* pacc,
+                           cudaStream_t stream, int* launches);
+
+// A shared-prefix call entirely on tcgen05: the suffix kernel (one CTA per (sequence, kv head,
+// 128-row tile) over the positions after the sequence's prefix; sequences outside every group
+// get their output there), then the prefix kernel, which merges each grouped row's suffix piece
+// (partial slot i) and writes the output.
+template <typename T, int D>
+int launch_shared_prefix_tc_typed(const DecodeArgs& a, float2* pml, float* pacc, cudaStream_t stream, int* launches) {
+    PrefillTcParams p;
+    if (int st = tc_params<D>(a, p)) return st;
+    p.pml_out = pml;
+    p.pacc_out = pacc;
+    const long long grid = (long long)a.num_seqs * a.num_kv_heads * p.mtiles;
+    if (grid > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    auto sfn = suffix_tc_kernel<T, D>;
+    const int smem = TcLayout<D>::kAlloc;
+    if (int st = ensure_dynamic_smem(reinterpret_cast<const void*>(sfn), smem)) return st;
+    const int pc = profile_call_begin();
+    profile_mark(pc, 0, stream);
+    profile_mark(pc, 1, stream);
+    if (launch_pdl(sfn, dim3((unsigned)grid), dim3(kTcThreads), (size_t)smem, stream, p, *a.groups) != cudaSuccess)
+        return PA_ERR_CUDA;
+    *launches += 1;
+    profile_mark(pc, 2, stream);
+    const int st = launch_prefix_tc_typed<T, D>(a, nullptr, pml, pacc, stream, launches);
+    profile_mark(pc, 3, stream);
+    return st;
+}
+
+template <typename T, int D>
+int launch_prefix_tc_typed(const DecodeArgs& a, const int* part_start, const float2* pml, const float* pacc,
                            cudaStream_t stream, int* launches) {
     const PrefixGroups& g = *a.groups;
     const int grid = g.tile_start[g.n];
@@ -712,6 +804,18 @@ int launch_prefix_tc_typed(const DecodeArgs& a, const int* part_start, const flo
 }
 
 }  // namespace
+
+int launch_shared_prefix_tc(const DecodeArgs& a, float2* pml, float* pacc, cudaStream_t stream, int* launches) {
+    if (a.fp8 || !a.groups) return PA_ERR_UNSUPPORTED;
+    if (a.dtype == PA_BF16) {
+        if (a.head_dim == 128) return launch_shared_prefix_tc_typed<__nv_bfloat16, 128>(a, pml, pacc, stream, launches);
+        if (a.head_dim == 64) return launch_shared_prefix_tc_typed<__nv_bfloat16, 64>(a, pml, pacc, stream, launches);
+    } else {
+        if (a.head_dim == 128) return launch_shared_prefix_tc_typed<__half, 128>(a, pml, pacc, stream, launches);
+        if (a.head_dim == 64) return launch_shared_prefix_tc_typed<__half, 64>(a, pml, pacc, stream, launches);
+    }
+    return PA_ERR_UNSUPPORTED;
+}
 
 int launch_prefill_tc(const DecodeArgs& a, cudaStream_t stream, int* launches) {
     if (a.fp8) return PA_ERR_UNSUPPORTED;
