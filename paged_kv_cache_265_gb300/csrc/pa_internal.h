@@ -176,6 +176,8 @@ int kv_tensor_map(CUtensorMap* map, const void* base, int dtype, int64_t num_blo
                   int head_dim);
 // Device address of the library's error word (PA_DEVERR_* bits) on the current device.
 int device_error_word(int** ptr);
+// Number of SMs of the current device (cached per device).
+int sm_count(int* sms);
 // Raises a kernel's dynamic shared-memory limit to `smem` bytes if it is lower.
 int ensure_dynamic_smem(const void* fn, int smem);
 

@@ -1933,6 +1933,13 @@ int device_error_word(int** ptr) {
     return PA_OK;
 }
 
+int sm_count(int* sms) {
+    DeviceInfo d;
+    if (int st = device_info(d)) return st;
+    *sms = d.sms;
+    return PA_OK;
+}
+
 int ensure_dynamic_smem(const void* fn, int smem) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;

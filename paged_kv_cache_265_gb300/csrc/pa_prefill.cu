@@ -58,6 +58,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "pa_device.cuh"
@@ -66,6 +67,10 @@
 
 namespace pa {
 namespace {
+
+#ifndef PA_TC_SUFFIX_PERSISTENT
+#define PA_TC_SUFFIX_PERSISTENT 1
+#endif
 
 constexpr int kTcRows = 128;             // query rows per CTA tile (MMA M)
 constexpr int kTcPos = 128;              // positions per K/V tile
@@ -96,6 +101,7 @@ struct PrefillTcParams {
     int total_rows;  // group * q_len query rows per kv head
     int mtiles;      // 128-row tiles per kv head
     int max_context_len;
+    int num_units;   // chunk and suffix modes: (sequence, kv head, 128-row tile) units
     float scale_log2;
     unsigned long long wait_limit_ns;  // limit of the pipeline waits (pa_set_wait_limit_ns)
     // Shared-prefix mode: the other pieces of each sequence, merged with the prefix's.
@@ -174,12 +180,11 @@ struct TcTile {
 enum : int { kModeChunk = 0, kModePrefix = 1, kModeSuffix = 2 };
 
 template <int kMode>
-__device__ __forceinline__ TcTile tc_tile(const PrefillTcParams& p, const PrefixGroups* g) {
+__device__ __forceinline__ TcTile tc_tile(const PrefillTcParams& p, const PrefixGroups* g, int idx) {
     constexpr bool kPrefix = kMode == kModePrefix;
     TcTile w;
-    const int idx = blockIdx.x;
     if constexpr (kPrefix) {
-        int lo = 0, hi = g->n - 1;  // the group whose tiles hold this CTA
+        int lo = 0, hi = g->n - 1;  // the group whose tiles hold this unit
         while (lo < hi) {
             const int mid = (lo + hi + 1) / 2;
             if (g->tile_start[mid] <= idx) lo = mid; else hi = mid - 1;
@@ -267,34 +272,52 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
     // waits for the plan kernel's partial slots.
     if constexpr (!kPrefix) griddep_wait();
 
-    const TcTile tile = tc_tile<kMode>(p, g);
-    const int seq = tile.seq, kvh = tile.kvh, row0 = tile.row0, L = tile.L, nblk = tile.nblk;
-    const int lastblk = tile.lastblk, sh = tile.sh;
-    const bool valid = tile.valid;
-    if (!kPrefix && !valid && threadIdx.x == 0) atomicOr(err, PA_DEVERR_CONTEXT);  // rows left untouched
-    const int ntiles = (nblk + kTcBlocks - 1) / kTcBlocks;
+    // The CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ... (one CTA per SM).  Every role
+    // walks the same units and counts their K/V tiles in one running index gt, so stage, S
+    // buffer and barrier phases carry on from one unit to the next; per-unit barriers (qready,
+    // lready) count valid units (vu).  Tensor memory and the barriers are set up once.
+    const int num_units = kPrefix ? g->tile_start[g->n] : p.num_units;
+    // Chunk mode launches one CTA per unit: its running indices are the compile-time 0 of a
+    // single unit (the loop below runs once), and the loop costs it nothing.
+    constexpr bool kLoop = kMode != kModeChunk;
+    const int u_step = kLoop ? (int)gridDim.x : num_units;
 
-    if (valid && warp == 8) {
+    if (warp == 8) {
         // ===================== TMA producer =====================
-        const int* bt = p.block_tables + (long long)seq * p.max_blocks_per_seq + tile.blk0;
         int armed[kTcStages] = {0, 0, 0};
+        int gt_run = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < num_units; u += u_step) {
+        const TcTile tile = tc_tile<kMode>(p, g, u);
+        if (!tile.valid) {
+            if (!kPrefix && lane == 0) atomicOr(err, PA_DEVERR_CONTEXT);  // rows left untouched
+            continue;
+        }
+        const int kvh = tile.kvh, nblk = tile.nblk, lastblk = tile.lastblk, sh = tile.sh;
+        const int ntiles = (nblk + kTcBlocks - 1) / kTcBlocks;
+        const int* bt = p.block_tables + (long long)tile.seq * p.max_blocks_per_seq + tile.blk0;
         // Block ids arrive 32 at a time (four tiles): lane l holds the id of block 32c + l
         // of chunk c, and chunk c + 1 is requested when chunk c starts, so no tile waits on
         // a block-table load.
         int ids = lane < nblk ? __ldg(bt + lane) : 0;
         int ids_next = 32 + lane < nblk ? __ldg(bt + 32 + lane) : 0;
+        const int gtb = kLoop ? gt_run : 0;
         for (int j = 0; j < ntiles; ++j) {
-            const int s = j % kTcStages;
+            const int gt = gtb + j;
+            const int s = gt % kTcStages;
             const int jj = j & 3;
             if (jj == 0 && j > 0) {
                 ids = ids_next;
                 const int nxt = 32 * ((j >> 2) + 1) + lane;
                 ids_next = nxt < nblk ? __ldg(bt + nxt) : 0;
             }
-            if (j >= kTcStages) {
+            if (gt >= kTcStages) {
                 bool w = true;
-                if (lane == 0) w = mbar_wait(kvempty + 8 * s, ((j / kTcStages) - 1) & 1, err, abort_flag, p.wait_limit_ns);
-                if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
+                if (lane == 0) w = mbar_wait(kvempty + 8 * s, ((gt / kTcStages) - 1) & 1, err, abort_flag, p.wait_limit_ns);
+                if (!__shfl_sync(0xffffffffu, (int)w, 0)) {
+                    ok = false;
+                    break;
+                }
             }
             const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
             const int bid = __shfl_sync(0xffffffffu, ids, (8 * jj + lane) & 31);
@@ -315,12 +338,14 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
             }
             ++armed[s];
         }
+        gt_run += ntiles;
+        }
         // No copy may still be landing when the CTA exits.
         if (lane == 0)
             for (int s = 0; s < kTcStages; ++s)
                 if (armed[s] > 0) mbar_wait(kvfull + 8 * s, (armed[s] - 1) & 1, err, nullptr);
         __syncwarp();
-    } else if (valid && warp == 9) {
+    } else if (warp == 9) {
         // ===================== MMA issuer =====================
         // Order: S_j, then P_{j-1} V_{j-1}.  S_j overwrites the buffer P_{j-2} was read
         // from, so it waits for P_{j-2} V_{j-2} to complete.
@@ -334,35 +359,50 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
             // 256 KB, so the 14-bit field never carries into the next one.
             const uint64_t kdesc0 = tc::smem_desc_sw128(st_s, 16, 1024);
             const uint64_t vdesc0 = tc::smem_desc_sw128(st_s + Lay::kKBytes, kRegion, 1024);
-            bool ok = mbar_wait(qready, 0, err, abort_flag, p.wait_limit_ns);
+            bool ok = true;
+            int gt_run = 0, vu_run = 0;
+            for (int u = blockIdx.x; ok && u < num_units; u += u_step) {
+            const TcTile tile = tc_tile<kMode>(p, g, u);
+            if (!tile.valid) continue;
+            const int nblk = tile.nblk;
+            const int ntiles = (nblk + kTcBlocks - 1) / kTcBlocks;
+            const int gt = kLoop ? gt_run : 0, vu = kLoop ? vu_run : 0;
+            // The unit's Q rows are in tensor memory (and, as every softmax thread arrives only
+            // after its epilogue of the previous unit, that unit's O has been read out).
+            ok = mbar_wait(qready, vu & 1, err, abort_flag, p.wait_limit_ns);
             for (int j = 0; ok && j <= ntiles; ++j) {
                 if (j < ntiles) {
-                    const int s = j % kTcStages;
-                    ok = mbar_wait(kvfull + 8 * s, (j / kTcStages) & 1, err, abort_flag, p.wait_limit_ns) &&
-                         (j < 2 || mbar_wait(odone, (j - 2) & 1, err, abort_flag, p.wait_limit_ns));
+                    const int g1 = gt + j, s = g1 % kTcStages;
+                    // S_g1 overwrites the buffer P_{g1-2} was read from.  Inside a unit the last
+                    // product issued is P_{g1-2} V; at a unit's first tile the previous unit's last
+                    // P_{g1-1} V is issued too, and the wait is on it (a parity wait is only
+                    // meaningful for the last phase issued).
+                    const int need = j == 0 ? g1 - 1 : g1 - 2;
+                    ok = mbar_wait(kvfull + 8 * s, (g1 / kTcStages) & 1, err, abort_flag, p.wait_limit_ns) &&
+                         (need < 0 || mbar_wait(odone, need & 1, err, abort_flag, p.wait_limit_ns));
                     if (!ok) break;
                     tc::fence_after_sync();
                     const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
                     const uint32_t id_s = tc::idesc_f16(kBf16, false, kTcRows, 16 * nb);
                     const uint64_t kd = kdesc0 + (uint64_t)((s * Lay::kStageBytes) >> 4);
-                    const uint32_t d_s = tmem + kTmemS + (uint32_t)(j & 1) * 128;
+                    const uint32_t d_s = tmem + kTmemS + (uint32_t)(g1 & 1) * 128;
                     mma_ts<false>(d_s, tmem + kTmemQ, kd, id_s);
 #pragma unroll
                     for (int kk = 1; kk < D / 16; ++kk)
                         mma_ts<true>(d_s, tmem + kTmemQ + kk * 8, kd + (((kk >> 2) * kRegion + (kk & 3) * 32) >> 4),
                                      id_s);
-                    tc::commit(sfull + 8 * (j & 1));
+                    tc::commit(sfull + 8 * (g1 & 1));
                 }
                 if (j > 0) {
-                    const int i = j - 1, s = i % kTcStages;
-                    ok = mbar_wait(pfull, i & 1, err, abort_flag, p.wait_limit_ns);
+                    const int i = j - 1, g0 = gt + i, s = g0 % kTcStages;
+                    ok = mbar_wait(pfull, g0 & 1, err, abort_flag, p.wait_limit_ns);
                     if (!ok) break;
                     tc::fence_after_sync();
                     const int nb = min(kTcBlocks, nblk - kTcBlocks * i);
                     const uint64_t vd = vdesc0 + (uint64_t)((s * Lay::kStageBytes) >> 4);
                     // K step kk = positions 16 kk .. 16 kk + 15: P_hi at column 64 (kk / 4) +
                     // 8 (kk % 4) of the buffer, P_lo 32 columns on; V rows 2048 B = 128 x 16 apart
-                    const uint32_t p_t = tmem + kTmemS + (uint32_t)(i & 1) * 128;
+                    const uint32_t p_t = tmem + kTmemS + (uint32_t)(g0 & 1) * 128;
                     if (i == 0)
                         mma_ts<false>(tmem + kTmemO, p_t, vd, id_o);
                     else
@@ -380,15 +420,30 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
                     tc::commit(odone);
                 }
             }
+            gt_run += ntiles;
+            ++vu_run;
+            }
             // No product may be in flight when TMEM is freed.
             tc::commit(drain);
             mbar_wait(drain, 0, err, nullptr);
         }
         __syncwarp();
-    } else if (valid) {
+    } else {
         // ===================== softmax and epilogue (warps 0-7) =====================
         const int hf = warp >> 2;                   // column half of the row this thread owns
         const int r = threadIdx.x & (kTcRows - 1);  // tile row = TMEM lane
+        const uint32_t lane_tmem = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t o_half = lane_tmem + kTmemO + (D / 2) * hf;  // this thread's half of O
+        const float c2 = p.scale_log2;
+        bool ok = true;
+        int gt_run = 0, vu_run = 0;
+        for (int u = blockIdx.x; ok && u < num_units; u += u_step) {
+        const TcTile tile = tc_tile<kMode>(p, g, u);
+        if (!tile.valid) continue;
+        const int gt = kLoop ? gt_run : 0, vu = kLoop ? vu_run : 0;
+        const int seq = tile.seq, kvh = tile.kvh, row0 = tile.row0, L = tile.L, nblk = tile.nblk;
+        const int lastblk = tile.lastblk, sh = tile.sh;
+        const int ntiles = (nblk + kTcBlocks - 1) / kTcBlocks;
         const int gr = row0 + r;
         const bool real = gr < tile.rows;
         // the row's sequence, chunk token and query head (padding rows: the tile's first row)
@@ -400,11 +455,8 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
         // sees the whole prefix.
         const int lim = kPrefix ? L - 1 : L - p.q_len + t;
         const int lim_min = kPrefix ? L - 1 : L - p.q_len + row0 / p.group;
-        const uint32_t lane_tmem = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        const uint32_t o_half = lane_tmem + kTmemO + (D / 2) * hf;  // this thread's half of O
         const long long row_id = ((long long)rseq * p.q_len + t) * p.num_heads + hq;
         const long long row_off = row_id * D;
-        const float c2 = p.scale_log2;
 
         // This thread's half of the Q row into TMEM lane r (rows past the chunk are zeros):
         // 32-bit column c holds elements 2c (low half) and 2c + 1, as the row lies in memory.
@@ -433,27 +485,27 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
         }
 
         float m_run = -INFINITY, l_run = 0.f;
-        bool ok = true;
         // A warp whose 32 tile rows are all padding (a tile of a few real rows) computes nothing:
         // its weights and outputs are never used.  It still waits for each tile's scores and for
         // the previous tile's products before it arrives, so its arrivals for a tile never mix
-        // with the next tile's.
+        // with the next tile's (for a unit's first tile its epilogue of the previous unit waited).
         const bool idle = row0 + 32 * (warp & 3) >= tile.rows;
         for (int j = 0; j < ntiles; ++j) {
-            if (!__all_sync(0xffffffffu, mbar_wait(sfull + 8 * (j & 1), (j >> 1) & 1, err, abort_flag, p.wait_limit_ns))) {
+            const int g1 = gt + j;
+            if (!__all_sync(0xffffffffu, mbar_wait(sfull + 8 * (g1 & 1), (g1 >> 1) & 1, err, abort_flag, p.wait_limit_ns))) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
             if (idle) {
-                if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(odone, (j - 1) & 1, err, abort_flag, p.wait_limit_ns))) {
+                if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(odone, (g1 - 1) & 1, err, abort_flag, p.wait_limit_ns))) {
                     ok = false;
                     break;
                 }
                 mbar_arrive(pfull);
                 continue;
             }
-            const uint32_t buf = lane_tmem + kTmemS + (uint32_t)(j & 1) * 128;
+            const uint32_t buf = lane_tmem + kTmemS + (uint32_t)(g1 & 1) * 128;
             const int nb = min(kTcBlocks, nblk - kTcBlocks * j);
             const int pos0 = 16 * tile.blk0 + kTcPos * j;
             // Column c holds position pos0 + c, except in the sequence's short last block
@@ -538,7 +590,7 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
             tc::st_x32(buf + 64 * hf, ph);
             tc::st_x32(buf + 64 * hf + 32, pl);
             // P_{j-1} V_{j-1} must be done before O is rescaled.
-            if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(odone, (j - 1) & 1, err, abort_flag, p.wait_limit_ns))) {
+            if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(odone, (g1 - 1) & 1, err, abort_flag, p.wait_limit_ns))) {
                 ok = false;
                 break;
             }
@@ -565,11 +617,11 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
         // Epilogue: the row's two half sums, then O / l, rounded once, to out[seq, t, hq, :]
         // (this thread's half of the columns); in prefix mode merged first with the sequence's
         // other pieces.
-        if (ok && __all_sync(0xffffffffu, mbar_wait(odone, (ntiles - 1) & 1, err, abort_flag, p.wait_limit_ns))) {
+        if (ok && __all_sync(0xffffffffu, mbar_wait(odone, (gt + ntiles - 1) & 1, err, abort_flag, p.wait_limit_ns))) {
             lsum[hf * kTcRows + r] = l_run;
             mbar_arrive(lready);
             if constexpr (kPrefix) {
-                if (__all_sync(0xffffffffu, mbar_wait(lready, 0, err, abort_flag, p.wait_limit_ns))) {
+                if (__all_sync(0xffffffffu, mbar_wait(lready, vu & 1, err, abort_flag, p.wait_limit_ns))) {
                     tc::fence_after_sync();
                     // The plan kernel's partial slots and the partition pass's pieces.
                     griddep_wait();
@@ -632,7 +684,7 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
             } else if (kMode == kModeSuffix && tile.blk0 > 0) {
                 // A sequence with a shared prefix: its suffix piece (m, l, unnormalised O) goes to
                 // partial slot i for the prefix kernel, which merges and writes the output.
-                if (__all_sync(0xffffffffu, mbar_wait(lready, 0, err, abort_flag, p.wait_limit_ns))) {
+                if (__all_sync(0xffffffffu, mbar_wait(lready, vu & 1, err, abort_flag, p.wait_limit_ns))) {
                     tc::fence_after_sync();
                     const long long prow = row_id;  // slot i: (i * q_len + t) * Hq + hq
                     if (real && hf == 0) p.pml_out[prow] = make_float2(m_run, lsum[r] + lsum[kTcRows + r]);
@@ -650,7 +702,7 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
                         }
                     }
                 }
-            } else if (__all_sync(0xffffffffu, mbar_wait(lready, 0, err, abort_flag, p.wait_limit_ns))) {
+            } else if (__all_sync(0xffffffffu, mbar_wait(lready, vu & 1, err, abort_flag, p.wait_limit_ns))) {
                 tc::fence_after_sync();
                 const float inv = 1.f / (lsum[r] + lsum[kTcRows + r]);
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row_off) + hf * (D / 16);
@@ -671,6 +723,10 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
                     }
                 }
             }
+        }
+        if (*abort_flag) ok = false;  // a wait of this unit gave up: no further unit
+        gt_run += ntiles;
+        ++vu_run;
         }
     }
 
@@ -722,6 +778,9 @@ int tc_params(const DecodeArgs& a, PrefillTcParams& p) {
     p.total_rows = p.group * a.q_len;
     p.mtiles = (p.total_rows + kTcRows - 1) / kTcRows;
     p.max_context_len = a.max_context_len;
+    const long long units = (long long)a.num_seqs * a.num_kv_heads * p.mtiles;
+    if (units > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    p.num_units = (int)units;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.wait_limit_ns = wait_limit_ns();
     p.part_start = nullptr;
@@ -736,15 +795,18 @@ template <typename T, int D>
 int launch_prefill_tc_typed(const DecodeArgs& a, cudaStream_t stream, int* launches) {
     PrefillTcParams p;
     if (int st = tc_params<D>(a, p)) return st;
-    const long long grid = (long long)a.num_seqs * a.num_kv_heads * p.mtiles;
-    if (grid > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    // One CTA per unit: the units of a prefill chunk are long and uneven (their causal ranges
+    // differ by up to the chunk), and the hardware's hand-out of CTAs to SMs as they free up
+    // balances them better than a fixed assignment of units to persistent CTAs (chunked-prefill
+    // batch: 317 vs 359 us).
+    const int grid = p.num_units;
     auto kfn = prefill_tc_kernel<T, D>;
     const int smem = TcLayout<D>::kAlloc;
     if (int st = ensure_dynamic_smem(reinterpret_cast<const void*>(kfn), smem)) return st;
     const int pc = profile_call_begin();
     profile_mark(pc, 0, stream);  // no plan kernel: marks 0 and 1 coincide
     profile_mark(pc, 1, stream);
-    if (launch_pdl(kfn, dim3((unsigned)grid), dim3(kTcThreads), (size_t)smem, stream, p) != cudaSuccess)
+    if (launch_pdl(kfn, dim3(grid), dim3(kTcThreads), (size_t)smem, stream, p) != cudaSuccess)
         return PA_ERR_CUDA;
     profile_mark(pc, 2, stream);
     profile_mark(pc, 3, stream);  // no merge kernel
@@ -766,15 +828,18 @@ int launch_shared_prefix_tc_typed(const DecodeArgs& a, float2* pml, float* pacc,
     if (int st = tc_params<D>(a, p)) return st;
     p.pml_out = pml;
     p.pacc_out = pacc;
-    const long long grid = (long long)a.num_seqs * a.num_kv_heads * p.mtiles;
-    if (grid > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    // Suffixes are a few tiles each: persistent CTAs (one per SM) save each unit the CTA's
+    // set-up (barriers, tensor memory, first copies).
+    int sms = 0;
+    if (int st = sm_count(&sms)) return st;
+    const int grid = PA_TC_SUFFIX_PERSISTENT ? std::min(p.num_units, sms) : p.num_units;
     auto sfn = suffix_tc_kernel<T, D>;
     const int smem = TcLayout<D>::kAlloc;
     if (int st = ensure_dynamic_smem(reinterpret_cast<const void*>(sfn), smem)) return st;
     const int pc = profile_call_begin();
     profile_mark(pc, 0, stream);
     profile_mark(pc, 1, stream);
-    if (launch_pdl(sfn, dim3((unsigned)grid), dim3(kTcThreads), (size_t)smem, stream, p, *a.groups) != cudaSuccess)
+    if (launch_pdl(sfn, dim3(grid), dim3(kTcThreads), (size_t)smem, stream, p, *a.groups) != cudaSuccess)
         return PA_ERR_CUDA;
     *launches += 1;
     profile_mark(pc, 2, stream);
@@ -787,17 +852,19 @@ template <typename T, int D>
 int launch_prefix_tc_typed(const DecodeArgs& a, const int* part_start, const float2* pml, const float* pacc,
                            cudaStream_t stream, int* launches) {
     const PrefixGroups& g = *a.groups;
-    const int grid = g.tile_start[g.n];
-    if (grid == 0) return PA_OK;
+    if (g.tile_start[g.n] == 0) return PA_OK;
     PrefillTcParams p;
     if (int st = tc_params<D>(a, p)) return st;
+    int sms = 0;
+    if (int st = sm_count(&sms)) return st;
+    const int grid = std::min(g.tile_start[g.n], sms);
     p.part_start = part_start;
     p.pml = pml;
     p.pacc = pacc;
     auto kfn = prefix_tc_kernel<T, D>;
     const int smem = TcLayout<D>::kAlloc;
     if (int st = ensure_dynamic_smem(reinterpret_cast<const void*>(kfn), smem)) return st;
-    if (launch_pdl(kfn, dim3((unsigned)grid), dim3(kTcThreads), (size_t)smem, stream, p, g) != cudaSuccess)
+    if (launch_pdl(kfn, dim3(grid), dim3(kTcThreads), (size_t)smem, stream, p, g) != cudaSuccess)
         return PA_ERR_CUDA;
     *launches += 1;
     return PA_OK;
