@@ -80,6 +80,7 @@ typedef enum {
 #define PA_DEVERR_TIMEOUT  0x8  /* a bounded wait inside a kernel gave up (internal error) */
 #define PA_DEVERR_INTERNAL 0x10 /* a kernel refused an inconsistent launch configuration (library bug) */
 #define PA_DEVERR_TOKEN    0x20 /* a draft token outside [0, vocab) (treated as rejected) */
+#define PA_DEVERR_QUERY_RANGE 0x40 /* FP8 caches: a bf16 query element of magnitude >= 65520 (beyond fp16) */
 
 #define PA_BLOCK_SIZE 16
 #define PA_DEFAULT_PARTITION 512  /* tokens per split-K partition */
@@ -329,9 +330,14 @@ int pa_decode_attention_noalloc(void* out, const void* query, const void* key_ca
  * pa_decode_attention_fp8kv: as pa_decode_attention_ex over FP8 caches (query and
  * out stay 16-bit, of dtype).  K and V bytes are widened exactly to fp16 in
  * registers; the score and P.V products run on the tensor cores in fp16 with fp32
- * accumulation (a bf16 query and the softmax weights P are rounded to fp16 for
- * them), k_scale folds into the softmax scale and v_scale into the output.
- * head_dim 128 only; the workspace is sized as for pa_decode_attention_ex.
+ * accumulation (the softmax weights P rounded to fp16), k_scale folds into the
+ * softmax scale and v_scale into the output.  A bf16 query is rounded to fp16 for
+ * the score products: exact for elements of magnitude 2^-17 .. 65504 (smaller ones
+ * are rounded to fp16's subnormal step, 2^-24).  An element of magnitude 65520 or
+ * more has no fp16 value: the call still completes and raises
+ * PA_DEVERR_QUERY_RANGE; the output row of that query row is undefined, the other
+ * rows are unaffected.  head_dim 128 only; the workspace is sized as for
+ * pa_decode_attention_ex.
  */
 int pa_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache, void* value_cache,
                              const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads, int head_dim,

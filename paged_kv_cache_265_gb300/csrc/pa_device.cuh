@@ -13,7 +13,7 @@ namespace pa {
 // A bounded wait gives up after this long and raises PA_DEVERR_TIMEOUT; every
 // legitimate wait in these kernels ends within microseconds.  Pipeline waits
 // take the limit of their launch (pa_set_wait_limit_ns), this by default.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+constexpr unsigned int kWaitLimitNs = 2000000000u;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -79,7 +79,7 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // non-blocking probe and reads the timer on every turn, so the wait gives up soon after
 // `limit_ns` even where a blocking probe would have slept until the phase completed.
 static __device__ __noinline__ bool mbar_wait_polled(uint32_t bar, uint32_t parity, int* err, volatile int* abort_flag,
-                                              unsigned long long limit_ns) {
+                                              unsigned int limit_ns) {
     const unsigned long long t0 = global_timer_ns();
     for (;;) {
         if (mbar_test_wait(bar, parity)) return true;
@@ -100,7 +100,7 @@ static __device__ __noinline__ bool mbar_wait_polled(uint32_t bar, uint32_t pari
 // always uses kWaitLimitNs, so no CTA leaves with work still in flight.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err,
                                           volatile int* abort_flag,
-                                          unsigned long long limit_ns = kWaitLimitNs) {
+                                          unsigned int limit_ns = kWaitLimitNs) {
     if (abort_flag && limit_ns < kWaitLimitNs) return mbar_wait_polled(bar, parity, err, abort_flag, limit_ns);
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();

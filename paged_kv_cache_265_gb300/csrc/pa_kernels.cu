@@ -659,7 +659,7 @@ struct alignas(128) DecodeParams {
     int slot_rows;     // min(8 NT, rows): rows each warp leaves in the combine buffer
     float scale_log2;  // scale * log2(e) (times the K dequantisation scale for an FP8 cache)
     float v_scale;     // V dequantisation scale (1 for 16-bit caches)
-    unsigned long long wait_limit_ns;  // limit of the pipeline waits (pa_set_wait_limit_ns)
+    unsigned int wait_limit_ns;  // limit of the pipeline waits (pa_set_wait_limit_ns), at most 2 s
 };
 
 // One work unit: positions tok0 .. tok0 + ntok - 1 of sequence `seq` (length len) for the kv
@@ -1052,7 +1052,12 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                     }
                 if constexpr (F8) {
                     // Same permuted contraction order as the K fragments: step kk of lane tig
-                    // takes query elements tig*32 + kk*4 .. +3; products run in fp16.
+                    // takes query elements tig*32 + kk*4 .. +3; products run in fp16.  A bf16
+                    // query is rounded to fp16 (exact for its 8 significant bits down to 2^-17);
+                    // an element of magnitude >= 65520 would become infinite, and is refused:
+                    // PA_DEVERR_QUERY_RANGE, that row's output undefined (each query row is its
+                    // own column of the products, so the other rows are unaffected).
+                    float amax = 0.f;
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         const uint8_t* qr = qrow + (nt * 8 + gid) * qpitch + tig * 64;
@@ -1064,6 +1069,8 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                             for (int h = 0; h < 2; ++h) {
                                 uint32_t r0 = w4[2 * h], r1 = w4[2 * h + 1];
                                 if constexpr (Elem<T>::kDtype == PA_BF16) {
+                                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(__uint_as_float(r0 << 16)), fabsf(__uint_as_float(r0 & 0xffff0000u))),
+                                                             fmaxf(fabsf(__uint_as_float(r1 << 16)), fabsf(__uint_as_float(r1 & 0xffff0000u)))));
                                     r0 = bf16x2_to_f16x2(r0);
                                     r1 = bf16x2_to_f16x2(r1);
                                 }
@@ -1072,6 +1079,8 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(NT, RT, F8))
                             }
                         }
                     }
+                    if (Elem<T>::kDtype == PA_BF16 && __any_sync(0xffffffffu, amax >= 65520.f) && lane == 0)
+                        atomicOr(&g_pa_error, PA_DEVERR_QUERY_RANGE);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qempty0 + 8 * qb);
@@ -1821,7 +1830,7 @@ int launch_decode_typed(const DecodeArgs& a, cudaStream_t stream, int* launches)
     p.partition = a.partition;
     p.scale_log2 = a.scale * (a.fp8 ? a.k_scale : 1.f) * 1.4426950408889634f;
     p.v_scale = a.fp8 ? a.v_scale : 1.f;
-    p.wait_limit_ns = wait_limit_ns();
+    p.wait_limit_ns = static_cast<unsigned int>(wait_limit_ns());
     // Each consumer warp owns 8 (NT = 1) or 16 (NT = 2) query rows of the kv head; the row
     // tiles per kv head are rounded up to a divisor of the consumer warp count (a third
     // tile becomes a fourth, all-padding one) so that every consumer warp owns exactly one

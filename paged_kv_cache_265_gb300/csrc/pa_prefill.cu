@@ -103,7 +103,7 @@ struct PrefillTcParams {
     int max_context_len;
     int num_units;   // chunk and suffix modes: (sequence, kv head, 128-row tile) units
     float scale_log2;
-    unsigned long long wait_limit_ns;  // limit of the pipeline waits (pa_set_wait_limit_ns)
+    unsigned int wait_limit_ns;  // limit of the pipeline waits (pa_set_wait_limit_ns), at most 2 s
     // Shared-prefix mode: the other pieces of each sequence, merged with the prefix's.
     const int* part_start;  // first partial slot of each sequence (the prefix piece's, not stored)
     const float2* pml;      // (max in log2 units, sum) per partial row
@@ -782,7 +782,7 @@ int tc_params(const DecodeArgs& a, PrefillTcParams& p) {
     if (units > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     p.num_units = (int)units;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    p.wait_limit_ns = wait_limit_ns();
+    p.wait_limit_ns = static_cast<unsigned int>(wait_limit_ns());
     p.part_start = nullptr;
     p.pml = nullptr;
     p.pacc = nullptr;

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libpa.so")
 PA_BF16, PA_FP16 = 0, 1
 PA_DEVERR_BLOCK_ID, PA_DEVERR_CONTEXT, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT, PA_DEVERR_INTERNAL = 1, 2, 4, 8, 16
 PA_DEVERR_TOKEN = 32
+PA_DEVERR_QUERY_RANGE = 64
 BLOCK_SIZE = 16
 DEFAULT_PARTITION = 512
 NOALLOC_WORKSPACE_BYTES = 32 << 20

@@ -33,6 +33,18 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), n
 
 
+def test_binding_constants_match_header():
+    """Every PA_* integer the header defines that the binding also names has the same value there."""
+    from paged_kv_cache_265_gb300 import pa
+
+    defines = dict(re.findall(r"^#define\s+(PA_[A-Z0-9_]+)\s+(0x[0-9a-fA-F]+|\d+)\b", open(HEADER).read(), flags=re.M))
+    assert "PA_DEVERR_QUERY_RANGE" in defines
+    shared = [n for n in defines if hasattr(pa, n)]
+    assert len(shared) >= 7
+    for n in shared:
+        assert getattr(pa, n) == int(defines[n], 0), n
+
+
 def test_status_strings(lib):
     for code, text in [(0, "ok"), (1, "invalid argument"), (2, "unsupported"), (3, "workspace"), (4, "CUDA")]:
         assert text in lib.pa_status_string(code).decode()

@@ -1,5 +1,7 @@
 """GPU parity of the FP8 (E4M3) KV cache against the oracle: the quantising append
 bit-exact over the whole pool, attention within the attention tolerance."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -92,3 +94,46 @@ def test_fp8_chunk_row_groups():
                         q_len=64, num_blocks=110, seed=42)
     got, ref = run_fp8(w)
     G.compare(got, ref, w.dtype, "fp8 chunk")
+
+
+def _query_row_scaled(w: W.Workload, row: int, log2_factor: int) -> W.Workload:
+    """The workload with query row `row` (a (sequence, token, head) row of the flattened query)
+    times 2^log2_factor, exact in bf16."""
+    q = G.bits_to_f64(w.query.ravel(), w.dtype).reshape(-1, w.head_dim)
+    q[row] *= 2.0 ** log2_factor
+    bits = torch.from_numpy(q.ravel()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(G.bits_to_f64(bits, "bf16"), q.ravel())
+    return dataclasses.replace(w, query=bits.reshape(w.query.shape))
+
+
+def test_fp8_bf16_query_beyond_fp16_is_refused():
+    """A bf16 query element beyond fp16's range (here a row scaled by 2^17, |q| up to ~5e5) has no
+    value in the fp16 score products: the call raises PA_DEVERR_QUERY_RANGE, and every other row
+    (another column of the products) still matches the oracle and the in-range call bit for bit."""
+    w = W.make_workload("fp8range", [1, 40, 700, 2100], num_heads=32, num_kv_heads=4, head_dim=128,
+                        dtype="bf16", q_len=1, num_blocks=190, seed=43)
+    base, _ = run_fp8(w)
+    assert pa.get_device_error(clear=True) == 0
+    bad_row = 2 * w.num_heads + 5  # sequence 2, head 5
+    wb = _query_row_scaled(w, bad_row, 17)
+    assert np.abs(G.bits_to_f64(wb.query.ravel(), "bf16")).max() >= 65520.0
+    got, ref = run_fp8(wb)
+    assert pa.get_device_error(clear=True) & pa.PA_DEVERR_QUERY_RANGE
+    keep = np.ones(got.reshape(-1, w.head_dim).shape[0], dtype=bool)
+    keep[bad_row] = False
+    g2, r2 = got.reshape(-1, w.head_dim)[keep], ref.reshape(-1, w.head_dim)[keep]
+    G.compare(g2, r2, w.dtype, "fp8 rows beside the refused one")
+    assert np.array_equal(g2, base.reshape(-1, w.head_dim)[keep])
+
+
+def test_fp8_bf16_query_at_fp16_edges():
+    """bf16 query rows at the edges of what fp16 holds exactly: a row scaled so its largest element
+    is just under 65504 and a row scaled down to about 2^-16: no flag, oracle tolerance."""
+    w = W.make_workload("fp8edge16", [33, 600], num_heads=16, num_kv_heads=4, head_dim=128, dtype="bf16",
+                        q_len=1, num_blocks=60, seed=44)
+    q = G.bits_to_f64(w.query.ravel(), "bf16").reshape(-1, w.head_dim)
+    big = int(np.floor(np.log2(65504.0 / np.abs(q[3]).max())))
+    wb = _query_row_scaled(_query_row_scaled(w, 3, big), 7, -14)
+    got, ref = run_fp8(wb)
+    assert pa.get_device_error(clear=True) == 0
+    G.compare(got, ref, w.dtype, "fp8 query rows at the fp16 edges")
