@@ -218,16 +218,37 @@ struct SpecParams {
     int vocab;
 };
 
-constexpr int kSpecCluster = 4;                      // CTAs per sequence
-constexpr int kSpecThreads = 256;                    // threads per CTA
+#ifndef PA_SPEC_CLUSTER
+#define PA_SPEC_CLUSTER 4
+#endif
+constexpr int kSpecCluster = PA_SPEC_CLUSTER;        // CTAs per sequence (4 or 8)
+constexpr int kSpecThreads = 1024 / kSpecCluster;    // threads per CTA
 constexpr int kSpecChunk = 4 * kSpecThreads;         // entries per chunk: thread t holds 4t .. 4t + 3
-constexpr int kSpecMaxChunks = 256;                  // vocabulary up to 262,144
+constexpr int kSpecMaxChunks = 262144 / kSpecChunk;  // vocabulary up to 262,144
 constexpr int kSpecOwn = kSpecMaxChunks / kSpecCluster;  // chunks one CTA may own
 constexpr int kSpecGroup = 8;                        // own chunks whose loads are in flight together
+constexpr int kSpecStageBytes = 2 * kSpecGroup * kSpecChunk * 4;  // one group of chunks of both rows
 
-// floor(x * 2^40) for 0 <= x < 2: the product is exact in fp32 (a power-of-two scale) and
-// the truncating conversion of a non-negative value is its floor.
-__device__ __forceinline__ unsigned long long fixed40(float x) { return __float2ull_rz(x * 1099511627776.0f); }
+// floor(x * 2^40) for 0 <= x < 2, built from the float's fields with integer operations (a
+// float-to-64-bit conversion instruction runs at the FP64 rate): x = m * 2^(e - 150) with
+// m = 1.f as a 24-bit integer (e >= 1), or x = f * 2^-149 for a subnormal (e = 0), so
+// x * 2^40 = m * 2^(e - 110), an exact left shift for e >= 110, else a right shift, which
+// drops exactly the fraction below 1.
+__device__ __forceinline__ unsigned long long fixed40(float x) {
+    const uint32_t b = __float_as_uint(x);
+    const int e = (int)(b >> 23);  // x >= 0: no sign bit
+    const uint32_t m = (b & 0x7fffffu) | (e ? 0x800000u : 0u);
+    const int s = max(e, 1) - 110;
+    return s >= 0 ? (unsigned long long)m << s : (s > -32 ? (unsigned long long)(m >> -s) : 0ull);
+}
+
+// Shared-memory staging of a group of chunks: kSpecGroup chunks of the first row, then of the
+// second, filled by bulk copies that complete on `bar` (phase parity `phase`, per thread).
+struct DrawStage {
+    float* buf;
+    uint32_t bar;
+    uint32_t phase;
+};
 
 struct DrawSmem {
     unsigned long long red[kSpecThreads / 32][kSpecOwn];  // per-warp sums of this CTA's chunks
@@ -284,27 +305,75 @@ __device__ __forceinline__ float4 draw_weights4(const float* a, const float* b, 
     return w;
 }
 
+// The four weights (a - b)+ (or a) of entries v0 .. v0 + 3 of group chunk q from the staging
+// buffer (0 past the vocabulary, where the buffer holds stale values).
+__device__ __forceinline__ float4 staged_weights4(const float* buf, int q, bool has_b, int v0, int vocab) {
+    const float4 x = *reinterpret_cast<const float4*>(buf + q * kSpecChunk + 4 * (threadIdx.x & (kSpecThreads - 1)));
+    float4 w = x;
+    if (has_b) {
+        const float4 y = *reinterpret_cast<const float4*>(buf + (kSpecGroup + q) * kSpecChunk + 4 * (threadIdx.x & (kSpecThreads - 1)));
+        w = make_float4(x.x - y.x, x.y - y.y, x.z - y.z, x.w - y.w);
+    }
+    w.x = (v0 < vocab && w.x > 0.f) ? w.x : 0.f;
+    w.y = (v0 + 1 < vocab && w.y > 0.f) ? w.y : 0.f;
+    w.z = (v0 + 2 < vocab && w.z > 0.f) ? w.z : 0.f;
+    w.w = (v0 + 3 < vocab && w.w > 0.f) ? w.w : 0.f;
+    return w;
+}
+
 // Inverse-CDF draw with uniform u over weights (a - b)+ (or a), `round` (0 or 1) naming the
 // draw's slot of chunk totals: the smallest v whose prefix sum of floor(w * 2^40) exceeds
 // floor(floor(u * 2^24) * total / 2^24).  Returns the token (-1 when all weights are 0) in
 // the CTA that owns the threshold's chunk and -2 in the others.  Every thread of every CTA of
 // the cluster must call it.
-__device__ int cluster_draw(const float* a, const float* b, int vocab, float u, int round, DrawSmem& sm) {
+__device__ int cluster_draw(const float* a, const float* b, int vocab, float u, int round, DrawSmem& sm,
+                            DrawStage& st) {
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const uint32_t rank = cluster_rank();
     const int chunks = (vocab + kSpecChunk - 1) / kSpecChunk;
     const int own = chunks > (int)rank ? (chunks - 1 - (int)rank) / kSpecCluster + 1 : 0;
     const bool vec = ((reinterpret_cast<uintptr_t>(a) | (b ? reinterpret_cast<uintptr_t>(b) : 0)) & 15) == 0;
-    // Pass 1: this CTA's chunks, the loads of kSpecGroup chunks in flight together.  The last
-    // group's weights stay in registers for pass 2.
+    // Rows 16-byte aligned with whole 16-byte chunks: each group of chunks is staged in shared
+    // memory by bulk copies (one thread issues them, the bytes complete the barrier), so the
+    // whole group is requested at once without a per-thread limit on loads in flight.
+    const bool bulk = vec && (vocab & 3) == 0;
+    // Pass 1: this CTA's chunks, kSpecGroup chunks in flight together.  The last group's
+    // weights stay in registers for pass 2.
     float4 w[kSpecGroup];
     int g_last = 0;
     for (int g0 = 0; g0 < own; g0 += kSpecGroup) {
         g_last = g0;
+        if (bulk) {
+            __syncthreads();  // every thread is done with the buffer's previous contents
+            if (t == 0) {
+                fence_proxy_async_smem();
+                const int ng = min(kSpecGroup, own - g0);
+                uint32_t bytes = 0;
+                for (int q = 0; q < ng; ++q) {
+                    const int j = (g0 + q) * kSpecCluster + (int)rank;
+                    bytes += 4u * (uint32_t)min(kSpecChunk, vocab - j * kSpecChunk) * (b ? 2u : 1u);
+                }
+                mbar_arrive_expect_tx(st.bar, bytes);
+                const uint64_t pol = l2_policy_evict_first();
+                for (int q = 0; q < ng; ++q) {
+                    const int j = (g0 + q) * kSpecCluster + (int)rank;
+                    const uint32_t nb = 4u * (uint32_t)min(kSpecChunk, vocab - j * kSpecChunk);
+                    bulk_g2s(smem_addr(st.buf + q * kSpecChunk), a + (long long)j * kSpecChunk, nb, st.bar, pol);
+                    if (b)
+                        bulk_g2s(smem_addr(st.buf + (kSpecGroup + q) * kSpecChunk), b + (long long)j * kSpecChunk, nb,
+                                 st.bar, pol);
+                }
+            }
+            mbar_wait(st.bar, st.phase, &g_pa_error, nullptr);
+            st.phase ^= 1u;
+        }
 #pragma unroll
-        for (int q = 0; q < kSpecGroup; ++q)
-            w[q] = g0 + q < own ? draw_weights4(a, b, ((g0 + q) * kSpecCluster + (int)rank) * kSpecChunk + 4 * t, vocab, vec)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < kSpecGroup; ++q) {
+            const int v0 = ((g0 + q) * kSpecCluster + (int)rank) * kSpecChunk + 4 * t;
+            w[q] = g0 + q >= own ? make_float4(0.f, 0.f, 0.f, 0.f)
+                   : bulk        ? staged_weights4(st.buf, q, b != nullptr, v0, vocab)
+                                 : draw_weights4(a, b, v0, vocab, vec);
+        }
 #pragma unroll
         for (int q = 0; q < kSpecGroup; ++q) {
             unsigned long long s = fixed40(w[q].x) + fixed40(w[q].y) + fixed40(w[q].z) + fixed40(w[q].w);
@@ -318,7 +387,8 @@ __device__ int cluster_draw(const float* a, const float* b, int vocab, float u, 
     for (int jl = warp; jl < own; jl += kSpecThreads / 32) {
         unsigned long long s = lane < kSpecThreads / 32 ? sm.red[lane][jl] : 0ull;
 #pragma unroll
-        for (int o = 4; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        for (int o = kSpecThreads / 64; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        s = __shfl_sync(0xffffffffu, s, 0);
         if (lane < kSpecCluster) {
             const int j = jl * kSpecCluster + (int)rank;
             st_cluster_u64(smem_addr(&sm.tot[round][j]), lane, s);
@@ -417,8 +487,10 @@ __device__ int cluster_draw(const float* a, const float* b, int vocab, float u, 
 }
 
 // One cluster of kSpecCluster CTAs per sequence (grid: num_seqs * kSpecCluster).
-__global__ void __launch_bounds__(kSpecThreads, 2) spec_verify_kernel(const SpecParams p) {
+__global__ void __launch_bounds__(kSpecThreads, kSpecCluster / 2) spec_verify_kernel(const SpecParams p) {
     griddep_launch_dependents();
+    extern __shared__ __align__(128) float spec_stage[];  // kSpecStageBytes
+    __shared__ __align__(8) unsigned long long s_bar;
     __shared__ DrawSmem sm;
     __shared__ int s_pos;
     __shared__ int s_ok[64];
@@ -431,6 +503,11 @@ __global__ void __launch_bounds__(kSpecThreads, 2) spec_verify_kernel(const Spec
     // The uniforms are loaded up front, beside the draft tokens: on cold data every dependent
     // load is a DRAM round trip, and only the probability lookups depend on the tokens.
     const float u = __ldg(p.u_sample + n);
+    DrawStage st{spec_stage, smem_addr(&s_bar), 0u};
+    if (threadIdx.x == 0) {
+        mbar_init(st.bar, 1);
+        fence_barrier_init();
+    }
     // Every draft position's accept decision in parallel (thread i), then the left-to-right
     // scan for the first rejection on the flags.  Every CTA of the cluster takes the same
     // decisions from the same values.
@@ -456,9 +533,9 @@ __global__ void __launch_bounds__(kSpecThreads, 2) spec_verify_kernel(const Spec
     }
     __syncthreads();
     const int i = s_pos;
-    int tok = cluster_draw(pl + i * V, i < p.k ? pd + i * V : nullptr, p.vocab, u, 0, sm);
+    int tok = cluster_draw(pl + i * V, i < p.k ? pd + i * V : nullptr, p.vocab, u, 0, sm, st);
     // An all-zero residual: the draw falls back to p_large[i] (every CTA takes this branch).
-    if (tok == -1 && i < p.k) tok = cluster_draw(pl + i * V, nullptr, p.vocab, u, 1, sm);
+    if (tok == -1 && i < p.k) tok = cluster_draw(pl + i * V, nullptr, p.vocab, u, 1, sm, st);
     // The CTA that drew the token (rank 0 if nothing was drawable) writes the outputs.
     if (threadIdx.x == 0 && (tok != -2) && (tok != -1 || cluster_rank() == 0)) {
         for (int jj = 0; jj < i; ++jj) out[jj] = s_tokv[jj];
@@ -2051,7 +2128,8 @@ int launch_spec_verify(int32_t* num_accepted, int32_t* out_tokens, const float* 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)num_seqs * kSpecCluster);
     cfg.blockDim = dim3(kSpecThreads);
-    cfg.dynamicSmemBytes = 0;
+    if (int st = ensure_dynamic_smem(reinterpret_cast<const void*>(spec_verify_kernel), kSpecStageBytes)) return st;
+    cfg.dynamicSmemBytes = kSpecStageBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
