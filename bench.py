@@ -578,7 +578,15 @@ def run_ours(args, rank, world, local):
     # tcgen05 prefill kernel, everything else on the split-K decode kernel.
     tc_path = not kv8 and not groups and (args.math == "tcgen05" or
                                           (args.math == "auto" and (w.num_heads // w.num_kv_heads) * w.q_len >= 128))
+    # A shared-prefix call with >= 16 query rows per kv head runs wholly on tcgen05: after the
+    # order kernel (marks 0-1), the suffix kernel (1-2) then the prefix kernel (2-3), which merges
+    # both pieces.
+    tc_shared = bool(groups) and not kv8 and (w.num_heads // w.num_kv_heads) * w.q_len >= 16
     kernel_name = ("prefill_tc_kernel (tcgen05, no split)" if tc_path and not groups else
+                   "suffix_tc_kernel + prefix_tc_kernel (tcgen05: each sequence's positions after its shared "
+                   "prefix, longest first, then each prefix once per kv head for the group's rows, merging both "
+                   "pieces)"
+                   if tc_shared else
                    "prefix_tc_kernel + decode_kernel + merge_kernel (shared prefix on tcgen05, the rest split-K, "
                    "log-sum-exp merge)" if groups else
                    "decode_kernel + merge_kernel (split-K partition pass and log-sum-exp merge)")
@@ -614,7 +622,12 @@ def run_ours(args, rank, world, local):
                       "traffic": traffic, "tflops": flops / (attn_ms * 1e-3) / 1e12,
                       "partition_kernel": {"ms": kern_ms, "achieved": achieved_k2, "frac": achieved_k2 / peak,
                                            "traffic": t["partition"] if t else None},
-                      "merge_kernel_ms_apart": merge_ms, "plan_kernel_ms_apart": plan_ms}),
+                      "merge_kernel_ms_apart": merge_ms, "plan_kernel_ms_apart": plan_ms,
+                      "part_kernels": ({"partition_kernel": "suffix_tc_kernel", "merge_kernel_ms_apart":
+                                        "prefix_tc_kernel", "plan_kernel_ms_apart": "suffix_order_kernel"}
+                                       if tc_shared else
+                                       {"partition_kernel": "decode_kernel", "merge_kernel_ms_apart":
+                                        "merge_kernel", "plan_kernel_ms_apart": "plan_kernel"})}),
         "gpu_launches": launches_per_step * args.steps,
         "roofline_steps": attn_n,
         "clocks": clocks.summary(),

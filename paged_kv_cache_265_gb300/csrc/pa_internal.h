@@ -22,7 +22,7 @@ namespace pa {
 // piece when `prefix` (which also always reserves the partials: a grouped sequence merges its
 // prefix piece with the rest even when the rest is one partition).
 struct WsLayout {
-    size_t header, part_start, units, pml, pacc, total;
+    size_t header, part_start, units, pml, pacc, order, total;
     int pmax;
 };
 
@@ -50,6 +50,9 @@ inline WsLayout ws_layout(int num_seqs, int q_len, int num_heads, int head_dim, 
         w.pacc = off;
         off += align256(4 * slots * (size_t)q_len * (size_t)num_heads * (size_t)head_dim);
     }
+    // Shared-prefix calls on tcgen05: the order of the suffix units (at most one per query row)
+    w.order = off;
+    if (prefix) off += align256(4 * n * (size_t)q_len * (size_t)num_heads);
     w.total = off;
     w.pmax = pmax;
     return w;
@@ -129,10 +132,12 @@ bool use_prefill_tc(const DecodeArgs& a);
 int launch_prefix_tc(const DecodeArgs& a, const int* part_start, const float2* pml, const float* pacc,
                      cudaStream_t stream, int* launches);
 // A shared-prefix call with at least kTcSuffixMinRows query rows per kv head, entirely on
-// tcgen05 (pa_prefill.cu): the suffix kernel (positions after each sequence's prefix; suffix
-// pieces to partial slot i) then the prefix kernel (merges them and writes the output).
+// tcgen05 (pa_prefill.cu): a one-CTA kernel orders the suffix units longest first (into
+// `order`), the suffix kernel (positions after each sequence's prefix; suffix pieces to partial
+// slot i) takes them in that order, then the prefix kernel merges them and writes the output.
 constexpr int kTcSuffixMinRows = 16;
-int launch_shared_prefix_tc(const DecodeArgs& a, float2* pml, float* pacc, cudaStream_t stream, int* launches);
+int launch_shared_prefix_tc(const DecodeArgs& a, float2* pml, float* pacc, int* order, cudaStream_t stream,
+                            int* launches);
 
 // Smallest split-K partition the library chooses for a shared-prefix call (the workspace of a
 // call with partition 0 is sized for it).

@@ -2163,7 +2163,7 @@ int launch_decode(const DecodeArgs& args, cudaStream_t stream, int* launches, in
                                      args.partition, true);
         uint8_t* ws = static_cast<uint8_t*>(args.workspace);
         return launch_shared_prefix_tc(args, reinterpret_cast<float2*>(ws + w.pml), reinterpret_cast<float*>(ws + w.pacc),
-                                       stream, launches);
+                                       reinterpret_cast<int*>(ws + w.order), stream, launches);
     }
     DecodeArgs a = args;
     if (a.partition_auto) {

@@ -111,6 +111,8 @@ struct PrefillTcParams {
     // Suffix mode: where a sequence with a shared prefix leaves its suffix piece (slot i).
     float2* pml_out;
     float* pacc_out;
+    // Suffix mode: the units, longest first (null: index order).
+    const int* order;
 };
 
 template <int D>
@@ -223,6 +225,20 @@ __device__ __forceinline__ TcTile tc_tile(const PrefillTcParams& p, const Prefix
     return w;
 }
 
+// The k-th unit this CTA takes, or -1 when it has no more.  With an order (suffix mode, units
+// sorted longest first) the CTAs take its positions back and forth, CTA b positions b,
+// 2G - 1 - b, 2G + b, ... of G CTAs, which balances their sums of unit lengths; otherwise
+// units b, b + G, ... (one unit per CTA in chunk mode, where G is the unit count).
+__device__ __forceinline__ int tc_unit(const PrefillTcParams& p, int num_units, int k) {
+    const int G = (int)gridDim.x, b = (int)blockIdx.x;
+    if (p.order) {
+        const long long pos = (long long)k * G + ((k & 1) ? G - 1 - b : b);
+        return pos < num_units ? __ldg(p.order + pos) : -1;
+    }
+    const long long u = (long long)k * G + b;
+    return u < num_units ? (int)u : -1;
+}
+
 template <typename T, int D, int kMode>
 __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const PrefixGroups* g) {
     constexpr bool kPrefix = kMode == kModePrefix;
@@ -272,7 +288,7 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
     // waits for the plan kernel's partial slots.
     if constexpr (!kPrefix) griddep_wait();
 
-    // The CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ... (one CTA per SM).  Every role
+    // The CTA takes the units tc_unit() names (one CTA per SM).  Every role
     // walks the same units and counts their K/V tiles in one running index gt, so stage, S
     // buffer and barrier phases carry on from one unit to the next; per-unit barriers (qready,
     // lready) count valid units (vu).  Tensor memory and the barriers are set up once.
@@ -280,14 +296,16 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
     // Chunk mode launches one CTA per unit: its running indices are the compile-time 0 of a
     // single unit (the loop below runs once), and the loop costs it nothing.
     constexpr bool kLoop = kMode != kModeChunk;
-    const int u_step = kLoop ? (int)gridDim.x : num_units;
+    const int k_end = kLoop ? 0x7fffffff : 1;
 
     if (warp == 8) {
         // ===================== TMA producer =====================
         int armed[kTcStages] = {0, 0, 0};
         int gt_run = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < num_units; u += u_step) {
+        for (int k = 0; ok && k < k_end; ++k) {
+        const int u = tc_unit(p, num_units, k);
+        if (u < 0) break;
         const TcTile tile = tc_tile<kMode>(p, g, u);
         if (!tile.valid) {
             if (!kPrefix && lane == 0) atomicOr(err, PA_DEVERR_CONTEXT);  // rows left untouched
@@ -361,7 +379,9 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
             const uint64_t vdesc0 = tc::smem_desc_sw128(st_s + Lay::kKBytes, kRegion, 1024);
             bool ok = true;
             int gt_run = 0, vu_run = 0;
-            for (int u = blockIdx.x; ok && u < num_units; u += u_step) {
+            for (int k = 0; ok && k < k_end; ++k) {
+            const int u = tc_unit(p, num_units, k);
+            if (u < 0) break;
             const TcTile tile = tc_tile<kMode>(p, g, u);
             if (!tile.valid) continue;
             const int nblk = tile.nblk;
@@ -437,7 +457,9 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
         const float c2 = p.scale_log2;
         bool ok = true;
         int gt_run = 0, vu_run = 0;
-        for (int u = blockIdx.x; ok && u < num_units; u += u_step) {
+        for (int k = 0; ok && k < k_end; ++k) {
+        const int u = tc_unit(p, num_units, k);
+        if (u < 0) break;
         const TcTile tile = tc_tile<kMode>(p, g, u);
         if (!tile.valid) continue;
         const int gt = kLoop ? gt_run : 0, vu = kLoop ? vu_run : 0;
@@ -759,6 +781,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_attention<T, D, kModeSuffix>(p, &g);
 }
 
+// Suffix mode: the units ordered by their count of K/V tiles, longest first (a counting sort
+// in one CTA; units of equal length in any order, which changes no result).  Bucket 0 holds
+// the longest, 255 tiles or more, and invalid units count as empty.
+constexpr int kOrderBuckets = 256;
+
+__global__ void __launch_bounds__(1024) suffix_order_kernel(const __grid_constant__ PrefillTcParams p,
+                                                            const __grid_constant__ PrefixGroups g) {
+    __shared__ int start[kOrderBuckets];
+    griddep_wait();  // the suffix kernel waits for this one, and so for every earlier kernel
+    griddep_launch_dependents();
+    for (int b = threadIdx.x; b < kOrderBuckets; b += blockDim.x) start[b] = 0;
+    __syncthreads();
+    auto bucket = [&](int idx) {
+        const TcTile t = tc_tile<kModeSuffix>(p, &g, idx);
+        const int tiles = t.valid ? (t.nblk + kTcBlocks - 1) / kTcBlocks : 0;
+        return kOrderBuckets - 1 - min(tiles, kOrderBuckets - 1);
+    };
+    for (int idx = threadIdx.x; idx < p.num_units; idx += blockDim.x) atomicAdd(&start[bucket(idx)], 1);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int b = 0; b < kOrderBuckets; ++b) {
+            const int c = start[b];
+            start[b] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    int* order = const_cast<int*>(p.order);
+    for (int idx = threadIdx.x; idx < p.num_units; idx += blockDim.x) order[atomicAdd(&start[bucket(idx)], 1)] = idx;
+}
+
 // Parameters shared by the chunk and prefix launches.
 template <int D>
 int tc_params(const DecodeArgs& a, PrefillTcParams& p) {
@@ -788,6 +842,7 @@ int tc_params(const DecodeArgs& a, PrefillTcParams& p) {
     p.pacc = nullptr;
     p.pml_out = nullptr;
     p.pacc_out = nullptr;
+    p.order = nullptr;
     return PA_OK;
 }
 
@@ -823,11 +878,13 @@ int launch_prefix_tc_typed(const DecodeArgs& a, const int* part_start, const flo
 // get their output there), then the prefix kernel, which merges each grouped row's suffix piece
 // (partial slot i) and writes the output.
 template <typename T, int D>
-int launch_shared_prefix_tc_typed(const DecodeArgs& a, float2* pml, float* pacc, cudaStream_t stream, int* launches) {
+int launch_shared_prefix_tc_typed(const DecodeArgs& a, float2* pml, float* pacc, int* order, cudaStream_t stream,
+                                  int* launches) {
     PrefillTcParams p;
     if (int st = tc_params<D>(a, p)) return st;
     p.pml_out = pml;
     p.pacc_out = pacc;
+    p.order = order;
     // Suffixes are a few tiles each: persistent CTAs (one per SM) save each unit the CTA's
     // set-up (barriers, tensor memory, first copies).
     int sms = 0;
@@ -838,6 +895,10 @@ int launch_shared_prefix_tc_typed(const DecodeArgs& a, float2* pml, float* pacc,
     if (int st = ensure_dynamic_smem(reinterpret_cast<const void*>(sfn), smem)) return st;
     const int pc = profile_call_begin();
     profile_mark(pc, 0, stream);
+    // The persistent CTAs take the units longest first, back and forth across the CTAs.
+    if (launch_pdl(suffix_order_kernel, dim3(1), dim3(1024), 0, stream, p, *a.groups) != cudaSuccess)
+        return PA_ERR_CUDA;
+    *launches += 1;
     profile_mark(pc, 1, stream);
     if (launch_pdl(sfn, dim3(grid), dim3(kTcThreads), (size_t)smem, stream, p, *a.groups) != cudaSuccess)
         return PA_ERR_CUDA;
@@ -872,14 +933,17 @@ int launch_prefix_tc_typed(const DecodeArgs& a, const int* part_start, const flo
 
 }  // namespace
 
-int launch_shared_prefix_tc(const DecodeArgs& a, float2* pml, float* pacc, cudaStream_t stream, int* launches) {
+int launch_shared_prefix_tc(const DecodeArgs& a, float2* pml, float* pacc, int* order, cudaStream_t stream,
+                            int* launches) {
     if (a.fp8 || !a.groups) return PA_ERR_UNSUPPORTED;
     if (a.dtype == PA_BF16) {
-        if (a.head_dim == 128) return launch_shared_prefix_tc_typed<__nv_bfloat16, 128>(a, pml, pacc, stream, launches);
-        if (a.head_dim == 64) return launch_shared_prefix_tc_typed<__nv_bfloat16, 64>(a, pml, pacc, stream, launches);
+        if (a.head_dim == 128)
+            return launch_shared_prefix_tc_typed<__nv_bfloat16, 128>(a, pml, pacc, order, stream, launches);
+        if (a.head_dim == 64)
+            return launch_shared_prefix_tc_typed<__nv_bfloat16, 64>(a, pml, pacc, order, stream, launches);
     } else {
-        if (a.head_dim == 128) return launch_shared_prefix_tc_typed<__half, 128>(a, pml, pacc, stream, launches);
-        if (a.head_dim == 64) return launch_shared_prefix_tc_typed<__half, 64>(a, pml, pacc, stream, launches);
+        if (a.head_dim == 128) return launch_shared_prefix_tc_typed<__half, 128>(a, pml, pacc, order, stream, launches);
+        if (a.head_dim == 64) return launch_shared_prefix_tc_typed<__half, 64>(a, pml, pacc, order, stream, launches);
     }
     return PA_ERR_UNSUPPORTED;
 }

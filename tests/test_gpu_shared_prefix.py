@@ -49,9 +49,10 @@ def test_shared_prefix_workload(partition):
     """The named shared-prefix workload: 64 sequences, one 1024-token prefix, q = 5."""
     w = W.shared_prefix_verify()
     step, got = run_prefix(w, [0, w.num_seqs], [w.shared_prefix_blocks * 16], partition)
-    # 20 query rows per kv head: the suffix kernel and the prefix kernel, both on tcgen05 (the
-    # prefix kernel merges every grouped sequence's pieces)
-    assert pa.last_launch_count() == 2
+    # 20 query rows per kv head: the one-CTA kernel that orders the suffix units longest first,
+    # then the suffix kernel and the prefix kernel, both on tcgen05 (the prefix kernel merges
+    # every grouped sequence's pieces)
+    assert pa.last_launch_count() == 3
     _, _, ref = G.oracle_step(w)
     G.compare(got, ref, w.dtype, f"shared prefix, partition {partition}")
     assert G.ulps_from_rounded_oracle(got, ref, w.dtype) <= 1
