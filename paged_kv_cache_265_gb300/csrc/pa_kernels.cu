@@ -253,8 +253,6 @@ struct DrawStage {
 struct DrawSmem {
     unsigned long long red[kSpecThreads / 32][kSpecOwn];  // per-warp sums of this CTA's chunks
     unsigned long long tot[2][kSpecMaxChunks];            // totals of every chunk, per draw
-    unsigned long long scan[kSpecThreads / 32];
-    int tok;
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -323,9 +321,9 @@ __device__ __forceinline__ float4 staged_weights4(const float* buf, int q, bool 
 
 // Inverse-CDF draw with uniform u over weights (a - b)+ (or a), `round` (0 or 1) naming the
 // draw's slot of chunk totals: the smallest v whose prefix sum of floor(w * 2^40) exceeds
-// floor(floor(u * 2^24) * total / 2^24).  Returns the token (-1 when all weights are 0) in
-// the CTA that owns the threshold's chunk and -2 in the others.  Every thread of every CTA of
-// the cluster must call it.
+// floor(floor(u * 2^24) * total / 2^24).  Returns the token in the one thread of the cluster
+// that found it, -1 in every thread when all weights are 0, and -2 in the others.  Every
+// thread of every CTA of the cluster must call it.
 __device__ int cluster_draw(const float* a, const float* b, int vocab, float u, int round, DrawSmem& sm,
                             DrawStage& st) {
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -395,95 +393,81 @@ __device__ int cluster_draw(const float* a, const float* b, int vocab, float u, 
         }
     }
     cluster_sync();
-    // Every CTA: prefix over all chunk totals (lane l holds chunks 8l .. 8l + 7), the threshold
-    // and the first chunk whose inclusive prefix exceeds it.
-    int chunk = -1;
-    unsigned long long base = 0, thresh = 0;
-    if (warp == 0) {
-        unsigned long long c[kSpecMaxChunks / 32];
-        unsigned long long mine = 0;
+    // Every warp of every CTA: prefix over all chunk totals (lane l holds chunks l * E .. + E - 1),
+    // the threshold and the first chunk whose inclusive prefix exceeds it.  Every warp reaches
+    // the same values from the same totals, so no barrier is needed to share them.
+    constexpr int E = kSpecMaxChunks / 32;
+    unsigned long long c[E];
+    unsigned long long mine = 0;
 #pragma unroll
-        for (int e = 0; e < kSpecMaxChunks / 32; ++e) {
-            const int j = lane * (kSpecMaxChunks / 32) + e;
-            c[e] = j < chunks ? sm.tot[round][j] : 0ull;
-            mine += c[e];
-        }
-        unsigned long long incl = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
-        if (total) {
-            const unsigned long long u24 = __float2ull_rz(u * 16777216.0f);
-            thresh = (__umul64hi(u24, total) << 40) | ((u24 * total) >> 24);
-            // the lane whose range holds the first prefix above the threshold
-            const unsigned m = __ballot_sync(0xffffffffu, incl > thresh);
-            const int l = __ffs(m) - 1;  // m != 0: the last lane's prefix is the total > thresh
-            unsigned long long run = __shfl_sync(0xffffffffu, incl - mine, l);
-            int found = -1;
-            unsigned long long found_base = 0;
-            if (lane == l) {
-#pragma unroll
-                for (int e = 0; e < kSpecMaxChunks / 32; ++e) {
-                    if (found < 0 && run + c[e] > thresh) {
-                        found = lane * (kSpecMaxChunks / 32) + e;
-                        found_base = run;
-                    }
-                    run += c[e];
-                }
-            }
-            chunk = __shfl_sync(0xffffffffu, found, l);
-            base = __shfl_sync(0xffffffffu, found_base, l);
-        }
-        if (lane == 0) {
-            sm.tok = chunk < 0 ? -1 : -2;
-            sm.scan[0] = base;
-            sm.scan[1] = thresh;
-            sm.scan[2] = (unsigned long long)(long long)chunk;
-        }
+    for (int e = 0; e < E; ++e) {
+        const int j = lane * E + e;
+        c[e] = j < chunks ? sm.tot[round][j] : 0ull;
+        mine += c[e];
     }
-    __syncthreads();
-    chunk = (int)(long long)sm.scan[2];
-    if (chunk < 0) return -1;                               // every weight is 0 (all CTAs agree)
-    if (chunk % kSpecCluster != (int)rank) return -2;       // another CTA owns the threshold's chunk
-    base = sm.scan[0];
-    thresh = sm.scan[1];
-    __syncthreads();  // scan[] is reused below
-    // Pass 2, in the owner: the chunk's entries in order (each thread's four, then a block scan),
-    // from the registers of pass 1 when the chunk was in its last group.
-    const int v0 = chunk * kSpecChunk + 4 * t;
-    const int jl = chunk / kSpecCluster - g_last;
-    float4 wc;
-    if (jl >= 0 && jl < kSpecGroup) {
-        wc = w[0];
-#pragma unroll
-        for (int q = 1; q < kSpecGroup; ++q)
-            if (q == jl) wc = w[q];
-    } else {
-        wc = draw_weights4(a, b, v0, vocab, vec);
-    }
-    const unsigned long long x[4] = {fixed40(wc.x), fixed40(wc.y), fixed40(wc.z), fixed40(wc.w)};
-    const unsigned long long mine = x[0] + x[1] + x[2] + x[3];
     unsigned long long incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
     }
-    if (lane == 31) sm.scan[warp] = incl;
-    __syncthreads();
-    unsigned long long before = base + (incl - mine);
-    for (int w2 = 0; w2 < warp; ++w2) before += sm.scan[w2];
+    const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total == 0) return -1;  // every weight is 0 (every warp of every CTA agrees)
+    const unsigned long long u24 = __float2ull_rz(u * 16777216.0f);
+    const unsigned long long thresh = (__umul64hi(u24, total) << 40) | ((u24 * total) >> 24);
+    // the lane whose range holds the first prefix above the threshold (the last lane's prefix is
+    // the total, which exceeds it)
+    const int l = __ffs(__ballot_sync(0xffffffffu, incl > thresh)) - 1;
+    int found = -1;
+    unsigned long long found_base = 0;
+    if (lane == l) {
+        unsigned long long run = incl - mine;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        if (before <= thresh && before + x[c] > thresh && v0 + c < vocab) sm.tok = v0 + c;
-        before += x[c];
+        for (int e = 0; e < E; ++e) {
+            if (found < 0 && run + c[e] > thresh) {
+                found = lane * E + e;
+                found_base = run;
+            }
+            run += c[e];
+        }
     }
-    __syncthreads();
-    const int tok = sm.tok;
-    return tok < 0 ? vocab - 1 : tok;
+    const int chunk = __shfl_sync(0xffffffffu, found, l);
+    if (chunk % kSpecCluster != (int)rank) return -2;  // another CTA owns the threshold's chunk
+    // In the owner: the warp whose 4 * 32 entries of the chunk hold the threshold, from the
+    // per-warp sums of pass 1.
+    const int jl = chunk / kSpecCluster;
+    unsigned long long before = __shfl_sync(0xffffffffu, found_base, l);
+    for (int w2 = 0; w2 < warp; ++w2) before += sm.red[w2][jl];
+    if (!(before <= thresh && thresh < before + sm.red[warp][jl])) return -2;
+    // Pass 2, in that warp: its entries in order (each lane's four, then a warp scan), from the
+    // registers of pass 1 when the chunk was in its last group.
+    const int v0 = chunk * kSpecChunk + 4 * t;
+    const int jg = jl - g_last;
+    float4 wc;
+    if (jg >= 0 && jg < kSpecGroup) {
+        wc = w[0];
+#pragma unroll
+        for (int q = 1; q < kSpecGroup; ++q)
+            if (q == jg) wc = w[q];
+    } else {
+        wc = draw_weights4(a, b, v0, vocab, vec);
+    }
+    const unsigned long long x[4] = {fixed40(wc.x), fixed40(wc.y), fixed40(wc.z), fixed40(wc.w)};
+    const unsigned long long mine2 = x[0] + x[1] + x[2] + x[3];
+    unsigned long long incl2 = mine2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl2, o);
+        if (lane >= o) incl2 += y;
+    }
+    unsigned long long run = before + (incl2 - mine2);
+    int tok = -2;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (run <= thresh && run + x[q] > thresh && v0 + q < vocab) tok = v0 + q;
+        run += x[q];
+    }
+    return tok;
 }
 
 // One cluster of kSpecCluster CTAs per sequence (grid: num_seqs * kSpecCluster).
@@ -536,8 +520,8 @@ __global__ void __launch_bounds__(kSpecThreads, kSpecCluster / 2) spec_verify_ke
     int tok = cluster_draw(pl + i * V, i < p.k ? pd + i * V : nullptr, p.vocab, u, 0, sm, st);
     // An all-zero residual: the draw falls back to p_large[i] (every CTA takes this branch).
     if (tok == -1 && i < p.k) tok = cluster_draw(pl + i * V, nullptr, p.vocab, u, 1, sm, st);
-    // The CTA that drew the token (rank 0 if nothing was drawable) writes the outputs.
-    if (threadIdx.x == 0 && (tok != -2) && (tok != -1 || cluster_rank() == 0)) {
+    // The thread that drew the token (thread 0 of rank 0 if nothing was drawable) writes the outputs.
+    if (tok >= 0 || (tok == -1 && threadIdx.x == 0 && cluster_rank() == 0)) {
         for (int jj = 0; jj < i; ++jj) out[jj] = s_tokv[jj];
         out[i] = tok;
         for (int jj = i + 1; jj <= p.k; ++jj) out[jj] = -1;
