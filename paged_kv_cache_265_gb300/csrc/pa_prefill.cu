@@ -789,7 +789,9 @@ constexpr int kOrderBuckets = 256;
 __global__ void __launch_bounds__(1024) suffix_order_kernel(const __grid_constant__ PrefillTcParams p,
                                                             const __grid_constant__ PrefixGroups g) {
     __shared__ int start[kOrderBuckets];
-    griddep_wait();  // the suffix kernel waits for this one, and so for every earlier kernel
+    // Every earlier kernel first: the previous call's suffix kernel may still be reading the
+    // order array, and the suffix kernel, which waits for this one, relies on the append.
+    griddep_wait();
     griddep_launch_dependents();
     for (int b = threadIdx.x; b < kOrderBuckets; b += blockDim.x) start[b] = 0;
     __syncthreads();
@@ -800,12 +802,26 @@ __global__ void __launch_bounds__(1024) suffix_order_kernel(const __grid_constan
     };
     for (int idx = threadIdx.x; idx < p.num_units; idx += blockDim.x) atomicAdd(&start[bucket(idx)], 1);
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int b = 0; b < kOrderBuckets; ++b) {
-            const int c = start[b];
-            start[b] = run;
-            run += c;
+    if (threadIdx.x < 32) {  // exclusive scan of the bucket counts: lane l holds buckets 8l .. 8l + 7
+        constexpr int E = kOrderBuckets / 32;
+        const int lane = threadIdx.x;
+        int c[E], mine = 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            c[e] = start[lane * E + e];
+            mine += c[e];
+        }
+        int incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int run = incl - mine;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            start[lane * E + e] = run;
+            run += c[e];
         }
     }
     __syncthreads();
