@@ -141,19 +141,30 @@ class ClockSampler:
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.out = None
         self.first = ""
+        self.t0 = self.t1 = None  # host wall clock at the timed region's start and end
+
+    def region_start(self):
+        import datetime
+
+        self.t0 = datetime.datetime.now()
+
+    def region_end(self):
+        import datetime
+
+        self.t1 = datetime.datetime.now()
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
         self.first = ""
@@ -182,8 +193,10 @@ class ClockSampler:
         self.out = (self.first or "") + (self.out or "")
         if not self.out:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        import datetime
+
         rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 8]
-        sm, smax, reasons = [], [], set()
+        sm, smax, inside, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             try:
@@ -194,9 +207,22 @@ class ClockSampler:
             for n, v in zip(names, r[5:9]):
                 if v.strip().lower() == "active":
                     reasons.add(n)
+            ts = None
+            if len(r) > 9:
+                try:
+                    ts = datetime.datetime.strptime(r[9].strip(), "%Y/%m/%d %H:%M:%S.%f")
+                except ValueError:
+                    ts = None
+            inside.append(ts is not None and self.t0 is not None and self.t1 is not None and
+                          self.t0 <= ts <= self.t1)
         busy = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
-        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        # Prefer the samples taken inside the timed region when there are any; the reasons are
+        # collected over every sample, just before and after included.
+        busy_in = [s for s, i in zip(sm, inside) if i and smax and s > 0.5 * max(smax)]
+        use = busy_in or busy
+        return {"sm_mhz": statistics.median(use) if use else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "samples_in_region": sum(inside) if self.t0 is not None else None}
 
 
 def dist_setup(args):
@@ -461,6 +487,7 @@ def run_ours(args, rank, world, local):
     with ClockSampler(local) as clocks:
         barrier(world)
         torch.cuda.synchronize(dev)
+        clocks.region_start()
         start.record(stream)
         for _ in range(args.steps):
             ev = flushed()
@@ -469,6 +496,7 @@ def run_ours(args, rank, world, local):
             step()
         stop.record(stream)
         torch.cuda.synchronize(dev)
+        clocks.region_end()
         barrier(world)
     total_ms = start.elapsed_time(stop)
     flush_ms = sum(a.elapsed_time(b) for a, b in flush_events)

@@ -40,6 +40,22 @@ def test_clock_summary_reports_slowdowns_and_missing_samples():
     assert s["samples"] == 0
 
 
+def test_clock_summary_counts_the_samples_inside_the_timed_region():
+    import datetime
+
+    cs = bench.ClockSampler(0)
+    cs.t0 = datetime.datetime(2026, 1, 2, 3, 4, 5, 100000)
+    cs.t1 = datetime.datetime(2026, 1, 2, 3, 4, 5, 400000)
+    before = _row(1500, 2070, 300.0).rstrip("\n") + ", 2026/01/02 03:04:05.050\n"
+    inside = [_row(2070, 2070, 900.0).rstrip("\n") + f", 2026/01/02 03:04:05.{ms:03d}\n" for ms in (150, 250, 350)]
+    after = _row(1900, 2070, 500.0, cap="Active").rstrip("\n") + ", 2026/01/02 03:04:05.450\n"
+    cs.first, cs.out = before, "".join(inside) + after
+    s = cs.summary()
+    assert s["samples"] == 5 and s["samples_in_region"] == 3
+    assert s["sm_mhz"] == 2070.0                       # from the samples inside the region
+    assert s["reasons"] == ["sw_power_cap"]             # reasons from every sample
+
+
 def test_peaks_use_the_measured_file_else_the_fallback(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.peaks() == (6800.0, "fallback")
