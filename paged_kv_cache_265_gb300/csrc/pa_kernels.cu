@@ -68,7 +68,10 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 #define PA_CTAS_PER_SM_NT1 4  // kernels whose warps own 8 query rows
 #endif
 #ifndef PA_CTAS_PER_SM_F8
-#define PA_CTAS_PER_SM_F8 5  // FP8-cache kernels whose warps own 8 query rows (measured best: 4 -> 131.1 us, 5 -> 128.4 us, 6 -> 129.0 us)
+// FP8-cache kernels whose warps own 8 query rows.  Same-box A/B on the GQA batch: 4 CTAs per SM
+// (96 registers, 92 B of spills) 131.8 us, 5 (72 registers, 220 B) 133.0 us; with the query
+// fragments read from shared memory instead (20 B of spills at 4 CTAs) 131.7 / 138.3 us.
+#define PA_CTAS_PER_SM_F8 4
 #endif
 #ifndef PA_CTAS_PER_SM_NT2
 #define PA_CTAS_PER_SM_NT2 2  // kernels whose warps own 16 query rows
