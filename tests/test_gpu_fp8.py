@@ -137,3 +137,45 @@ def test_fp8_bf16_query_at_fp16_edges():
     got, ref = run_fp8(wb)
     assert pa.get_device_error(clear=True) == 0
     G.compare(got, ref, w.dtype, "fp8 query rows at the fp16 edges")
+
+
+def test_fp8_kernel_wait_runs_out_and_recovers():
+    """The FP8 decode kernel (whose warps release each stage right after loading it) stops on a
+    pipeline wait that runs out (pa_set_wait_limit_ns(1)): the call reports PA_DEVERR_TIMEOUT and
+    nothing else, and the next call with the default limit matches the oracle."""
+    w = W.make_workload("fp8_timeout", [40, 700, 1900, 3000], num_heads=32, num_kv_heads=8, head_dim=128,
+                        q_len=1, num_blocks=400, seed=43)
+    kc, vc = fp8_pools(w)
+    dk, dv = torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
+    pa.reshape_and_cache_fp8(G.to_dev(w.new_key, w.dtype), G.to_dev(w.new_value, w.dtype), dk, dv,
+                             torch.from_numpy(w.slot_mapping).cuda(), K_SCALE, V_SCALE)
+    q = G.to_dev(w.query, w.dtype)
+    out = torch.empty_like(q)
+    ws = pa.alloc_workspace(w.num_seqs, w.q_len, w.num_heads, w.head_dim, w.max_context_len, 0)
+    bt, cl = torch.from_numpy(w.block_tables).cuda(), torch.from_numpy(w.context_lens).cuda()
+
+    def call():
+        pa.decode_attention_fp8kv(out, q, dk, dv, bt, cl, w.scale, w.max_context_len, ws, K_SCALE, V_SCALE)
+        torch.cuda.synchronize()
+
+    torch.cuda.synchronize()
+    pa.get_device_error(clear=True)
+    try:
+        pa.set_wait_limit_ns(1)
+        call()
+        pa.set_wait_limit_ns(0)
+        flags = pa.get_device_error(clear=True)
+        assert flags & pa.PA_DEVERR_TIMEOUT, f"no wait ran out (flags {flags:#x})"
+        assert flags & ~pa.PA_DEVERR_TIMEOUT == 0, f"unexpected flags {flags:#x}"
+        out.fill_(float("nan"))
+        call()
+        got = G.to_bits(out)
+    finally:
+        pa.set_wait_limit_ns(0)
+    assert pa.get_device_error(clear=True) == 0
+    orc = oracle.load()
+    assert orc.reshape_and_cache_fp8(w.new_key, w.new_value, kc, vc, w.slot_mapping, w.dtype, K_SCALE, V_SCALE) == 0
+    ref, bad = orc.decode_attention_fp8(w.query, kc, vc, w.block_tables, w.context_lens, w.scale, w.dtype,
+                                        K_SCALE, V_SCALE)
+    assert bad == 0
+    G.compare(got, ref, w.dtype, "fp8 after a timed-out call")
