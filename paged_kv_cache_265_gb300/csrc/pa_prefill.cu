@@ -138,6 +138,13 @@ __device__ __forceinline__ float hi16(uint32_t v, std::false_type) {
     return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
 }
 
+// max(a, b, c) in one instruction (the softmax's row maxima are most of its non-exponential work).
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Bits of the columns in [lo, hi] that fall in the 32-column word starting at `base`.
 __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base) {
     const int a = max(lo - base, 0), b = min(hi - base, 31);
@@ -560,33 +567,38 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
                 tc::ld_x64(buf + 64 * oh, ov);
                 if (transform) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) {
+                    for (int c = 0; c < 64; c += 2) {
                         const uint32_t w = vm[2 * oh + (c >> 5)];
-                        const float v = __uint_as_float(ov[c]);
-                        mx[c & 7] = fmaxf(mx[c & 7], ((w >> (c & 31)) & 1u) ? (raw ? v : v * c2) : -INFINITY);
+                        const float v0 = __uint_as_float(ov[c]), v1 = __uint_as_float(ov[c + 1]);
+                        const float x0 = ((w >> (c & 31)) & 1u) ? (raw ? v0 : v0 * c2) : -INFINITY;
+                        const float x1 = ((w >> ((c + 1) & 31)) & 1u) ? (raw ? v1 : v1 * c2) : -INFINITY;
+                        mx[(c >> 1) & 7] = fmax3f(mx[(c >> 1) & 7], x0, x1);
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(ov[c]));
+                    for (int c = 0; c < 64; c += 2)
+                        mx[(c >> 1) & 7] = fmax3f(mx[(c >> 1) & 7], __uint_as_float(ov[c]), __uint_as_float(ov[c + 1]));
                 }
             }
             uint32_t sv[64];
             tc::ld_x64(buf + 64 * hf, sv);
             if (transform) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < 64; c += 2) {
                     const uint32_t w = vm[2 * hf + (c >> 5)];
-                    const float v = __uint_as_float(sv[c]);
-                    const float x = ((w >> (c & 31)) & 1u) ? (raw ? v : v * c2) : -INFINITY;
-                    sv[c] = __float_as_uint(x);
-                    mx[c & 7] = fmaxf(mx[c & 7], x);
+                    const float v0 = __uint_as_float(sv[c]), v1 = __uint_as_float(sv[c + 1]);
+                    const float x0 = ((w >> (c & 31)) & 1u) ? (raw ? v0 : v0 * c2) : -INFINITY;
+                    const float x1 = ((w >> ((c + 1) & 31)) & 1u) ? (raw ? v1 : v1 * c2) : -INFINITY;
+                    sv[c] = __float_as_uint(x0);
+                    sv[c + 1] = __float_as_uint(x1);
+                    mx[(c >> 1) & 7] = fmax3f(mx[(c >> 1) & 7], x0, x1);
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sv[c]));
+                for (int c = 0; c < 64; c += 2)
+                    mx[(c >> 1) & 7] = fmax3f(mx[(c >> 1) & 7], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
             }
-            float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            float tmax = fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
             if (raw) tmax *= c2;
             // Both threads of a row see the same maxima, so they take the same decisions.
             float alpha = 1.f;
