@@ -71,6 +71,12 @@ namespace {
 #ifndef PA_TC_SUFFIX_PERSISTENT
 #define PA_TC_SUFFIX_PERSISTENT 1
 #endif
+// Kernel modes whose softmax takes its weights in packed fp32 pairs (bit m: mode m): fewer
+// instructions shorten the chain of the suffix kernel's few-row tiles, while beside eight busy
+// softmax warps (full tiles) the denser arithmetic slows the tensor-core products.
+#ifndef PA_TC_PACKED_MODES
+#define PA_TC_PACKED_MODES 4
+#endif
 
 constexpr int kTcRows = 128;             // query rows per CTA tile (MMA M)
 constexpr int kTcPos = 128;              // positions per K/V tile
@@ -142,6 +148,32 @@ __device__ __forceinline__ float hi16(uint32_t v, std::false_type) {
 __device__ __forceinline__ float fmax3f(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Packed pairs of fp32 (one 64-bit register, two lanes of arithmetic per instruction): each lane
+// rounds as the scalar instruction does.
+__device__ __forceinline__ unsigned long long f2_make(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(unsigned long long v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
 
@@ -608,10 +640,12 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
                 m_run = tmax;
             }
             const float msub = m_run == -INFINITY ? 0.f : m_run;
+            uint32_t ph[32], pl[32];  // P_hi and P_lo of positions 64 hf .., two weights per register
+            float sum;
+            if constexpr (((PA_TC_PACKED_MODES >> kMode) & 1) == 0) {
             float sm[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) sm[u] = 0.f;
-            uint32_t ph[32], pl[32];  // P_hi and P_lo of positions 64 hf .., two weights per register
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 const float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), cs, -msub));
@@ -620,7 +654,31 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
                 pl[c] = Elem<T>::pack(p0 - lo16(ph[c], IsBf16()), p1 - hi16(ph[c], IsBf16()));
                 sm[c & 7] += p0 + p1;
             }
-            const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+            sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+            } else {
+            // Weights two at a time in packed fp32 pairs: one FFMA, one residual subtraction and
+            // one accumulation per pair.
+            const unsigned long long cs2 = f2_make(cs, cs), nm2 = f2_make(-msub, -msub);
+            unsigned long long sm2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                float x0, x1;
+                f2_split(f2_fma(f2_make(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), cs2, nm2), x0, x1);
+                const float p0 = ex2(x0), p1 = ex2(x1);
+                ph[c] = Elem<T>::pack(p0, p1);
+                const unsigned long long p2 = f2_make(p0, p1);
+                float r0, r1;
+                f2_split(f2_sub(p2, f2_make(lo16(ph[c], IsBf16()), hi16(ph[c], IsBf16()))), r0, r1);
+                pl[c] = Elem<T>::pack(r0, r1);
+                sm2[c & 3] = f2_add(sm2[c & 3], p2);
+            }
+            float sa, sb, sc, sd, se, sf, sg, sh;
+            f2_split(sm2[0], sa, sb);
+            f2_split(sm2[1], sc, sd);
+            f2_split(sm2[2], se, sf);
+            f2_split(sm2[3], sg, sh);
+            sum = ((sa + sb) + (sc + sd)) + ((se + sf) + (sg + sh));
+            }
             tc::st_x32(buf + 64 * hf, ph);
             tc::st_x32(buf + 64 * hf + 32, pl);
             // P_{j-1} V_{j-1} must be done before O is rescaled.
