@@ -717,58 +717,105 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
                     tc::fence_after_sync();
                     // The plan kernel's partial slots and the partition pass's pieces.
                     griddep_wait();
-                    // A sequence the plan found invalid has no slot of its own: nothing is written.
-                    const bool write = real && seq_len_valid(p.context_lens[rseq], p.q_len, L, p.max_context_len,
-                                                             p.max_blocks_per_seq);
-                    // The sequence's other pieces: partial slots part_start[i] + 1 .. (split-K
-                    // partitions), or without part_start the one suffix piece in slot i.
-                    const long long slot0 = !write ? 0 : p.part_start ? p.part_start[rseq] : rseq - 1;
                     const float l_pre = lsum[r] + lsum[kTcRows + r];
-                    // Merge the prefix piece (m_run, l_pre, O in TMEM) with the sequence's other
-                    // pieces, in slot order, by their log-sum-exp, and write the output row.
-                    const int npieces = !write ? 1 : p.part_start ? p.part_start[rseq + 1] - (int)slot0 : 2;
-                    const long long stride = (long long)p.q_len * p.num_heads;
-                    const long long prow0 = (slot0 * p.q_len + t) * p.num_heads + hq;
-                    float M = m_run;
-                    for (int c = 1; c < npieces; ++c) M = fmaxf(M, p.pml[prow0 + c * stride].x);
-                    const float f0 = ex2(m_run - M);
-                    float ltot = l_pre * f0;
-                    for (int c = 1; c < npieces; ++c) {
-                        const float2 ml = p.pml[prow0 + c * stride];
-                        ltot += ml.y * ex2(ml.x - M);
-                    }
-                    const float inv = 1.f / ltot;
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row_off) + hf * (D / 16);
+                    if (!p.part_start) {
+                        // One other piece per row, the suffix kernel's, in the row's own slot: the
+                        // sequence's length, the piece's (max, sum) and this thread's half of its
+                        // unnormalised output are loaded together, in one round trip.
+                        const int len = p.context_lens[rseq];
+                        const float2 ml = p.pml[row_id];
+                        const float4* src = reinterpret_cast<const float4*>(p.pacc + row_id * D) + hf * (D / 8);
+                        float4 pv[D / 8];
 #pragma unroll
-                    for (int h = 0; h < D / 64; ++h) {
-                        uint32_t o[32];
-                        tc::ld_x32(o_half + 32 * h, o);
-                        float acc[32];
+                        for (int e = 0; e < D / 8; ++e) pv[e] = src[e];
+                        // A sequence the plan found invalid has no slot of its own: nothing is written.
+                        const bool write = real && seq_len_valid(len, p.q_len, L, p.max_context_len, p.max_blocks_per_seq);
+                        const float M = write ? fmaxf(m_run, ml.x) : m_run;
+                        const float f0 = ex2(m_run - M);
+                        float ltot = l_pre * f0;
+                        const float fc = write ? ex2(ml.x - M) : 0.f;
+                        if (write) ltot += ml.y * fc;
+                        const float inv = 1.f / ltot;
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(o[e]) * f0;
-                        for (int c = 1; c < npieces; ++c) {
-                            const long long prow = prow0 + c * stride;
-                            const float fc = ex2(p.pml[prow].x - M);
-                            const float4* src = reinterpret_cast<const float4*>(p.pacc + prow * D) +
-                                                hf * (D / 8) + h * 8;
+                        for (int h = 0; h < D / 64; ++h) {
+                            uint32_t o[32];
+                            tc::ld_x32(o_half + 32 * h, o);
+                            float acc[32];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const float4 v = src[e];
-                                acc[4 * e] += v.x * fc;
-                                acc[4 * e + 1] += v.y * fc;
-                                acc[4 * e + 2] += v.z * fc;
-                                acc[4 * e + 3] += v.w * fc;
+                            for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(o[e]) * f0;
+                            if (write) {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const float4 v = pv[h * 8 + e];
+                                    acc[4 * e] += v.x * fc;
+                                    acc[4 * e + 1] += v.y * fc;
+                                    acc[4 * e + 2] += v.z * fc;
+                                    acc[4 * e + 3] += v.w * fc;
+                                }
+#pragma unroll
+                                for (int c = 0; c < 4; ++c) {
+                                    uint4 v;
+                                    v.x = Elem<T>::pack(acc[8 * c + 0] * inv, acc[8 * c + 1] * inv);
+                                    v.y = Elem<T>::pack(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv);
+                                    v.z = Elem<T>::pack(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv);
+                                    v.w = Elem<T>::pack(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv);
+                                    dst[h * 4 + c] = v;
+                                }
                             }
                         }
-                        if (write) {
+                    } else {
+                        // A sequence the plan found invalid has no slot of its own: nothing is written.
+                        const bool write = real && seq_len_valid(p.context_lens[rseq], p.q_len, L, p.max_context_len,
+                                                                 p.max_blocks_per_seq);
+                        // The sequence's other pieces: partial slots part_start[i] + 1 .. (split-K
+                        // partitions).
+                        const long long slot0 = !write ? 0 : p.part_start[rseq];
+                        // Merge the prefix piece (m_run, l_pre, O in TMEM) with the sequence's other
+                        // pieces, in slot order, by their log-sum-exp, and write the output row.
+                        const int npieces = !write ? 1 : p.part_start[rseq + 1] - (int)slot0;
+                        const long long stride = (long long)p.q_len * p.num_heads;
+                        const long long prow0 = (slot0 * p.q_len + t) * p.num_heads + hq;
+                        float M = m_run;
+                        for (int c = 1; c < npieces; ++c) M = fmaxf(M, p.pml[prow0 + c * stride].x);
+                        const float f0 = ex2(m_run - M);
+                        float ltot = l_pre * f0;
+                        for (int c = 1; c < npieces; ++c) {
+                            const float2 ml = p.pml[prow0 + c * stride];
+                            ltot += ml.y * ex2(ml.x - M);
+                        }
+                        const float inv = 1.f / ltot;
 #pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                uint4 v;
-                                v.x = Elem<T>::pack(acc[8 * c + 0] * inv, acc[8 * c + 1] * inv);
-                                v.y = Elem<T>::pack(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv);
-                                v.z = Elem<T>::pack(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv);
-                                v.w = Elem<T>::pack(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv);
-                                dst[h * 4 + c] = v;
+                        for (int h = 0; h < D / 64; ++h) {
+                            uint32_t o[32];
+                            tc::ld_x32(o_half + 32 * h, o);
+                            float acc[32];
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(o[e]) * f0;
+                            for (int c = 1; c < npieces; ++c) {
+                                const long long prow = prow0 + c * stride;
+                                const float fc = ex2(p.pml[prow].x - M);
+                                const float4* src = reinterpret_cast<const float4*>(p.pacc + prow * D) +
+                                                    hf * (D / 8) + h * 8;
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const float4 v = src[e];
+                                    acc[4 * e] += v.x * fc;
+                                    acc[4 * e + 1] += v.y * fc;
+                                    acc[4 * e + 2] += v.z * fc;
+                                    acc[4 * e + 3] += v.w * fc;
+                                }
+                            }
+                            if (write) {
+#pragma unroll
+                                for (int c = 0; c < 4; ++c) {
+                                    uint4 v;
+                                    v.x = Elem<T>::pack(acc[8 * c + 0] * inv, acc[8 * c + 1] * inv);
+                                    v.y = Elem<T>::pack(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv);
+                                    v.z = Elem<T>::pack(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv);
+                                    v.w = Elem<T>::pack(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv);
+                                    dst[h * 4 + c] = v;
+                                }
                             }
                         }
                     }
