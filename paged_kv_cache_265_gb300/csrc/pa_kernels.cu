@@ -88,7 +88,10 @@ __global__ void __launch_bounds__(256) reshape_kernel(const uint4* __restrict__ 
                                                       const long long* __restrict__ slots,
                                                       long long num_tokens, int row_vecs,
                                                       long long num_slots) {
+    // Launched under programmatic dependence: resident early, it touches no memory before the
+    // kernel ahead of it in the stream has finished.
     griddep_launch_dependents();
+    griddep_wait();
     const long long per_token = 2LL * row_vecs;
     const long long total = num_tokens * per_token;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
@@ -143,6 +146,7 @@ __global__ void __launch_bounds__(256) reshape_fp8_kernel(const uint4* __restric
                                                           int row_vecs, long long num_slots, float k_scale,
                                                           float v_scale) {
     griddep_launch_dependents();
+    griddep_wait();  // as in reshape_kernel
     const long long per_token = 2LL * row_vecs;  // 8 elements per vector
     const long long total = num_tokens * per_token;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
@@ -1625,13 +1629,15 @@ __device__ __forceinline__ void merge_body(const MergeParams& p, const PrefixGro
 
 template <typename T, int D>
 __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
-    griddep_wait();  // the partition pass must have finished
+    griddep_launch_dependents();  // the next call's append may be scheduled; it waits for this grid
+    griddep_wait();               // the partition pass must have finished
     merge_body<T, D>(p, nullptr);
 }
 
 // After a shared-prefix call's prefix kernel (which merges its own sequences): the others.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) merge_ungrouped_kernel(const MergeParams p, const __grid_constant__ PrefixGroups g) {
+    griddep_launch_dependents();
     griddep_wait();
     merge_body<T, D>(p, &g);
 }
@@ -2057,11 +2063,11 @@ int launch_reshape_and_cache(const void* key, const void* value, void* key_cache
     const long long total = (long long)num_tokens * 2 * row_vecs;
     const long long want = (total + 255) / 256;
     const int grid = (int)std::max(1LL, std::min<long long>(want, (long long)dev.sms * 8));
-    reshape_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-                                             static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache),
-                                             reinterpret_cast<const long long*>(slot_mapping), num_tokens,
-                                             row_vecs, num_slots);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_pdl(reshape_kernel, dim3(grid), dim3(256), 0, stream, static_cast<const uint4*>(key),
+                   static_cast<const uint4*>(value), static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache),
+                   reinterpret_cast<const long long*>(slot_mapping), (long long)num_tokens, row_vecs,
+                   (long long)num_slots) != cudaSuccess)
+        return PA_ERR_CUDA;
     *launches += 1;
     return PA_OK;
 }
@@ -2079,13 +2085,12 @@ int launch_reshape_and_cache_fp8(const void* key, const void* value, void* key_c
     auto* kc = static_cast<uint2*>(key_cache);
     auto* vc = static_cast<uint2*>(value_cache);
     const auto* sm = reinterpret_cast<const long long*>(slot_mapping);
-    if (dtype == PA_BF16)
-        reshape_fp8_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(k, v, kc, vc, sm, num_tokens, row_vecs, num_slots,
-                                                                    k_scale, v_scale);
-    else
-        reshape_fp8_kernel<__half><<<grid, 256, 0, stream>>>(k, v, kc, vc, sm, num_tokens, row_vecs, num_slots,
-                                                             k_scale, v_scale);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    const cudaError_t le =
+        dtype == PA_BF16 ? launch_pdl(reshape_fp8_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, stream, k, v, kc, vc,
+                                      sm, (long long)num_tokens, row_vecs, (long long)num_slots, k_scale, v_scale)
+                         : launch_pdl(reshape_fp8_kernel<__half>, dim3(grid), dim3(256), 0, stream, k, v, kc, vc, sm,
+                                      (long long)num_tokens, row_vecs, (long long)num_slots, k_scale, v_scale);
+    if (le != cudaSuccess) return PA_ERR_CUDA;
     *launches += 1;
     return PA_OK;
 }
