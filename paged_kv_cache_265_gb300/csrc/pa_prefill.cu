@@ -643,41 +643,41 @@ __device__ __forceinline__ void tc_attention(const PrefillTcParams& p, const Pre
             uint32_t ph[32], pl[32];  // P_hi and P_lo of positions 64 hf .., two weights per register
             float sum;
             if constexpr (((PA_TC_PACKED_MODES >> kMode) & 1) == 0) {
-            float sm[8];
+                float sm[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) sm[u] = 0.f;
+                for (int u = 0; u < 8; ++u) sm[u] = 0.f;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), cs, -msub));
-                const float p1 = ex2(fmaf(__uint_as_float(sv[2 * c + 1]), cs, -msub));
-                ph[c] = Elem<T>::pack(p0, p1);
-                pl[c] = Elem<T>::pack(p0 - lo16(ph[c], IsBf16()), p1 - hi16(ph[c], IsBf16()));
-                sm[c & 7] += p0 + p1;
-            }
-            sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+                for (int c = 0; c < 32; ++c) {
+                    const float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), cs, -msub));
+                    const float p1 = ex2(fmaf(__uint_as_float(sv[2 * c + 1]), cs, -msub));
+                    ph[c] = Elem<T>::pack(p0, p1);
+                    pl[c] = Elem<T>::pack(p0 - lo16(ph[c], IsBf16()), p1 - hi16(ph[c], IsBf16()));
+                    sm[c & 7] += p0 + p1;
+                }
+                sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
             } else {
-            // Weights two at a time in packed fp32 pairs: one FFMA, one residual subtraction and
-            // one accumulation per pair.
-            const unsigned long long cs2 = f2_make(cs, cs), nm2 = f2_make(-msub, -msub);
-            unsigned long long sm2[4] = {0ull, 0ull, 0ull, 0ull};
+                // Weights two at a time in packed fp32 pairs: one FFMA, one residual subtraction and
+                // one accumulation per pair.
+                const unsigned long long cs2 = f2_make(cs, cs), nm2 = f2_make(-msub, -msub);
+                unsigned long long sm2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                float x0, x1;
-                f2_split(f2_fma(f2_make(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), cs2, nm2), x0, x1);
-                const float p0 = ex2(x0), p1 = ex2(x1);
-                ph[c] = Elem<T>::pack(p0, p1);
-                const unsigned long long p2 = f2_make(p0, p1);
-                float r0, r1;
-                f2_split(f2_sub(p2, f2_make(lo16(ph[c], IsBf16()), hi16(ph[c], IsBf16()))), r0, r1);
-                pl[c] = Elem<T>::pack(r0, r1);
-                sm2[c & 3] = f2_add(sm2[c & 3], p2);
-            }
-            float sa, sb, sc, sd, se, sf, sg, sh;
-            f2_split(sm2[0], sa, sb);
-            f2_split(sm2[1], sc, sd);
-            f2_split(sm2[2], se, sf);
-            f2_split(sm2[3], sg, sh);
-            sum = ((sa + sb) + (sc + sd)) + ((se + sf) + (sg + sh));
+                for (int c = 0; c < 32; ++c) {
+                    float x0, x1;
+                    f2_split(f2_fma(f2_make(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), cs2, nm2), x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    ph[c] = Elem<T>::pack(p0, p1);
+                    const unsigned long long p2 = f2_make(p0, p1);
+                    float r0, r1;
+                    f2_split(f2_sub(p2, f2_make(lo16(ph[c], IsBf16()), hi16(ph[c], IsBf16()))), r0, r1);
+                    pl[c] = Elem<T>::pack(r0, r1);
+                    sm2[c & 3] = f2_add(sm2[c & 3], p2);
+                }
+                float sa, sb, sc, sd, se, sf, sg, sh;
+                f2_split(sm2[0], sa, sb);
+                f2_split(sm2[1], sc, sd);
+                f2_split(sm2[2], se, sf);
+                f2_split(sm2[3], sg, sh);
+                sum = ((sa + sb) + (sc + sd)) + ((se + sf) + (sg + sh));
             }
             tc::st_x32(buf + 64 * hf, ph);
             tc::st_x32(buf + 64 * hf + 32, pl);
