@@ -110,3 +110,53 @@ def ulps_from_rounded_oracle(gpu_bits: np.ndarray, ref: np.ndarray, dtype: str, 
     r = np.where(r & 0x8000, 0x8000 - r, r)
     big = np.abs(ref) >= floor
     return int(np.abs(g - r)[big].max(initial=0))
+
+
+def from_f64(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round to the 16-bit type (nearest even) and return the bit patterns."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64)).to(TORCH_DT[dtype])
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def rising_scores_workload(dtype: str, seed: int = 77, gain: float = 8.0) -> W.Workload:
+    """A GQA 32/8, d = 128 batch whose scores move steadily instead of staying in a narrow band,
+    so that an online softmax keeps meeting scores above its running max.  Every key is a small
+    random part plus a(p) times the unit direction of the sum of its kv head's query rows, and the
+    queries are scaled by `gain`.  a(p), per sequence: rising from -10 to 10 over 3000 positions
+    (scores from about -42..-63 to +42..+63 in log2 units, +0.3..0.5 per block: a max that passes
+    the previous one by more than 8 every 12-19 blocks, with weights up to nearly 2^8 against the
+    old max in between), falling from 10 to -10 over 1700 (the first block holds the max; later
+    weights underflow), a step from -10 to 10 at position 407 of 650 (a jump of about 136 inside
+    a block, after 25 blocks), and rising over 40.  The gain keeps |scores| below about 70: at
+    gain 41 (|scores| up to 220) the fp32 rounding of the scores alone moves fp16 outputs by up
+    to 1.4e-3 relative, more than one unit in the last place."""
+    lens = [3000, 1700, 650, 40]
+    hq, hkv, d = 32, 8, 128
+    g = hq // hkv
+    w = W.make_workload(f"rising_{dtype}", lens, num_heads=hq, num_kv_heads=hkv, head_dim=d, dtype=dtype,
+                        q_len=1, seed=seed, keep_logical=True)
+    q = bits_to_f64(w.query.ravel(), dtype).reshape(w.query.shape) * gain
+    qbits = from_f64(q, dtype).reshape(w.query.shape)
+    q = bits_to_f64(qbits.ravel(), dtype).reshape(w.query.shape)
+    key_cache = w.key_cache.reshape(-1, hkv, d).copy()
+    new_key = w.new_key.copy()
+    for i, L in enumerate(lens):
+        p = np.arange(L, dtype=np.float64)
+        if i == 0 or i == 3:
+            a = -10.0 + 20.0 * p / (L - 1)
+        elif i == 1:
+            a = 10.0 - 20.0 * p / (L - 1)
+        else:
+            a = np.where(p < 407, -10.0, 10.0)
+        u = q[i, 0].reshape(hkv, g, d).sum(axis=1)
+        u /= np.linalg.norm(u, axis=1, keepdims=True)
+        k = 0.05 * bits_to_f64(w.logical_key[i].ravel(), dtype).reshape(L, hkv, d) + a[:, None, None] * u[None]
+        kb = from_f64(k, dtype).reshape(L, hkv, d)
+        slots = w.block_tables[i, np.arange(L) // w.block_size].astype(np.int64) * w.block_size + np.arange(L) % w.block_size
+        key_cache[slots[:L - 1]] = kb[:L - 1]
+        new_key[i] = kb[L - 1]
+    assert np.array_equal(w.slot_mapping, [w.block_tables[i, (L - 1) // w.block_size] * w.block_size
+                                           + (L - 1) % w.block_size for i, L in enumerate(lens)])
+    import dataclasses
+    return dataclasses.replace(w, query=qbits, key_cache=key_cache.reshape(w.key_cache.shape), new_key=new_key,
+                               logical_key=None, logical_value=None)

@@ -77,6 +77,16 @@ def test_fp8_partitions_and_edges(partition):
     G.compare(got, ref, w.dtype, f"fp8 partition {partition}")
 
 
+@pytest.mark.parametrize("partition", [0, 32])
+def test_fp8_rising_falling_and_jumping_scores(partition):
+    """Scores that keep passing the running max, fall, or jump inside a block, over an FP8 cache
+    (keys up to about 10, within E4M3's range at the test's k_scale)."""
+    w = G.rising_scores_workload("bf16")
+    got, ref = run_fp8(w, partition)
+    G.compare(got, ref, w.dtype, f"{w.name} fp8 partition {partition}")
+    assert pa.get_device_error(clear=True) == 0
+
+
 def test_fp8_head_dim_64_is_unsupported():
     q = torch.empty((2, 4, 64), dtype=torch.bfloat16, device="cuda")
     kc = torch.empty((4, 16, 4, 64), dtype=torch.uint8, device="cuda")

@@ -81,6 +81,22 @@ EDGE = [
 ]
 
 
+@pytest.mark.parametrize("partition", [0, 32])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_rising_falling_and_jumping_scores(dtype, partition):
+    """Scores that keep passing the running max every few blocks, that fall from the first block
+    on, or that jump inside a block: the online softmax's rescaling paths, held to the same bar
+    as the named workloads (with and without a split into 32-token partitions)."""
+    w = G.rising_scores_workload(dtype)
+    step = G.GpuStep(w, partition_size=partition)
+    got = step.run()
+    kc, _, ref = G.oracle_step(w)
+    assert np.array_equal(G.to_bits(step.key_cache), kc)
+    G.compare(got, ref, dtype, f"{w.name} partition {partition}")
+    assert G.ulps_from_rounded_oracle(got, ref, dtype) <= 1
+    assert pa.get_device_error(clear=True) == 0
+
+
 @pytest.mark.parametrize("case", range(len(EDGE)))
 def test_edge_shapes(case):
     lens, hq, hkv, d, q_len, dt = EDGE[case]
