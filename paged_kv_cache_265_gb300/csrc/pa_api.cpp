@@ -236,7 +236,6 @@ int pa_decode_attention_fp8kv(void* out, const void* query, const void* key_cach
                                    max_context_len, scale, dtype, partition_size, workspace);
     const size_t need = pa::ws_layout(num_seqs, q_len, num_heads, head_dim, max_context_len, a.partition).total;
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
-    a.partition_auto = false;  // FP8 caches keep the default split unless the caller chooses one
     a.fp8 = true;
     a.k_scale = k_scale;
     a.v_scale = v_scale;

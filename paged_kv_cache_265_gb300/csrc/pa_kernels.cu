@@ -1860,9 +1860,9 @@ void decode_variant(int rows, bool fp8, int& rt, int& nt) {
 // the largest-first hand-out keeps the tail short while units are plentiful.  Measured on GB300
 // (call time): GQA batch of 128, 512 / 1024 / 2048 tokens: 181.7 / 177.6 / - us; long context
 // (16 sequences of 16-32K + 240 short): 408.6 / 376.5 / 357.3 us (4096: 397.9); OPT-13B-shaped
-// MHA: 156.2 / 158.7 / 182.4 us; 32 GQA sequences: 68.1 / 68.3 / 92.2 us.
+// MHA: 156.2 / 158.7 / 182.4 us; 32 GQA sequences: 68.1 / 68.3 / 92.2 us.  The same rule for an
+// FP8 cache; GQA batch of 128, partition kernel, 512 / 1024 / 2048 tokens: 130.5 / 126.5 / 141.3 us.
 int auto_partition(const DecodeArgs& a, int sms) {
-    if (a.fp8) return PA_DEFAULT_PARTITION;
     const int group = a.num_heads / a.num_kv_heads;
     const long long total_rows = (long long)group * a.q_len;
     const int rows = (int)std::min<long long>(PA_ROW_GROUP_ROWS, total_rows);
