@@ -123,11 +123,11 @@ def rising_scores_workload(dtype: str, seed: int = 77, gain: float = 8.0) -> W.W
     so that an online softmax keeps meeting scores above its running max.  Every key is a small
     random part plus a(p) times the unit direction of the sum of its kv head's query rows, and the
     queries are scaled by `gain`.  a(p), per sequence: rising from -10 to 10 over 3000 positions
-    (scores from about -42..-63 to +42..+63 in log2 units, +0.3..0.5 per block: a max that passes
-    the previous one by more than 8 every 12-19 blocks, with weights up to nearly 2^8 against the
-    old max in between), falling from 10 to -10 over 1700 (the first block holds the max; later
-    weights underflow), a step from -10 to 10 at position 407 of 650 (a jump of about 136 inside
-    a block, after 25 blocks), and rising over 40.  The gain keeps |scores| below about 70: at
+    (scores from about -42..-63 to +42..+63 in log2 units, +0.3..0.5 per block: every query row's
+    max passes the previous one by more than 8 on 10-18 blocks, with weights up to nearly 2^8
+    against the old max in between), falling from 10 to -10 over 1700 (the first block holds the
+    max; later weights underflow), a step from -10 to 10 at position 407 of 650 (a jump of 68-148
+    inside a block, after 25 blocks), and rising over 40.  The gain keeps |scores| below 90: at
     gain 41 (|scores| up to 220) the fp32 rounding of the scores alone moves fp16 outputs by up
     to 1.4e-3 relative, more than one unit in the last place."""
     lens = [3000, 1700, 650, 40]

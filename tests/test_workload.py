@@ -61,3 +61,39 @@ def test_length_recipe_bounds_and_seed():
     assert not np.array_equal(a, W._uniform_lens(2654, 128, 1, 4096))
     q = W.make_workload("q", [3, 9], num_heads=2, num_kv_heads=2, head_dim=64, seed=1).query
     assert q.dtype == np.uint16 and q.shape == (2, 1, 2, 64)
+
+
+def test_rising_scores_case_moves_the_running_max():
+    """The GPU parity case with moving scores does what it is there for: in the rising sequence every
+    query row sees its block maximum pass the running maximum by more than 8 (log2 units) many times,
+    with blocks in between whose scores sit nearly 8 above it; the falling sequence never moves it after
+    its first block; the step sequence jumps by more than 60 inside block 25; and no score is large
+    enough for fp32 rounding of the scores to cost fp16 a unit in the last place (|s| < 90)."""
+    import math
+
+    import gpu_helpers as G
+
+    w = G.rising_scores_workload("bf16")
+    q = G.bits_to_f64(w.query.ravel(), "bf16").reshape(w.query.shape)
+    pool = G.bits_to_f64(w.key_cache.ravel(), "bf16").reshape(-1, w.num_kv_heads, w.head_dim)
+    new = G.bits_to_f64(w.new_key.ravel(), "bf16").reshape(w.new_key.shape)
+    g = w.num_heads // w.num_kv_heads
+    for i, L in enumerate(w.context_lens.tolist()):
+        p = np.arange(L - 1)
+        keys = np.concatenate([pool[w.block_tables[i, p // 16].astype(np.int64) * 16 + p % 16], new[i][None]])
+        for h in range(w.num_heads):
+            s = keys[:, h // g] @ q[i, 0, h] * w.scale / math.log(2)
+            assert np.abs(s).max() < 90
+            block_max = [s[j:j + 16].max() for j in range(0, L, 16)]
+            m, moves, near = -np.inf, 0, 0
+            for b in block_max:
+                if b > m + 8:
+                    m, moves = b, moves + 1
+                elif b > m + 6:
+                    near += 1
+            if i == 0:
+                assert moves >= 8 and near >= 20, (h, moves, near)
+            if i == 1:
+                assert moves == 1, (h, moves)
+            if i == 2:
+                assert s[407:416].min() - s[400:407].max() > 60
